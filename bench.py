@@ -1,0 +1,387 @@
+"""Benchmark: decode attention over an int8 paged KV cache at 128K context on
+one GB300 (batch 1, 16 query heads / 2 KV heads, head_dim 256, page 16,
+shuffled page table, bf16 N(0,1) inputs with four x20 K outlier channels).
+
+One step = quantize-on-write append of the step's new token (K and V) into the
+cache + split-K decode attention over all 131072 cached tokens. Eight
+independent layer caches (1.1 GB, well above the 129 MB L2) are cycled so no
+step reads another's data from L2.
+
+Prints one JSON line (rank 0). `--impl reference` times the CPU oracle on the
+same workload instead (the reference arm).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn packed-KV HBM GB/s (% of peak) and steps/s at 128K ctx, 1 GB300"
+B, HQ, HKV, D, L = 1, 16, 2, 256, 131072
+LAYERS = 8
+KV_BYTES_PER_TOKEN = 2 * HKV * (D + 2 * D // 64)        # int8 codes + fp16 scales, K and V: 1056
+DECODE_BYTES = L * KV_BYTES_PER_TOKEN                     # 138,412,032 packed bytes read per step
+WORKLOAD = ("int8 KV decode at 128K context: batch 1, 16 q heads / 2 KV heads, head_dim 256, "
+            "131072 cached tokens, page 16, shuffled page table; step = append 1 token + decode")
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def _clock_sampler():
+    f = tempfile.NamedTemporaryFile(prefix="qkv_clk", suffix=".csv", delete=False)
+    q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+    try:
+        p = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits", "-lms", "100"],
+                             stdout=f, stderr=subprocess.DEVNULL)
+    except OSError:
+        return None, f.name
+    return p, f.name
+
+
+def _clock_summary(proc, path, gpu_index):
+    if proc is None:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+    proc.terminate()
+    try:
+        proc.wait(timeout=5)
+    except subprocess.TimeoutExpired:
+        proc.kill()
+    sm, smax, reasons = [], None, set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in open(path):
+        parts = [x.strip() for x in line.split(",")]
+        if len(parts) < 9 or not parts[0].isdigit() or int(parts[0]) != gpu_index:
+            continue
+        try:
+            sm.append(float(parts[1]))
+            smax = float(parts[2])
+        except ValueError:
+            continue
+        for nm, v in zip(names, parts[5:9]):
+            if v.lower() == "active":
+                reasons.add(nm)
+    os.unlink(path)
+    return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax, "reasons": sorted(reasons),
+            "samples": len(sm)}
+
+
+_INPUT_CACHE = {}
+
+
+def _inputs(seed=0):
+    if seed in _INPUT_CACHE:
+        return _INPUT_CACHE[seed]
+    from quantized_paged_kv_append_gb300 import synth
+    pages = (L + 15) // 16
+    k = synth.tensor_bf16(seed, "k", (L, HKV, D), outlier_scale=20.0)
+    v = synth.tensor_bf16(seed, "v", (L, HKV, D))
+    q = synth.tensor_bf16(seed, "q", (LAYERS, B, HQ, D))
+    kn = synth.tensor_bf16(seed, "k_new", (LAYERS, 1, HKV, D), outlier_scale=20.0)
+    vn = synth.tensor_bf16(seed, "v_new", (LAYERS, 1, HKV, D))
+    tables = [synth.page_table(seed * 100 + layer, [pages])[0] for layer in range(LAYERS)]
+    _INPUT_CACHE[seed] = (pages, k, v, q, kn, vn, tables)
+    return _INPUT_CACHE[seed]
+
+
+# ---------------------------------------------------------------------------
+# CUDA arm
+# ---------------------------------------------------------------------------
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import quantized_paged_kv_append_gb300 as qkv
+    from quantized_paged_kv_append_gb300 import build as qbuild
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    if rank == 0:
+        qbuild.build()
+    if world > 1:
+        dist.barrier()
+    qbuild.build()  # no-op when up to date
+    dev = torch.device("cuda", local)
+
+    pages, k, v, q, kn, vn, tables = _inputs(args.seed)
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+    k_d, v_d = bf(k), bf(v)
+    seq_all = i32(np.zeros(L, np.int32))
+    pos_all = i32(np.arange(L, dtype=np.int32))
+    caches, tabs = [], []
+    for layer in range(LAYERS):
+        c = qkv.PagedKVCache("int8", pages, HKV, D, device=dev)
+        t = i32(tables[layer])
+        qkv.append(c, k_d, v_d, seq_all, pos_all, t)   # fill the cache (quantize-on-write of all tokens)
+        caches.append(c)
+        tabs.append(t)
+    del k_d, v_d
+    q_d = bf(q)                       # [LAYERS, 1, HQ, D]
+    kn_d, vn_d = bf(kn), bf(vn)       # [LAYERS, 1, HKV, D]
+    seq1 = i32(np.zeros(1, np.int32))
+    pos1 = i32(np.array([L - 1], np.int32))
+    lens = i32(np.array([L], np.int32))
+    out = torch.empty((B, HQ, D), dtype=torch.bfloat16, device=dev)
+    ws = qkv.decode_workspace(caches[0], B, HQ, L, device=dev)
+    scale = 1.0 / math.sqrt(D)
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+    assert qkv.device_error() == 0
+
+    def step(i, ev=None):
+        layer = i % LAYERS
+        qkv.append(caches[layer], kn_d[layer], vn_d[layer], seq1, pos1, tabs[layer], stream=stream)
+        if ev is not None:
+            ev[0].record(stream)
+        qkv.decode(caches[layer], q_d[layer], tabs[layer], lens, L, scale=scale, out=out, workspace=ws, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    # warm-up (eager), then capture K steps into one graph with per-decode events
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+    stream.synchronize()
+    def timing_event():
+        try:
+            return torch.cuda.Event(enable_timing=True, external=True)
+        except TypeError:
+            return torch.cuda.Event(enable_timing=True)
+
+    # one graph of K steps; each decode launch bracketed by event-record nodes so the
+    # decode kernel's own duration is measured inside the timed region
+    evs = [(timing_event(), timing_event()) for _ in range(args.steps)]
+    per_launch = True
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(args.steps):
+                step(i, evs[i])
+        graph.replay()
+        stream.synchronize()
+        _ = evs[0][0].elapsed_time(evs[0][1])
+    except Exception:
+        per_launch = False
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(args.steps):
+                step(i)
+        graph.replay()
+        stream.synchronize()
+    if not per_launch:
+        # decode-only graph: average launch duration = graph time / K
+        dgraph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(dgraph, stream=stream):
+            for i in range(args.steps):
+                layer = i % LAYERS
+                qkv.decode(caches[layer], q_d[layer], tabs[layer], lens, L, scale=scale, out=out, workspace=ws,
+                           stream=stream)
+        dgraph.replay()
+        stream.synchronize()
+
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    proc, cpath = _clock_sampler()
+    time.sleep(0.3)
+    reps = max(1, args.reps)
+    t0.record(stream)
+    for _ in range(reps):
+        graph.replay()
+    t1.record(stream)
+    t1.synchronize()
+    if per_launch:
+        dec_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)   # last replay's launches
+    else:
+        d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        d0.record(stream)
+        dgraph.replay()
+        d1.record(stream)
+        d1.synchronize()
+        dec_ms = d0.elapsed_time(d1) / args.steps
+    torch.cuda.synchronize()
+    clocks = _clock_summary(proc, cpath, local)
+    total_ms = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    nsteps = args.steps * reps
+    ms_per_step = total_ms / nsteps
+    value = DECODE_BYTES * nsteps * world / (total_ms / 1e3) / 1e9
+
+    # end to end through the public API with host buffers (pinned), copies inside the timed region
+    h_q = torch.from_numpy(np.ascontiguousarray(q[0]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_kn = torch.from_numpy(np.ascontiguousarray(kn[0]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_vn = torch.from_numpy(np.ascontiguousarray(vn[0]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_meta = torch.tensor([0, L - 1, L], dtype=torch.int32).pin_memory()
+    h_out = torch.empty((B, HQ, D), dtype=torch.bfloat16).pin_memory()
+    d_q, d_kn, d_vn = torch.empty_like(q_d[0]), torch.empty_like(kn_d[0]), torch.empty_like(vn_d[0])
+    d_meta = torch.empty(3, dtype=torch.int32, device=dev)
+    h2d = h_q.numel() * 2 + h_kn.numel() * 2 + h_vn.numel() * 2 + h_meta.numel() * 4
+    d2h = h_out.numel() * 2
+
+    def e2e_step(i):
+        layer = i % LAYERS
+        d_q.copy_(h_q, non_blocking=True)
+        d_kn.copy_(h_kn, non_blocking=True)
+        d_vn.copy_(h_vn, non_blocking=True)
+        d_meta.copy_(h_meta, non_blocking=True)
+        qkv.append(caches[layer], d_kn, d_vn, d_meta[0:1], d_meta[1:2], tabs[layer], stream=stream)
+        qkv.decode(caches[layer], d_q, tabs[layer], d_meta[2:3], L, scale=scale, out=out, workspace=ws, stream=stream)
+        h_out.copy_(out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            e2e_step(i)
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        w0 = time.perf_counter()
+        e0.record(stream)
+        for i in range(args.steps):
+            e2e_step(i)
+        e1.record(stream)
+        e1.synchronize()
+        wall = time.perf_counter() - w0
+    e2e_ms = max(e0.elapsed_time(e1), wall * 1e3) / args.steps
+    assert qkv.device_error() == 0
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    peak, peak_kind = peaks()
+    dec_gbs = DECODE_BYTES / (dec_ms / 1e3) / 1e9
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": nsteps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+        "data": "synthetic (seeded splitmix64 + Box-Muller, bf16)",
+        "config": {"workload": WORKLOAD, "batch": B, "q_heads": HQ, "kv_heads": HKV, "head_dim": D,
+                   "context": L, "page_size": 16, "format": "int8", "layer_copies": LAYERS,
+                   "l2": "inputs larger than L2: 8 layer caches (1.1 GB) cycled", "parallelism": f"replicas x{world}"},
+        "steps_per_s": round(1e3 / ms_per_step, 1),
+        "pct_of_peak": round(100.0 * value / peak, 2),
+        "decode_us": round(dec_ms * 1e3, 2),
+        "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(dec_gbs / peak, 4), "traffic": None, "peak_kind": peak_kind,
+                     "kernel": "decode_kernel<int8,int8,256,8>", "bytes_per_launch": DECODE_BYTES,
+                     "timing": "events around each launch in the timed graph" if per_launch
+                     else "decode-only graph time / launches"},
+        "e2e": {"value": round(DECODE_BYTES / (e2e_ms / 1e3) / 1e9, 1), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * nsteps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        res["cpu_baseline"] = cpu_baseline(args, quick=True)
+    print(json.dumps(res))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline / reference arm)
+# ---------------------------------------------------------------------------
+def _oracle_workload(seed):
+    import oracle
+    oracle.build()
+    pages, k, v, q, kn, vn, tables = _inputs(seed)
+    pool = oracle.Pool(0, pages, HKV, D)
+    seq = np.zeros(L, np.int32)
+    pos = np.arange(L, dtype=np.int32)
+    pool.append(k, v, seq, pos, tables[0])
+    return oracle, pool, q, kn, vn, tables
+
+
+def _oracle_step(pool, q, kn, vn, table, layer):
+    pool.append(kn[layer], vn[layer], np.zeros(1, np.int32), np.array([L - 1], np.int32), table)
+    return pool.decode(q[layer], table, np.array([L], np.int32), float(np.float32(1 / math.sqrt(D))))
+
+
+def cpu_baseline(args, quick=False, steps=None, warmup=0):
+    oracle, pool, q, kn, vn, tables = _oracle_workload(args.seed)
+    for i in range(warmup):
+        _oracle_step(pool, q, kn, vn, tables[0], i % LAYERS)
+    n = steps if steps is not None else (2 if quick else 3)
+    t0 = time.perf_counter()
+    for i in range(n):
+        _oracle_step(pool, q, kn, vn, tables[0], i % LAYERS)
+    dt = time.perf_counter() - t0
+    return {"value": round(DECODE_BYTES * n / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} full steps (append 1 token + decode over 131072 tokens), single thread, "
+                      f"{dt / n:.2f} s per step"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    oracle, pool, q, kn, vn, tables = _oracle_workload(args.seed)
+    for i in range(args.warmup):
+        _oracle_step(pool, q, kn, vn, tables[0], i % LAYERS)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        _oracle_step(pool, q, kn, vn, tables[0], i % LAYERS)
+    dt = time.perf_counter() - t0
+    ms = dt * 1e3 / args.steps
+    value = DECODE_BYTES / (ms / 1e3) / 1e9
+    res = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic (seeded splitmix64 + Box-Muller, bf16)",
+           "config": {"workload": WORKLOAD, "batch": B, "q_heads": HQ, "kv_heads": HKV, "head_dim": D,
+                      "context": L, "page_size": 16, "format": "int8", "parallelism": "none (host CPU)"},
+           "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                            "sample": f"{args.steps} full steps (append 1 token + decode over 131072 tokens)"},
+           "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(res))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--reps", type=int, default=5, help="graph replays of the K captured steps")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        if args.steps > 10:
+            args.steps = 10   # each oracle step is seconds of CPU work
+        args.warmup = min(args.warmup, 1)
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,169 @@
+/*
+ * qkv.h -- C ABI of the GB300 quantized paged KV-cache library (libqkv.so).
+ *
+ * Three operations make up the path:
+ *   iso_kv_append   quantize-on-write of new K/V tokens into a paged pool
+ *   kv_decode_attn  paged split-K decode attention with on-the-fly dequant
+ *                   and the partial-softmax merge
+ *   kv_extend_attn  prefill-chunk attention over a packed prefix plus the
+ *                   chunk's own bf16 K/V (packed afterwards by iso_kv_append)
+ *
+ * Sources (page title, section):
+ *   [FT] "feat(kvcache): add ISO3/ISO4 KV-cache quantization (--kv-cache-iso)":
+ *        "What" (ISO3/ISO4 blocks, quantize-on-write decode, deferred packing in
+ *        extend), "Caveats" (bf16 KV input, head_dim % 128 == 0, validated at
+ *        configuration time).
+ *   [S8] "qwen35/q36: --kv - int8 K/V caches (codes + a FP16 scale per 64
+ *        values)": "What it does" (int8 codes + one fp16 scale per 64 values,
+ *        separate code and scale buffers, head_dim a multiple of 64, a format
+ *        dispatcher, decode splits and on-the-fly dequant).
+ *   [K4] "--kv k8v4: hybrid KV cache -- INT8 K + Hadamard-rotated Q4_0 V": "What",
+ *        "How" (separate K/V pointers, V and the output Hadamard-rotated, q not),
+ *        "Tests" (non-identity page table, ties-to-even int8 rules).
+ *
+ * Conventions common to every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller. The library
+ *     allocates no memory and never synchronizes the stream. `stream` is a
+ *     cudaStream_t (NULL = legacy default stream).
+ *   - Arguments are validated on the host before any launch; an invalid call
+ *     returns a negative QKV_ERR_* code and launches nothing. No C++ exception
+ *     crosses this interface. Device-side range checks (page-table entries,
+ *     positions) never trap: the offending token or page is skipped and a bit
+ *     is set in a device error word read by qkv_device_error().
+ *   - bf16 tensors are little-endian IEEE bfloat16; fp16 scales are IEEE
+ *     binary16.
+ *   - Page size is 16 tokens. A token at position `pos` of sequence `b` lives
+ *     in physical page page_table[b * max_pages_per_seq + pos / 16], slot
+ *     pos % 16. page_table is int32, row-major [batch][max_pages_per_seq].
+ */
+#ifndef QKV_H_
+#define QKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define QKV_API __attribute__((visibility("default")))
+#else
+#define QKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* KV formats [S8 "What it does"; K4 "What"; FT "What"]. */
+typedef enum {
+    QKV_INT8 = 0, /* K and V: int8 codes + fp16 scale (group absmax/127) per 64 values     */
+    QKV_K8V4 = 1, /* K as QKV_INT8; V: FWHT-256 (x1/16) then q4_0 per 32 values; D = 256   */
+    QKV_ISO3 = 2, /* K and V: per 128 values, 3-bit Lloyd-Max codes (48 B) + fp16 norm    */
+    QKV_ISO4 = 3  /* K and V: per 128 values, 4-bit codes (64 B) + fp16 norm + 2 B reserved */
+} qkv_format;
+
+typedef enum { QKV_OUT_BF16 = 0, QKV_OUT_F32 = 1 } qkv_out_dtype;
+
+enum {
+    QKV_OK = 0,
+    QKV_ERR_ARG = -1,        /* null pointer, negative size, bad page size, ...          */
+    QKV_ERR_HEAD_DIM = -2,   /* head_dim not supported by the format                     */
+    QKV_ERR_GQA = -3,        /* num_q_heads not a supported multiple of num_kv_heads     */
+    QKV_ERR_WORKSPACE = -4,  /* workspace pointer null or smaller than *_workspace_size   */
+    QKV_ERR_FORMAT = -5,     /* unknown format enum                                       */
+    QKV_ERR_CUDA = -6,       /* a CUDA runtime call failed; see qkv_last_cuda_error()     */
+    QKV_ERR_DEVICE = -7,     /* a device-side range check fired (qkv_device_error)        */
+    QKV_ERR_UNSUPPORTED = -8 /* valid request outside what this build implements          */
+};
+
+/*
+ * Pool descriptor. The four planes are caller-owned device buffers laid out
+ * [num_pages][num_kv_heads][page_size][row bytes] with the row bytes of
+ * qkv_row_bytes(). Plane contents per format (element order within a row):
+ *   int8 codes : int8, one per value; scales: fp16 per 64 values.
+ *   q4 codes   : per 32-value block 16 bytes, byte j = value j (low nibble) |
+ *                value j+16 (high nibble); scales: signed fp16 d per block.
+ *   iso3 codes : per 128-value block 48 bytes: bytes 0..31 hold the low two
+ *                code bits (value i at byte i/4, bits 2*(i%4)); bytes 32..47
+ *                the high bit (value i at byte 32 + i/8, bit i%8);
+ *                scales: fp16 corrected norm per block.
+ *   iso4 codes : per block 64 bytes, value i at byte i/2 (low nibble if i even);
+ *                scales: per block fp16 corrected norm followed by a reserved
+ *                fp16 written as 0 (68 B per block in total).
+ * `quat` is the fixed unit quaternion (w, x, y, z) of the ISO formats; it is
+ * ignored by the other formats. Buffers must be 16-byte aligned.
+ */
+typedef struct {
+    int32_t format;       /* qkv_format                                  */
+    int32_t num_pages;    /* physical pages in the pool                  */
+    int32_t page_size;    /* must be 16                                  */
+    int32_t num_kv_heads;
+    int32_t head_dim;     /* int8: 128 or 256; k8v4: 256; iso: 128 or 256 */
+    int32_t reserved0;
+    void* k_codes;
+    void* k_scales;
+    void* v_codes;
+    void* v_scales;
+    float quat[4];
+} qkv_cache_desc;
+
+/* Bytes of codes and of scales in one row (one token, one KV head) of store
+ * `store` (0 = K, 1 = V) for a format and head_dim. Host only. */
+QKV_API int qkv_row_bytes(int format, int store, int head_dim, int* code_bytes, int* scale_bytes);
+
+/* The fp16-rounded Lloyd-Max levels (ascending, as fp32) that this library
+ * uses for ISO3 (bits = 3, 8 levels) or ISO4 (bits = 4, 16 levels), computed by
+ * its own host code for N(0, 1/128). Returns the level count. Host only. */
+QKV_API int qkv_iso_levels(int bits, float* levels);
+
+/*
+ * iso_kv_append -- quantize-on-write [FT "What"; S8 "What it does"].
+ * k, v: bf16 [n_tokens][num_kv_heads][head_dim]. seq_id, pos: int32
+ * [n_tokens]. Token n is quantized per the descriptor's format and written to
+ * page_table[seq_id[n] * max_pages_per_seq + pos[n] / 16], slot pos[n] % 16,
+ * for every KV head, K and V. page_table has num_seqs rows. A token whose
+ * seq_id is outside [0, num_seqs), whose pos is outside
+ * [0, 16 * max_pages_per_seq), or whose page entry is outside [0, num_pages)
+ * is skipped and flags the device error word. n_tokens == 0 is a no-op.
+ * The bytes written are a deterministic function of the bf16 inputs (fixed
+ * fp32 operation order, IEEE division and square root, no contraction).
+ */
+QKV_API int iso_kv_append(const qkv_cache_desc* cache, const void* k, const void* v, int n_tokens,
+                  const int32_t* seq_id, const int32_t* pos, const int32_t* page_table,
+                  int num_seqs, int max_pages_per_seq, void* stream);
+
+/*
+ * kv_decode_attn -- decode attention, one query per sequence [S8 "What it
+ * does"; K4 "How"]. q: bf16 [batch][num_q_heads][head_dim]; query head h reads
+ * KV head h / (num_q_heads / num_kv_heads). Sequence b attends positions
+ * [0, seq_lens[b]) (seq_lens: int32 device [batch]); under quantize-on-write the
+ * caller appends the current token first. max_seq_len is a host-side upper
+ * bound on seq_lens used to size the split-K schedule. out: [batch][num_q_heads]
+ * [head_dim] in bf16 or fp32. scale is the softmax scale (usually
+ * 1/sqrt(head_dim)). An empty sequence gives a zero output row.
+ * workspace: device scratch of at least kv_decode_workspace_size() bytes,
+ * zero-filled before its first use; every call leaves its counter region
+ * zeroed again. Calls sharing a workspace must not overlap in time.
+ */
+QKV_API size_t kv_decode_workspace_size(const qkv_cache_desc* cache, int batch, int num_q_heads, int max_seq_len);
+
+QKV_API int kv_decode_attn(const qkv_cache_desc* cache, const void* q, int batch, int num_q_heads,
+                   const int32_t* page_table, int max_pages_per_seq, const int32_t* seq_lens,
+                   int max_seq_len, float scale, void* out, int out_dtype, void* workspace,
+                   size_t workspace_bytes, void* stream);
+
+/* Human-readable text for a QKV_* return code. */
+QKV_API const char* qkv_strerror(int code);
+
+/* The cudaError_t of the last failed CUDA call made by this library. */
+QKV_API int qkv_last_cuda_error(void);
+
+/* Reads (and if `clear`, resets) the device error word: bit 0 = page-table
+ * entry out of range, bit 1 = bad position / sequence index, bit 2 = a bounded
+ * wait gave up. Synchronizes the device. Returns the word, or a negative
+ * QKV_ERR_CUDA. */
+QKV_API int qkv_device_error(int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QKV_H_ */

@@ -1,0 +1,374 @@
+// abi.cu -- the C ABI of libqkv.so: argument validation, per-device set-up,
+// workspace sizing, TMA descriptor encoding and kernel dispatch by format.
+// Declared in include/qkv.h.
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/qkv.h"
+#include "qkv_device.cuh"
+
+#include "qkv_params.h"
+
+using namespace qkv;
+
+namespace {
+
+thread_local int g_last_cuda = 0;
+
+int cuda_fail(cudaError_t e) {
+    g_last_cuda = (int)e;
+    return QKV_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// Lloyd-Max levels for N(0, 1/128), computed by this library's host code.
+// Normalised levels z_j solve the Lloyd conditions for a standard normal:
+// cell edges are midpoints, each level is its cell's conditional mean
+// (pdf(a) - pdf(b)) / (cdf(b) - cdf(a)). Iterated from an even spacing on
+// [-2.5, 2.5] until the largest move is below 1e-15; then scaled by
+// 1/sqrt(128) and rounded to fp16 (round to nearest even).
+// ---------------------------------------------------------------------------
+double std_pdf(double z) { return std::isinf(z) ? 0.0 : 0.3989422804014327 * std::exp(-0.5 * z * z); }
+double std_cdf_upper(double z) { return 0.5 * std::erfc(z * 0.7071067811865476); }  // P(Z > z)
+
+void lloyd_levels(int n, double* z) {
+    for (int j = 0; j < n; ++j) z[j] = -2.5 + 5.0 * j / (n - 1);
+    for (int it = 0; it < 500000; ++it) {
+        double nz[16], move = 0.0;
+        for (int j = 0; j < n; ++j) {
+            double a = j == 0 ? -INFINITY : 0.5 * (z[j - 1] + z[j]);
+            double b = j == n - 1 ? INFINITY : 0.5 * (z[j] + z[j + 1]);
+            double mass = std_cdf_upper(a) - std_cdf_upper(b);
+            nz[j] = (std_pdf(a) - std_pdf(b)) / mass;
+            move = std::max(move, std::fabs(nz[j] - z[j]));
+        }
+        for (int j = 0; j < n; ++j) z[j] = nz[j];
+        if (move < 1e-15) break;
+    }
+}
+
+// double -> binary16 bits, round to nearest even, from the IEEE-754 double encoding
+uint16_t half_bits_rne(double v) {
+    uint64_t u;
+    std::memcpy(&u, &v, 8);
+    uint16_t sign = (uint16_t)((u >> 48) & 0x8000);
+    int e = (int)((u >> 52) & 0x7ff) - 1023;
+    uint64_t mant = (u & ((1ull << 52) - 1)) | (1ull << 52);  // 53-bit significand (normal doubles only)
+    if (((u >> 52) & 0x7ff) == 0) return sign;               // zero / double subnormal -> 0
+    int shift;        // bits to drop from the 53-bit significand
+    int hexp;         // biased half exponent of the result before rounding carry
+    if (e >= -14) { shift = 42; hexp = e + 15; }
+    else { shift = 42 + (-14 - e); hexp = 0; }
+    if (shift > 63) return sign;
+    uint64_t keep = mant >> shift, rem = mant & ((1ull << shift) - 1), halfway = 1ull << (shift - 1);
+    if (rem > halfway || (rem == halfway && (keep & 1))) ++keep;
+    uint32_t bits;
+    if (hexp == 0) bits = (uint32_t)keep;                     // subnormal (keep may reach 0x400 = min normal)
+    else {
+        if (keep == (1ull << 11)) { keep >>= 1; ++hexp; }
+        if (hexp >= 31) return (uint16_t)(sign | 0x7c00);
+        bits = ((uint32_t)hexp << 10) | (uint32_t)(keep & 0x3ff);
+    }
+    return (uint16_t)(sign | bits);
+}
+
+float half_bits_to_float(uint16_t h) {
+    int e = (h >> 10) & 0x1f, m = h & 0x3ff;
+    float v = e == 0 ? std::ldexp((float)m, -24) : std::ldexp((float)(m | 0x400), e - 25);
+    return (h & 0x8000) ? -v : v;
+}
+
+struct Levels { float l3[8]; float l4[16]; };
+
+const Levels& levels() {
+    static Levels L;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        const double sigma = 1.0 / std::sqrt(128.0);
+        double z[16];
+        lloyd_levels(8, z);
+        for (int j = 0; j < 8; ++j) L.l3[j] = half_bits_to_float(half_bits_rne(sigma * z[j]));
+        lloyd_levels(16, z);
+        for (int j = 0; j < 16; ++j) L.l4[j] = half_bits_to_float(half_bits_rne(sigma * z[j]));
+    });
+    return L;
+}
+
+// ---------------------------------------------------------------------------
+// per-device set-up (constant tables, SM count), done once per device with that
+// device current
+// ---------------------------------------------------------------------------
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mu;
+bool g_dev_ready[kMaxDevices];
+int g_dev_sms[kMaxDevices];
+
+int device_setup(int* dev_out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return QKV_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!g_dev_ready[dev]) {
+        const Levels& L = levels();
+        if ((e = append_upload_levels(L.l3, L.l4)) != cudaSuccess) return cuda_fail(e);
+        if ((e = decode_upload_levels(L.l3, L.l4)) != cudaSuccess) return cuda_fail(e);
+        int sms = 0;
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return cuda_fail(e);
+        g_dev_sms[dev] = sms;
+        g_dev_ready[dev] = true;
+    }
+    *dev_out = dev;
+    return QKV_OK;
+}
+
+// ---------------------------------------------------------------------------
+// TMA descriptors for the int8 / q4 code planes: 2-D [rows][row bytes] uint8,
+// box 16 rows x 128 bytes, 128-byte swizzle.
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+int make_code_map(CUtensorMap* map, const void* base, long long rows, int row_bytes) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return cuda_fail(cudaErrorNotSupported);
+    cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    cuuint32_t box[2] = {128u, 16u};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+    return QKV_OK;
+}
+
+// ---------------------------------------------------------------------------
+// validation
+// ---------------------------------------------------------------------------
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+int check_desc(const qkv_cache_desc* d) {
+    if (!d) return QKV_ERR_ARG;
+    if (d->format < QKV_INT8 || d->format > QKV_ISO4) return QKV_ERR_FORMAT;
+    if (d->page_size != kPage || d->num_pages <= 0 || d->num_kv_heads <= 0) return QKV_ERR_ARG;
+    const int D = d->head_dim;
+    switch (d->format) {
+        case QKV_INT8: if (D != 128 && D != 256) return QKV_ERR_HEAD_DIM; break;
+        case QKV_K8V4: if (D != 256) return QKV_ERR_HEAD_DIM; break;
+        default: if (D != 128 && D != 256) return QKV_ERR_HEAD_DIM; break;
+    }
+    if (!d->k_codes || !d->k_scales || !d->v_codes || !d->v_scales) return QKV_ERR_ARG;
+    if (!aligned16(d->k_codes) || !aligned16(d->k_scales) || !aligned16(d->v_codes) || !aligned16(d->v_scales))
+        return QKV_ERR_ARG;
+    return QKV_OK;
+}
+
+int enc_of(int fmt, int store) {
+    switch (fmt) {
+        case QKV_INT8: return ENC_INT8;
+        case QKV_K8V4: return store == 0 ? ENC_INT8 : ENC_Q4;
+        case QKV_ISO3: return ENC_ISO3;
+        case QKV_ISO4: return ENC_ISO4;
+    }
+    return -1;
+}
+
+struct DecodeLayout {
+    int G;          // query heads per CTA
+    int NH;         // head groups per sequence
+    int S;          // segments
+    int Cmax;       // CTA upper bound
+    int slot_floats;
+    size_t off_p2, off_seg, off_grp, bytes;
+};
+
+int decode_layout(const qkv_cache_desc* d, int batch, int num_q_heads, int sms, DecodeLayout* L) {
+    if (num_q_heads <= 0 || num_q_heads % d->num_kv_heads) return QKV_ERR_GQA;
+    const int Gtot = num_q_heads / d->num_kv_heads;
+    if (!(Gtot == 1 || Gtot == 2 || Gtot == 4 || Gtot % 8 == 0)) return QKV_ERR_GQA;
+    L->G = decode_heads_per_cta(Gtot);
+    L->NH = d->num_kv_heads * (Gtot / L->G);
+    L->S = batch * L->NH;
+    L->Cmax = sms;
+    L->slot_floats = 16 + 8 * d->head_dim;
+    const size_t slots = (size_t)L->Cmax + L->S;
+    auto al = [](size_t x) { return (x + 255) / 256 * 256; };
+    const size_t part = al(slots * L->slot_floats * sizeof(float));
+    L->off_p2 = part;
+    L->off_seg = 2 * part;
+    L->off_grp = L->off_seg + al((size_t)L->S * sizeof(int));
+    L->bytes = L->off_grp + al(slots * sizeof(int));
+    return QKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int qkv_row_bytes(int format, int store, int head_dim, int* code_bytes, int* scale_bytes) {
+    if (format < QKV_INT8 || format > QKV_ISO4) return QKV_ERR_FORMAT;
+    if ((store != 0 && store != 1) || head_dim <= 0 || !code_bytes || !scale_bytes) return QKV_ERR_ARG;
+    const int enc = enc_of(format, store);
+    if (head_dim % group_size(enc) || (enc == ENC_Q4 && head_dim != 256)) return QKV_ERR_HEAD_DIM;
+    *code_bytes = code_row_bytes(enc, head_dim);
+    *scale_bytes = scale_row_bytes(enc, head_dim);
+    return QKV_OK;
+}
+
+int qkv_iso_levels(int bits, float* out) {
+    if (!out || (bits != 3 && bits != 4)) return QKV_ERR_ARG;
+    const Levels& L = levels();
+    if (bits == 3) { std::memcpy(out, L.l3, sizeof(L.l3)); return 8; }
+    std::memcpy(out, L.l4, sizeof(L.l4));
+    return 16;
+}
+
+int iso_kv_append(const qkv_cache_desc* cache, const void* k, const void* v, int n_tokens, const int32_t* seq_id,
+                  const int32_t* pos, const int32_t* page_table, int num_seqs, int max_pages_per_seq, void* stream) {
+    int rc = check_desc(cache);
+    if (rc) return rc;
+    if (n_tokens < 0) return QKV_ERR_ARG;
+    if (n_tokens == 0) return QKV_OK;
+    if (!k || !v || !seq_id || !pos || !page_table || num_seqs <= 0 || max_pages_per_seq <= 0) return QKV_ERR_ARG;
+    if (!aligned16(k) || !aligned16(v)) return QKV_ERR_ARG;
+    int dev;
+    if ((rc = device_setup(&dev))) return rc;
+    AppendParams p;
+    p.codes[0] = (uint8_t*)cache->k_codes;
+    p.codes[1] = (uint8_t*)cache->v_codes;
+    p.scales[0] = (uint8_t*)cache->k_scales;
+    p.scales[1] = (uint8_t*)cache->v_scales;
+    p.src[0] = (const uint16_t*)k;
+    p.src[1] = (const uint16_t*)v;
+    p.seq_id = seq_id;
+    p.pos = pos;
+    p.page_table = page_table;
+    p.n_tokens = n_tokens;
+    p.Hkv = cache->num_kv_heads;
+    p.num_pages = cache->num_pages;
+    p.num_seqs = num_seqs;
+    p.max_pages = max_pages_per_seq;
+    for (int i = 0; i < 4; ++i) p.quat[i] = cache->quat[i];
+    cudaError_t e = append_launch(cache->format, cache->head_dim, p, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return QKV_OK;
+}
+
+size_t kv_decode_workspace_size(const qkv_cache_desc* cache, int batch, int num_q_heads, int max_seq_len) {
+    (void)max_seq_len;
+    if (check_desc(cache) || batch < 0) return 0;
+    int dev;
+    if (device_setup(&dev)) return 0;
+    DecodeLayout L;
+    if (decode_layout(cache, batch, num_q_heads, g_dev_sms[dev], &L)) return 0;
+    return L.bytes;
+}
+
+int kv_decode_attn(const qkv_cache_desc* cache, const void* q, int batch, int num_q_heads, const int32_t* page_table,
+                   int max_pages_per_seq, const int32_t* seq_lens, int max_seq_len, float scale, void* out,
+                   int out_dtype, void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = check_desc(cache);
+    if (rc) return rc;
+    if (batch < 0 || max_seq_len < 0) return QKV_ERR_ARG;
+    if (batch == 0) return QKV_OK;
+    if (batch > decode_max_batch()) return QKV_ERR_UNSUPPORTED;
+    if (!q || !page_table || !seq_lens || !out || max_pages_per_seq <= 0) return QKV_ERR_ARG;
+    if (out_dtype != QKV_OUT_BF16 && out_dtype != QKV_OUT_F32) return QKV_ERR_ARG;
+    if (!aligned16(q) || !aligned16(out)) return QKV_ERR_ARG;
+    if (!std::isfinite(scale)) return QKV_ERR_ARG;
+    int dev;
+    if ((rc = device_setup(&dev))) return rc;
+    DecodeLayout L;
+    if ((rc = decode_layout(cache, batch, num_q_heads, g_dev_sms[dev], &L))) return rc;
+    if (!workspace || workspace_bytes < L.bytes || !aligned16(workspace)) return QKV_ERR_WORKSPACE;
+
+    const int D = cache->head_dim;
+    const long long rows = (long long)cache->num_pages * cache->num_kv_heads * kPage;
+    CUtensorMap tk, tv;
+    std::memset(&tk, 0, sizeof(tk));
+    std::memset(&tv, 0, sizeof(tv));
+    const int kenc = enc_of(cache->format, 0), venc = enc_of(cache->format, 1);
+    if (kenc == ENC_INT8 && (rc = make_code_map(&tk, cache->k_codes, rows, code_row_bytes(kenc, D)))) return rc;
+    if ((venc == ENC_INT8 || venc == ENC_Q4) && (rc = make_code_map(&tv, cache->v_codes, rows, code_row_bytes(venc, D))))
+        return rc;
+
+    // grid: at most one CTA per SM, and about 8 pages (one per warp) or more per CTA
+    const long long max_pages_hint = ((long long)std::min(max_seq_len, max_pages_per_seq * kPage) + kPage - 1) / kPage;
+    const long long units = (long long)L.S * std::max(1LL, max_pages_hint);
+    const int grid = (int)std::max(1LL, std::min<long long>(L.Cmax, (units + 7) / 8));
+
+    DecodeParams p;
+    p.kc = (const uint8_t*)cache->k_codes;
+    p.ks = (const uint8_t*)cache->k_scales;
+    p.vc = (const uint8_t*)cache->v_codes;
+    p.vs = (const uint8_t*)cache->v_scales;
+    p.num_pages = cache->num_pages;
+    p.Hkv = cache->num_kv_heads;
+    p.q = (const uint16_t*)q;
+    p.B = batch;
+    p.Hq = num_q_heads;
+    p.Gtot = num_q_heads / cache->num_kv_heads;
+    p.NH = L.NH;
+    p.page_table = page_table;
+    p.max_pages = max_pages_per_seq;
+    p.seq_lens = seq_lens;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.out = out;
+    p.out_f32 = out_dtype == QKV_OUT_F32;
+    for (int i = 0; i < 4; ++i) p.quat[i] = cache->quat[i];
+    uint8_t* ws = (uint8_t*)workspace;
+    p.part1 = (float*)ws;
+    p.part2 = (float*)(ws + L.off_p2);
+    p.seg_cnt = (int*)(ws + L.off_seg);
+    p.grp_cnt = (int*)(ws + L.off_grp);
+    p.slot_floats = L.slot_floats;
+    cudaError_t e = decode_launch(cache->format, D, L.G, grid, tk, tv, p, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return QKV_OK;
+}
+
+const char* qkv_strerror(int code) {
+    switch (code) {
+        case QKV_OK: return "ok";
+        case QKV_ERR_ARG: return "invalid argument (null pointer, negative size, misalignment or bad page size)";
+        case QKV_ERR_HEAD_DIM: return "head_dim not supported for this format";
+        case QKV_ERR_GQA: return "num_q_heads must be a supported multiple of num_kv_heads";
+        case QKV_ERR_WORKSPACE: return "workspace missing or smaller than the required size";
+        case QKV_ERR_FORMAT: return "unknown KV format";
+        case QKV_ERR_CUDA: return "CUDA runtime error (see qkv_last_cuda_error)";
+        case QKV_ERR_DEVICE: return "device-side range check fired";
+        case QKV_ERR_UNSUPPORTED: return "request outside what this build implements";
+    }
+    return "unknown error code";
+}
+
+int qkv_last_cuda_error(void) { return g_last_cuda; }
+
+int qkv_device_error(int clear) {
+    unsigned a = 0, b = 0;
+    cudaError_t e = append_read_error(&a, clear != 0);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = decode_read_error(&b, clear != 0);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return (int)(a | b);
+}
+
+}  // extern "C"

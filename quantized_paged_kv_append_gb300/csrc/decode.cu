@@ -1,0 +1,820 @@
+// decode.cu -- paged split-K decode attention over the quantized pool.
+//
+// Method (page title, section):
+//   "qwen35/q36: --kv - int8 K/V caches", "What it does": decode splits the
+//   context ("part" kernels) and dequantizes K/V on the fly.
+//   "--kv k8v4: hybrid KV cache", "How": K int8 unrotated (q is not rotated), V
+//   in the FWHT-256 domain; the attention output is rotated back.
+//   "feat(kvcache): add ISO3/ISO4 KV-cache quantization", "What": dequant is
+//   norm * (conjugate rotation of the levels); here the query is rotated once
+//   instead, <q, conj(R) c> = <R q, c>, and the output is rotated back once.
+//
+// GB300 design (one CTA per SM, 8 warps):
+//   * Work is the list of (sequence, KV-head group, page) units; each CTA takes
+//     an equal contiguous share (stream-K style), so any mix of lengths keeps
+//     all SMs equally busy. A share may span several sequences ("pieces").
+//   * Each warp owns a contiguous run of pages and a private NS-stage pipeline:
+//     lane 0 issues TMA copies (2-D tiled, 128-byte swizzle, for int8/q4 code
+//     planes; 1-D bulk copies for scales and ISO codes) into shared memory,
+//     completing on an mbarrier. Page ids come through a 32-wide register ring.
+//   * QK^T and PV are warp-level fp16 tensor-core products (m16n8k16) on exact
+//     operands: codes (int8, q4-8, Lloyd-Max levels) are exact in fp16, the
+//     query is split into fp16 hi + lo rows, and per-(token, group) scales are
+//     applied to fp32 scores (K) or folded into the fp16 hi + lo probabilities
+//     (V). Softmax is online in fp32 (base 2); a warp-uniform exponent keeps
+//     the scaled probabilities inside the fp16 normal range.
+//   * Warps merge in shared memory; CTAs merge through the caller's workspace
+//     with the partial-softmax rule, done by the last-arriving CTA of each group
+//     of pieces (atomic ticket, no waiting), in two levels.
+#include "qkv_device.cuh"
+#include "qkv_params.h"
+
+namespace qkv {
+
+__device__ unsigned int g_err_decode;
+__constant__ float c_dec_levels[2][16];
+
+constexpr int kNW = 8;          // warps per CTA
+constexpr int kMaxBatch = 1024; // sequences per call (prefix table in shared memory)
+constexpr int kMaxMerge = 64;   // partials merged by one CTA in one level
+
+
+// ---------------------------------------------------------------------------
+// compile-time geometry of one pipeline stage (one page of one KV head)
+// ---------------------------------------------------------------------------
+template <int KENC, int VENC, int D>
+struct StageGeo {
+    static constexpr int KCB = code_row_bytes(KENC, D), KSB = scale_row_bytes(KENC, D);
+    static constexpr int VCB = code_row_bytes(VENC, D), VSB = scale_row_bytes(VENC, D);
+    static constexpr bool K_TMA = (KENC == ENC_INT8);                 // swizzled 2-D boxes of 16 x 128 B
+    static constexpr bool V_TMA = (VENC == ENC_INT8 || VENC == ENC_Q4);
+    static constexpr int al(int x, int a) { return (x + a - 1) / a * a; }
+    static constexpr int OFF_KC = 0;
+    static constexpr int OFF_VC = al(kPage * KCB, 1024);
+    static constexpr int OFF_KS = OFF_VC + al(kPage * VCB, 1024);
+    static constexpr int OFF_VS = OFF_KS + al(kPage * KSB, 128);
+    static constexpr int BYTES = al(OFF_VS + kPage * VSB, 1024);
+    static constexpr int TX = kPage * (KCB + KSB + VCB + VSB);
+};
+
+// byte address inside a 128-byte-swizzled tile of 16 rows (box width 128 B)
+__device__ __forceinline__ int swz(int row, int byte) {
+    return (byte >> 7) * 2048 + row * 128 + ((((byte >> 4) & 7) ^ (row & 7)) << 4) + (byte & 15);
+}
+
+template <typename T>
+__device__ __forceinline__ T lds(const uint8_t* base, int off) { return *reinterpret_cast<const T*>(base + off); }
+
+// int8 word (4 codes) -> two half2 (codes 0,1) and (codes 2,3), exact
+__device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, uint32_t& h01, uint32_t& h23) {
+    uint32_t x = w ^ 0x80808080u;
+    h01 = hsub2_u32(prmt(x, 0x64646464u, 0x4140u), 0x64806480u);
+    h23 = hsub2_u32(prmt(x, 0x64646464u, 0x4342u), 0x64806480u);
+}
+// byte i of word a and byte i of word b -> half2(a_i, b_i) of int8 codes, exact
+__device__ __forceinline__ uint32_t i8pair_to_h2(uint32_t a, uint32_t b, int i) {
+    uint32_t sel = (uint32_t)(i | (i << 4) | ((4 + i) << 8) | ((4 + i) << 12));
+    return hsub2_u32(lop3_and_xor(prmt(a, b, sel), 0x00ff00ffu, 0x64806480u), 0x64806480u);
+}
+
+template <int KENC, int VENC, int D, int G>
+struct DecodeKernel {
+    using Geo = StageGeo<KENC, VENC, D>;
+    static constexpr bool KISO = (KENC == ENC_ISO3 || KENC == ENC_ISO4);
+    static constexpr bool VISO = (VENC == ENC_ISO3 || VENC == ENC_ISO4);
+    static constexpr bool QLO = KISO;            // rotated query needs an fp16 lo part
+    static constexpr int NGK = D / group_size(KENC);
+    static constexpr int KSTEPS = D / 16;        // k-steps over the head dimension
+    static constexpr int KSPG = KSTEPS / NGK;    // k-steps per K group
+    static constexpr int MT = D / 16;            // PV m-tiles (16 dims each)
+    static constexpr int NGV = D / group_size(VENC);
+    static constexpr int MTPG = MT / NGV;        // m-tiles per V group
+    // pipeline depth per warp: as many stages (up to 4) as fit in ~216 KB with the tables
+    static constexpr int NS = (221184 / (kNW * Geo::BYTES)) >= 4 ? 4 : (221184 / (kNW * Geo::BYTES));
+    static constexpr bool ISO_LUT = KISO || VISO;
+    static constexpr int LUT_ENTRIES = (KENC == ENC_ISO4 || VENC == ENC_ISO4) ? 256 : 64;
+    static constexpr int LUT_BYTES = ISO_LUT ? LUT_ENTRIES * 32 * 4 : 0;
+    static constexpr int PIPE_BYTES = kNW * NS * Geo::BYTES;
+    static constexpr int MERGE_BYTES = kNW * 8 * D * 4;
+    static constexpr int AREA = PIPE_BYTES > MERGE_BYTES ? PIPE_BYTES : MERGE_BYTES;
+    static constexpr int OFF_LUT = AREA;
+    static constexpr int OFF_SMALL = OFF_LUT + LUT_BYTES;              // merge scalars + barriers + prefix
+    static constexpr int SMALL_BYTES = kNW * 8 * 4 * 2 + kMaxMerge * 8 * 4 + 64;
+    static constexpr int OFF_BAR = OFF_SMALL + SMALL_BYTES;
+    static constexpr int OFF_PREF = OFF_BAR + kNW * NS * 8;
+    static constexpr int SMEM = OFF_PREF + (kMaxBatch + 1) * 4;
+    static_assert(NS >= 2, "pipeline needs at least two stages");
+    static_assert(SMEM + 1024 + 2048 <= 232448, "shared memory budget (dynamic + alignment slack + static)");
+};
+
+// final output row: o [G][D] fp32 in shared memory, already normalised
+template <int VENC, int D, int G>
+__device__ void write_output(const DecodeParams& p, float* o, int b, int hq0, int tid) {
+    if constexpr (VENC == ENC_Q4) {
+        // inverse FWHT-256 (the transform is its own inverse) per head, one warp per head
+        const int w = tid >> 5, lane = tid & 31;
+        for (int h = w; h < G; h += kNW) {
+            float x[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) x[j] = o[h * D + lane * 8 + j];
+#pragma unroll
+            for (int hh = 1; hh < 8; hh <<= 1)
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if ((j & hh) == 0) { float a = x[j], c = x[j + hh]; x[j] = a + c; x[j + hh] = a - c; }
+#pragma unroll
+            for (int k = 0; k < 5; ++k) {
+                bool upper = (lane >> k) & 1;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    float ot = __shfl_xor_sync(0xffffffffu, x[j], 1 << k);
+                    x[j] = upper ? ot - x[j] : x[j] + ot;
+                }
+            }
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) o[h * D + lane * 8 + j] = x[j] * 0.0625f;
+        }
+        __syncthreads();
+    } else if constexpr (VENC == ENC_ISO3 || VENC == ENC_ISO4) {
+        // undo the rotation: conj(q) (x) o per 4-D group
+        const float q0 = p.quat[0], q1 = -p.quat[1], q2 = -p.quat[2], q3 = -p.quat[3];
+        for (int i = tid; i < G * D / 4; i += blockDim.x) {
+            float* v = o + 4 * i;
+            float a = v[0], bb = v[1], c = v[2], d = v[3];
+            float y0 = q0 * a - q1 * bb - q2 * c - q3 * d;
+            float y1 = q0 * bb + q1 * a + q2 * d - q3 * c;
+            float y2 = q0 * c - q1 * d + q2 * a + q3 * bb;
+            float y3 = q0 * d + q1 * c - q2 * bb + q3 * a;
+            v[0] = y0; v[1] = y1; v[2] = y2; v[3] = y3;
+        }
+        __syncthreads();
+    }
+    const size_t base = ((size_t)b * p.Hq + hq0) * D;
+    if (p.out_f32) {
+        float* out = reinterpret_cast<float*>(p.out) + base;
+        for (int i = tid; i < G * D; i += blockDim.x) out[i] = o[i];
+    } else {
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + base;
+        for (int i = tid; i < G * D; i += blockDim.x) out[i] = __float2bfloat16_rn(o[i]);
+    }
+}
+
+// Merge n partial slots (m[8], l[8], O[8][D]) into either a partial slot `dst`
+// or the final output. Partial-softmax rule: M = max m_j,
+// O = sum_j 2^(m_j - M) O_j, L = sum_j 2^(m_j - M) l_j (base-2 scores).
+template <int VENC, int D, int G>
+__device__ void merge_slots(const DecodeParams& p, const float* const* slots, int n, float* dst, bool final_out,
+                            int b, int hq0, float* sm_w, float* sm_o, int tid) {
+    __shared__ float s_M[8], s_L[8];
+    if (tid < G) {
+        float M = -INFINITY;
+        for (int j = 0; j < n; ++j) M = fmaxf(M, slots[j][tid]);
+        float L = 0.0f;
+        for (int j = 0; j < n; ++j) {
+            float mj = slots[j][tid];
+            float w = (mj == -INFINITY) ? 0.0f : exp2f(mj - M);
+            sm_w[j * 8 + tid] = w;
+            L += w * slots[j][8 + tid];
+        }
+        s_M[tid] = M;
+        s_L[tid] = L;
+    }
+    __syncthreads();
+    for (int i = tid; i < G * D; i += blockDim.x) {
+        int h = i / D;
+        float acc = 0.0f;
+        for (int j = 0; j < n; ++j) acc += sm_w[j * 8 + h] * slots[j][16 + i];
+        if (final_out) {
+            float L = s_L[h];
+            sm_o[i] = (L > 0.0f) ? acc / L : 0.0f;
+        } else {
+            dst[16 + i] = acc;
+        }
+    }
+    if (!final_out && tid < G) { dst[tid] = s_M[tid]; dst[8 + tid] = s_L[tid]; }
+    __syncthreads();
+    if (final_out) write_output<VENC, D, G>(p, sm_o, b, hq0, tid);
+}
+
+template <int KENC, int VENC, int D, int G>
+__global__ void __launch_bounds__(kNW * 32, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const DecodeParams p) {
+    using K = DecodeKernel<KENC, VENC, D, G>;
+    using Geo = typename K::Geo;
+    constexpr int NS = K::NS;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // 128-byte TMA swizzle patterns are defined on absolute shared addresses: align the base to 1 KB
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int C = gridDim.x, c = blockIdx.x;
+
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + K::OFF_BAR) + warp * NS;
+    int* pref = reinterpret_cast<int*>(smem + K::OFF_PREF);
+    float* sm_mw = reinterpret_cast<float*>(smem + K::OFF_SMALL);       // [kNW][8]
+    float* sm_lw = sm_mw + kNW * 8;                                     // [kNW][8]
+    float* sm_w = sm_lw + kNW * 8;                                      // [kMaxMerge][8]
+    __shared__ int s_ticket;
+    __shared__ const float* s_slots[kMaxMerge];
+
+    // ---- per-call setup: barriers, ISO pair tables, page-count prefix ----
+    if (lane == 0) {
+        for (int s = 0; s < NS; ++s) mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
+    if constexpr (K::ISO_LUT) {
+        uint32_t* lut = reinterpret_cast<uint32_t*>(smem + K::OFF_LUT);
+        constexpr int T = (KENC == ENC_ISO4 || VENC == ENC_ISO4) ? 1 : 0;
+        for (int e = tid; e < K::LUT_ENTRIES * 32; e += blockDim.x) {
+            int idx = e >> 5;
+            int c0, c1;
+            if constexpr (T == 1) { c0 = idx & 15; c1 = idx >> 4; }
+            else { c0 = (idx & 3) | (((idx >> 4) & 1) << 2); c1 = ((idx >> 2) & 3) | (((idx >> 5) & 1) << 2); }
+            lut[e] = f32x2_to_h2(c_dec_levels[T][c0], c_dec_levels[T][c1]);
+        }
+    }
+    {
+        // prefix of page counts over sequences (B <= kMaxBatch): pref[b] = sum_{b' < b} np(b')
+        __shared__ int s_wsum[kNW];
+        const int per = (p.B + blockDim.x - 1) / blockDim.x;
+        const int b0 = tid * per;
+        int local = 0;
+        for (int i = 0; i < per; ++i) {
+            int b = b0 + i;
+            if (b < p.B) {
+                int L = p.seq_lens[b];
+                if (L < 0 || L > p.max_pages * kPage) { atomicOr(&g_err_decode, kErrPos); L = max(0, min(L, p.max_pages * kPage)); }
+                local += (L + kPage - 1) / kPage;
+            }
+        }
+        int incl = local;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            int v = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += v;
+        }
+        if (lane == 31) s_wsum[warp] = incl;
+        __syncthreads();
+        int wpre = 0;
+        for (int w = 0; w < warp; ++w) wpre += s_wsum[w];
+        int run = wpre + incl - local;
+        for (int i = 0; i < per; ++i) {
+            int b = b0 + i;
+            if (b < p.B) {
+                int L = max(0, min(p.seq_lens[b], p.max_pages * kPage));
+                pref[b] = run;
+                run += (L + kPage - 1) / kPage;
+            }
+        }
+        if (b0 < p.B && b0 + per >= p.B) pref[p.B] = run;
+        if (p.B == 0 && tid == 0) pref[0] = 0;
+        __syncthreads();
+    }
+    const long long NH = p.NH;
+    const long long T = (long long)pref[p.B] * NH;   // total (segment, page) units
+    const long long beg = T * c / C, end = T * (c + 1) / C;
+    auto cta_of = [&](long long x) -> long long { return ((x + 1) * C + T - 1) / T - 1; };
+
+    // empty sequences: zero rows, written by CTA (s mod C)
+    for (long long s = c; s < (long long)p.B * NH; s += C) {
+        int b = (int)(s / NH);
+        if (pref[b + 1] == pref[b]) {
+            int hg = (int)(s % NH);
+            int kvh = hg / (p.Gtot / G), hgi = hg % (p.Gtot / G);
+            size_t base = ((size_t)b * p.Hq + kvh * p.Gtot + hgi * G) * D;
+            for (int i = tid; i < G * D; i += blockDim.x) {
+                if (p.out_f32) reinterpret_cast<float*>(p.out)[base + i] = 0.0f;
+                else reinterpret_cast<__nv_bfloat16*>(p.out)[base + i] = __float2bfloat16_rn(0.0f);
+            }
+        }
+    }
+
+    uint32_t gi = 0;   // pages consumed by this warp so far (stage / parity bookkeeping)
+    long long x = beg;
+    while (x < end) {
+        // ---- locate the piece: sequence b, head group hg, pages [p0, p1) ----
+        int lo = 0, hi = p.B;   // largest b with pref[b] * NH <= x
+        while (hi - lo > 1) { int mid = (lo + hi) >> 1; if ((long long)pref[mid] * NH <= x) lo = mid; else hi = mid; }
+        const int b = lo;
+        const int np = pref[b + 1] - pref[b];
+        const long long seg0 = (long long)pref[b] * NH;
+        const int hg = (int)((x - seg0) / np);
+        const long long soff = seg0 + (long long)hg * np;          // first unit of this segment
+        const int p0 = (int)(x - soff);
+        const long long xe = min(end, soff + np);
+        const int p1 = (int)(xe - soff);
+        const int L = max(0, min(p.seq_lens[b], p.max_pages * kPage));
+        const int kvh = hg / (p.Gtot / G), hgi = hg % (p.Gtot / G);
+        const int hq0 = kvh * p.Gtot + hgi * G;
+        const long long seg = (long long)b * NH + hg;
+        const long long clo = cta_of(soff), chi = cta_of(soff + np - 1);
+        const int npieces = (int)(chi - clo + 1);
+
+        // ---- this warp's pages ----
+        const int npc = p1 - p0;
+        const int wp0 = p0 + (int)((long long)npc * warp / kNW);
+        const int wp1 = p0 + (int)((long long)npc * (warp + 1) / kNW);
+        const int npg = wp1 - wp0;
+        const int32_t* ptrow = p.page_table + (size_t)b * p.max_pages;
+
+        // query fragments (A operand): rows r < 8 -> head r % G (hi part), rows r + 8 -> lo part
+        uint32_t qa[K::KSTEPS][4];
+        {
+            const int hh = g % G;
+            const uint16_t* qrow = p.q + ((size_t)b * p.Hq + hq0 + hh) * D;
+#pragma unroll
+            for (int ks = 0; ks < K::KSTEPS; ++ks) {
+                const int gg = ks / K::KSPG, u = ks % K::KSPG;
+                int d0;
+                if constexpr (KENC == ENC_INT8) d0 = 64 * gg + 16 * t + 4 * u;
+                else d0 = 128 * gg + 32 * t + 4 * u;
+                float qv[4];
+                if constexpr (!K::KISO) {
+                    uint2 w = *reinterpret_cast<const uint2*>(qrow + d0);
+                    qv[0] = bf16_bits_to_f32(w.x & 0xffffu); qv[1] = bf16_bits_to_f32(w.x >> 16);
+                    qv[2] = bf16_bits_to_f32(w.y & 0xffffu); qv[3] = bf16_bits_to_f32(w.y >> 16);
+                } else {
+                    // rotated query R q for this 4-D group (d0 is a multiple of 4)
+                    uint2 w = *reinterpret_cast<const uint2*>(qrow + d0);
+                    float a = bf16_bits_to_f32(w.x & 0xffffu), bq = bf16_bits_to_f32(w.x >> 16);
+                    float cq = bf16_bits_to_f32(w.y & 0xffffu), dq = bf16_bits_to_f32(w.y >> 16);
+                    const float q0 = p.quat[0], q1 = p.quat[1], q2 = p.quat[2], q3 = p.quat[3];
+                    qv[0] = q0 * a - q1 * bq - q2 * cq - q3 * dq;
+                    qv[1] = q0 * bq + q1 * a + q2 * dq - q3 * cq;
+                    qv[2] = q0 * cq - q1 * dq + q2 * a + q3 * bq;
+                    qv[3] = q0 * dq + q1 * cq - q2 * bq + q3 * a;
+                }
+                uint32_t h01 = f32x2_to_h2(qv[0], qv[1]), h23 = f32x2_to_h2(qv[2], qv[3]);
+                qa[ks][0] = h01;
+                qa[ks][2] = h23;
+                if constexpr (K::QLO) {
+                    float2 f01 = h2_to_f32x2(h01), f23 = h2_to_f32x2(h23);
+                    qa[ks][1] = f32x2_to_h2(qv[0] - f01.x, qv[1] - f01.y);
+                    qa[ks][3] = f32x2_to_h2(qv[2] - f23.x, qv[3] - f23.y);
+                } else {
+                    qa[ks][1] = 0u;
+                    qa[ks][3] = 0u;
+                }
+            }
+        }
+
+        float oacc[K::MT][4];
+#pragma unroll
+        for (int i = 0; i < K::MT; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.0f;
+        float m_run = -INFINITY, l_run = 0.0f;
+        int E_run = 1000;   // "unset"
+        bool failed = false;
+
+        // page-id ring: pid_cur covers warp pages [32*bc, 32*bc+32), pid_nxt the next 32
+        int bc = 0;
+        int pid_cur = (lane < npg) ? ptrow[wp0 + lane] : 0;
+        int pid_nxt = (32 + lane < npg) ? ptrow[wp0 + 32 + lane] : 0;
+        auto issue = [&](int j) {
+            // j: warp-local page index to load (uniform across the warp)
+            if ((j >> 5) > bc) {
+                pid_cur = pid_nxt;
+                ++bc;
+                pid_nxt = (32 * (bc + 1) + lane < npg) ? ptrow[wp0 + 32 * (bc + 1) + lane] : 0;
+            }
+            int pid = __shfl_sync(0xffffffffu, pid_cur, j & 31);
+            if (lane == 0) {
+                if (pid < 0 || pid >= p.num_pages) { atomicOr(&g_err_decode, kErrPage); pid = 0; }
+                const uint32_t slot = (gi + (uint32_t)j) % NS;
+                uint8_t* st = smem + (size_t)(warp * NS + slot) * Geo::BYTES;
+                uint64_t* bar = &bars[slot];
+                fence_proxy_async();
+                mbar_arrive_expect_tx(bar, Geo::TX);
+                const long long row = ((long long)pid * p.Hkv + kvh) * kPage;
+                if constexpr (Geo::K_TMA) {
+#pragma unroll
+                    for (int bx = 0; bx < (Geo::KCB + 127) / 128; ++bx) tma_load_2d(st + Geo::OFF_KC + bx * 2048, &tmK, bar, bx * 128, (int)row);
+                } else {
+                    bulk_load(st + Geo::OFF_KC, p.kc + row * Geo::KCB, kPage * Geo::KCB, bar);
+                }
+                if constexpr (Geo::V_TMA) {
+#pragma unroll
+                    for (int bx = 0; bx < (Geo::VCB + 127) / 128; ++bx) tma_load_2d(st + Geo::OFF_VC + bx * 2048, &tmV, bar, bx * 128, (int)row);
+                } else {
+                    bulk_load(st + Geo::OFF_VC, p.vc + row * Geo::VCB, kPage * Geo::VCB, bar);
+                }
+                bulk_load(st + Geo::OFF_KS, p.ks + row * Geo::KSB, kPage * Geo::KSB, bar);
+                bulk_load(st + Geo::OFF_VS, p.vs + row * Geo::VSB, kPage * Geo::VSB, bar);
+            }
+        };
+        // prologue
+        for (int j = 0; j < NS - 1 && j < npg; ++j) issue(j);
+
+        const uint32_t* lut = reinterpret_cast<const uint32_t*>(smem + K::OFF_LUT) + lane;
+        const int tk[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
+
+        for (int i = 0; i < npg; ++i) {
+            __syncwarp();
+            if (i + NS - 1 < npg) issue(i + NS - 1);
+            const uint32_t slot = (gi + (uint32_t)i) % NS;
+            const uint32_t parity = ((gi + (uint32_t)i) / NS) & 1u;
+            const uint8_t* st = smem + (size_t)(warp * NS + slot) * Geo::BYTES;
+            if (!mbar_wait_bounded(&bars[slot], parity)) {
+                if (lane == 0) atomicOr(&g_err_decode, kErrWait);
+                failed = true;
+                break;
+            }
+            const int pg = wp0 + i;
+            const int valid = min(kPage, L - pg * kPage);
+
+            // ---------------- scores: S = q . K^T (per K group) ----------------
+            float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int gg = 0; gg < K::NGK; ++gg) {
+                float cacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                if constexpr (KENC == ENC_INT8) {
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const int r = g + 8 * nt;
+                        uint4 w = lds<uint4>(st, Geo::OFF_KC + swz(r, 64 * gg + 16 * t));
+                        uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            uint32_t b0, b1;
+                            i8x4_to_h2x2(ws[u], b0, b1);
+                            const int ks = gg * 4 + u;
+                            mma_f16_16816(cacc[nt], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const int r = g + 8 * nt;
+                        if constexpr (KENC == ENC_ISO3) {
+                            const int rb = Geo::OFF_KC + r * Geo::KCB + 48 * gg;
+                            uint2 lo2 = lds<uint2>(st, rb + 8 * t);
+                            uint32_t hib = lds<uint32_t>(st, rb + 32 + 4 * t);
+#pragma unroll
+                            for (int u = 0; u < 8; ++u) {
+                                uint32_t lw = (u < 4) ? lo2.x : lo2.y;
+                                uint32_t lb = (lw >> (8 * (u & 3))) & 0xffu;
+                                uint32_t hb = (hib >> (4 * u)) & 0xfu;
+                                uint32_t i0 = (lb & 0xfu) | ((hb & 3u) << 4);
+                                uint32_t i1 = (lb >> 4) | ((hb >> 2) << 4);
+                                uint32_t b0 = lut[i0 * 32], b1 = lut[i1 * 32];
+                                const int ks = gg * 8 + u;
+                                mma_f16_16816(cacc[nt], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+                            }
+                        } else {
+                            uint4 w = lds<uint4>(st, Geo::OFF_KC + r * Geo::KCB + 64 * gg + 16 * t);
+                            uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                            for (int u = 0; u < 8; ++u) {
+                                uint32_t wd = ws[u >> 1];
+                                uint32_t i0 = (wd >> (16 * (u & 1))) & 0xffu;
+                                uint32_t i1 = (wd >> (16 * (u & 1) + 8)) & 0xffu;
+                                uint32_t b0 = lut[i0 * 32], b1 = lut[i1 * 32];
+                                const int ks = gg * 8 + u;
+                                mma_f16_16816(cacc[nt], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+                            }
+                        }
+                    }
+                }
+                // per-(token, group) K scale
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int tok = tk[j];
+                    float sk;
+                    if constexpr (KENC == ENC_INT8) sk = f16_bits_to_f32(lds<uint16_t>(st, Geo::OFF_KS + tok * Geo::KSB + 2 * gg));
+                    else if constexpr (KENC == ENC_ISO3) sk = f16_bits_to_f32(lds<uint16_t>(st, Geo::OFF_KS + tok * Geo::KSB + 2 * gg));
+                    else sk = f16_bits_to_f32(lds<uint16_t>(st, Geo::OFF_KS + tok * Geo::KSB + 4 * gg));
+                    const int nt = j >> 1, e = j & 1;
+                    float cv = cacc[nt][e];
+                    if constexpr (K::QLO) cv += cacc[nt][2 + e];
+                    sc[j] += sk * cv;
+                }
+            }
+            // mask, scale to base-2 logits
+#pragma unroll
+            for (int j = 0; j < 4; ++j) sc[j] = (tk[j] < valid) ? sc[j] * p.scale_log2 : -INFINITY;
+
+            // ---------------- V scales and the fp16 range exponent ----------------
+            float sv[4][K::NGV];
+            uint32_t vmax = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const bool ok = tk[j] < valid;
+#pragma unroll
+                for (int gv = 0; gv < K::NGV; ++gv) {
+                    uint32_t hb;
+                    if constexpr (VENC == ENC_ISO4) hb = lds<uint16_t>(st, Geo::OFF_VS + tk[j] * Geo::VSB + 4 * gv);
+                    else hb = lds<uint16_t>(st, Geo::OFF_VS + tk[j] * Geo::VSB + 2 * gv);
+                    if (!ok) hb = 0;
+                    vmax = max(vmax, hb & 0x7fffu);
+                    sv[j][gv] = f16_bits_to_f32(hb);
+                }
+            }
+            vmax = __reduce_max_sync(0xffffffffu, vmax);
+            const int Epage = 28 - max((int)(vmax >> 10), 1);
+
+            // ---------------- online softmax ----------------
+            float pm = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+            pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 1));
+            pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 2));
+            const float m_new = fmaxf(m_run, pm);
+            const bool need = (m_new > m_run) || (Epage < E_run);
+            if (__any_sync(0xffffffffu, need)) {
+                const float alpha = (m_new == m_run) ? 1.0f : fast_exp2(m_run - m_new);
+                l_run *= alpha;
+                const float a0 = __shfl_sync(0xffffffffu, alpha, ((2 * t) % G) * 4);
+                const float a1 = __shfl_sync(0xffffffffu, alpha, ((2 * t + 1) % G) * 4);
+                const int Enew = min(E_run, Epage);
+                const float ef = (E_run == 1000) ? 1.0f : __int_as_float((Enew - E_run + 127) << 23);
+                const float f0 = a0 * ef, f1 = a1 * ef;
+#pragma unroll
+                for (int mt = 0; mt < K::MT; ++mt) { oacc[mt][0] *= f0; oacc[mt][1] *= f1; oacc[mt][2] *= f0; oacc[mt][3] *= f1; }
+                m_run = m_new;
+                E_run = Enew;
+            }
+            float pr[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) { pr[j] = fast_exp2(sc[j] - m_run); l_run += pr[j]; }
+            const float e2 = __int_as_float((E_run + 127) << 23);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) pr[j] *= e2;
+
+            // ---------------- O^T += V^T P (per V group) ----------------
+            const int part = (G <= 4) ? ((g / G) & 1) : 0;
+            const bool colzero = (G <= 4) && (g >= 2 * G);
+#pragma unroll
+            for (int gv = 0; gv < K::NGV; ++gv) {
+                float P0 = pr[0] * sv[0][gv], P1 = pr[1] * sv[1][gv], P2 = pr[2] * sv[2][gv], P3 = pr[3] * sv[3][gv];
+                uint32_t h0 = f32x2_to_h2(P0, P1), h1 = f32x2_to_h2(P2, P3);
+                float2 f0 = h2_to_f32x2(h0), f1 = h2_to_f32x2(h1);
+                uint32_t l0 = f32x2_to_h2(P0 - f0.x, P1 - f0.y), l1 = f32x2_to_h2(P2 - f1.x, P3 - f1.y);
+                uint32_t bA0, bA1, bB0 = 0, bB1 = 0;
+                if constexpr (G <= 4) {
+                    bA0 = colzero ? 0u : (part ? l0 : h0);
+                    bA1 = colzero ? 0u : (part ? l1 : h1);
+                } else {
+                    bA0 = h0; bA1 = h1; bB0 = l0; bB1 = l1;
+                }
+                if constexpr (VENC == ENC_INT8) {
+                    const int byte = 64 * gv + 8 * g;
+                    uint2 va = lds<uint2>(st, Geo::OFF_VC + swz(tk[0], byte));
+                    uint2 vb = lds<uint2>(st, Geo::OFF_VC + swz(tk[1], byte));
+                    uint2 vc2 = lds<uint2>(st, Geo::OFF_VC + swz(tk[2], byte));
+                    uint2 vd = lds<uint2>(st, Geo::OFF_VC + swz(tk[3], byte));
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const uint32_t wa = (u < 2) ? va.x : va.y, wb = (u < 2) ? vb.x : vb.y;
+                        const uint32_t wc = (u < 2) ? vc2.x : vc2.y, wd = (u < 2) ? vd.x : vd.y;
+                        const int bi = (2 * u) & 3;
+                        uint32_t a0 = i8pair_to_h2(wa, wb, bi), a1 = i8pair_to_h2(wa, wb, bi + 1);
+                        uint32_t a2 = i8pair_to_h2(wc, wd, bi), a3 = i8pair_to_h2(wc, wd, bi + 1);
+                        const int mt = 4 * gv + u;
+                        mma_f16_16816(oacc[mt], a0, a1, a2, a3, bA0, bA1);
+                        if constexpr (G > 4) mma_f16_16816(oacc[mt], a0, a1, a2, a3, bB0, bB1);
+                    }
+                } else if constexpr (VENC == ENC_Q4) {
+                    const int byte = 16 * gv + 2 * g;
+                    uint32_t xa = lds<uint16_t>(st, Geo::OFF_VC + swz(tk[0], byte));
+                    uint32_t xb = lds<uint16_t>(st, Geo::OFF_VC + swz(tk[1], byte));
+                    uint32_t xc = lds<uint16_t>(st, Geo::OFF_VC + swz(tk[2], byte));
+                    uint32_t xd = lds<uint16_t>(st, Geo::OFF_VC + swz(tk[3], byte));
+                    const uint32_t X = xa | (xb << 16), Y = xc | (xd << 16);
+                    const uint32_t X8 = X >> 8, Y8 = Y >> 8;
+                    // low nibbles -> (q - 8) via 1024 + q - 1032; high nibbles via (1024 + 16 q) / 16 - 72
+                    const uint32_t kSubLo = 0x64086408u;            // half2(1032, 1032)
+                    const uint32_t kMul = 0x2c002c00u, kAdd = 0xd480d480u;  // half2(1/16), half2(-72)
+                    uint32_t a0 = hsub2_u32((X & 0x000f000fu) | 0x64006400u, kSubLo);
+                    uint32_t a1 = hsub2_u32((X8 & 0x000f000fu) | 0x64006400u, kSubLo);
+                    uint32_t a2 = hsub2_u32((Y & 0x000f000fu) | 0x64006400u, kSubLo);
+                    uint32_t a3 = hsub2_u32((Y8 & 0x000f000fu) | 0x64006400u, kSubLo);
+                    mma_f16_16816(oacc[2 * gv], a0, a1, a2, a3, bA0, bA1);
+                    if constexpr (G > 4) mma_f16_16816(oacc[2 * gv], a0, a1, a2, a3, bB0, bB1);
+                    uint32_t c0 = hfma2_u32((X & 0x00f000f0u) | 0x64006400u, kMul, kAdd);
+                    uint32_t c1 = hfma2_u32((X8 & 0x00f000f0u) | 0x64006400u, kMul, kAdd);
+                    uint32_t c2 = hfma2_u32((Y & 0x00f000f0u) | 0x64006400u, kMul, kAdd);
+                    uint32_t c3 = hfma2_u32((Y8 & 0x00f000f0u) | 0x64006400u, kMul, kAdd);
+                    mma_f16_16816(oacc[2 * gv + 1], c0, c1, c2, c3, bA0, bA1);
+                    if constexpr (G > 4) mma_f16_16816(oacc[2 * gv + 1], c0, c1, c2, c3, bB0, bB1);
+                } else if constexpr (VENC == ENC_ISO3) {
+                    uint32_t lo[4], hi16[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int rb = Geo::OFF_VC + tk[j] * Geo::VCB + 48 * gv;
+                        lo[j] = lds<uint32_t>(st, rb + 4 * g);
+                        hi16[j] = lds<uint16_t>(st, rb + 32 + 2 * g);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        uint32_t X[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            uint32_t idx = ((lo[j] >> (4 * u)) & 0xfu) | (((hi16[j] >> (2 * u)) & 3u) << 4);
+                            X[j] = lut[idx * 32];
+                        }
+                        uint32_t a0 = prmt(X[0], X[1], 0x5410u), a1 = prmt(X[0], X[1], 0x7632u);
+                        uint32_t a2 = prmt(X[2], X[3], 0x5410u), a3 = prmt(X[2], X[3], 0x7632u);
+                        const int mt = 8 * gv + u;
+                        mma_f16_16816(oacc[mt], a0, a1, a2, a3, bA0, bA1);
+                        if constexpr (G > 4) mma_f16_16816(oacc[mt], a0, a1, a2, a3, bB0, bB1);
+                    }
+                } else {  // ISO4
+                    uint2 cw[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) cw[j] = lds<uint2>(st, Geo::OFF_VC + tk[j] * Geo::VCB + 64 * gv + 8 * g);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        uint32_t X[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            uint32_t wd = (u < 4) ? cw[j].x : cw[j].y;
+                            X[j] = lut[((wd >> (8 * (u & 3))) & 0xffu) * 32];
+                        }
+                        uint32_t a0 = prmt(X[0], X[1], 0x5410u), a1 = prmt(X[0], X[1], 0x7632u);
+                        uint32_t a2 = prmt(X[2], X[3], 0x5410u), a3 = prmt(X[2], X[3], 0x7632u);
+                        const int mt = 8 * gv + u;
+                        mma_f16_16816(oacc[mt], a0, a1, a2, a3, bA0, bA1);
+                        if constexpr (G > 4) mma_f16_16816(oacc[mt], a0, a1, a2, a3, bB0, bB1);
+                    }
+                }
+            }
+        }
+        gi += (uint32_t)npg;
+        (void)failed;
+
+        // ---------------- warp -> CTA merge ----------------
+        __syncthreads();   // all warps done with their stages: the area becomes the merge buffer
+        {
+            float* Ow = reinterpret_cast<float*>(smem) + (size_t)warp * 8 * D;   // [8 cols][D]
+            float lq = l_run;
+            lq += __shfl_xor_sync(0xffffffffu, lq, 1);
+            lq += __shfl_xor_sync(0xffffffffu, lq, 2);
+            if (t == 0) { sm_mw[warp * 8 + g] = m_run; sm_lw[warp * 8 + g] = lq; }
+            const float inv = (E_run == 1000) ? 0.0f : __int_as_float((127 - E_run) << 23);
+#pragma unroll
+            for (int mt = 0; mt < K::MT; ++mt) {
+                int dA;
+                if constexpr (VENC == ENC_INT8) dA = 64 * (mt >> 2) + 8 * g + 2 * (mt & 3);
+                else if constexpr (VENC == ENC_Q4) dA = 32 * (mt >> 1) + 2 * g + 16 * (mt & 1);
+                else dA = 128 * (mt >> 3) + 16 * g + 2 * (mt & 7);
+                Ow[(2 * t) * D + dA] = oacc[mt][0] * inv;
+                Ow[(2 * t + 1) * D + dA] = oacc[mt][1] * inv;
+                Ow[(2 * t) * D + dA + 1] = oacc[mt][2] * inv;
+                Ow[(2 * t + 1) * D + dA + 1] = oacc[mt][3] * inv;
+            }
+        }
+        __syncthreads();
+        __shared__ float s_pM[8], s_pL[8], s_pw[kNW][8];
+        if (tid < G) {
+            float M = -INFINITY;
+            for (int w = 0; w < kNW; ++w) M = fmaxf(M, sm_mw[w * 8 + tid]);
+            float Ls = 0.0f;
+            for (int w = 0; w < kNW; ++w) {
+                float mw = sm_mw[w * 8 + tid];
+                float wt = (mw == -INFINITY) ? 0.0f : exp2f(mw - M);
+                s_pw[w][tid] = wt;
+                Ls += wt * sm_lw[w * 8 + tid];
+            }
+            s_pM[tid] = M;
+            s_pL[tid] = Ls;
+        }
+        __syncthreads();
+        // combine warps and the columns belonging to the same head
+        constexpr int PER = (8 * D + kNW * 32 - 1) / (kNW * 32);
+        float vals[PER];
+#pragma unroll
+        for (int k = 0; k < PER; ++k) {
+            const int i = tid + k * kNW * 32;
+            float acc = 0.0f;
+            if (i < G * D) {
+                const int h = i / D, d = i % D;
+#pragma unroll 1
+                for (int w = 0; w < kNW; ++w) {
+                    const float wt = s_pw[w][h];
+                    if (wt == 0.0f) continue;
+                    const float* Ow2 = reinterpret_cast<const float*>(smem) + (size_t)w * 8 * D;
+                    float cs = 0.0f;
+                    for (int n = h; n < 8; n += G) cs += Ow2[n * D + d];
+                    acc += wt * cs;
+                }
+            }
+            vals[k] = acc;
+        }
+        __syncthreads();   // warp rows fully read
+        if (npieces == 1) {
+            float* o = reinterpret_cast<float*>(smem);
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
+                const int i = tid + k * kNW * 32;
+                if (i < G * D) { const float Lh = s_pL[i / D]; o[i] = (Lh > 0.0f) ? vals[k] / Lh : 0.0f; }
+            }
+            __syncthreads();
+            write_output<VENC, D, G>(p, o, b, hq0, tid);
+        } else {
+            float* mine = p.part1 + (size_t)(c + seg) * p.slot_floats;
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
+                const int i = tid + k * kNW * 32;
+                if (i < G * D) mine[16 + i] = vals[k];
+            }
+            if (tid < G) { mine[tid] = s_pM[tid]; mine[8 + tid] = s_pL[tid]; }
+            __threadfence();
+            __syncthreads();
+            // two-level last-arrival merge over the pieces of this segment
+            const int j = (int)(c - clo);
+            int GS = 1;
+            while (GS * GS < npieces) ++GS;
+            const int ngroups = (npieces + GS - 1) / GS;
+            const int grp = j / GS;
+            const int gsize = min(GS, npieces - grp * GS);
+            const long long gslot = clo + (long long)grp * GS + seg;
+            if (tid == 0) s_ticket = atomicAdd(&p.grp_cnt[gslot], 1);
+            __syncthreads();
+            if (s_ticket == gsize - 1) {
+                __threadfence();
+                if (tid == 0) p.grp_cnt[gslot] = 0;
+                for (int k = tid; k < gsize; k += blockDim.x)
+                    s_slots[k] = p.part1 + (size_t)(clo + (long long)grp * GS + k + seg) * p.slot_floats;
+                __syncthreads();
+                float* o = reinterpret_cast<float*>(smem);
+                if (ngroups == 1) {
+                    merge_slots<VENC, D, G>(p, s_slots, gsize, nullptr, true, b, hq0, sm_w, o, tid);
+                } else {
+                    float* gdst = p.part2 + (size_t)gslot * p.slot_floats;
+                    merge_slots<VENC, D, G>(p, s_slots, gsize, gdst, false, b, hq0, sm_w, o, tid);
+                    __threadfence();
+                    __syncthreads();
+                    if (tid == 0) s_ticket = atomicAdd(&p.seg_cnt[seg], 1);
+                    __syncthreads();
+                    if (s_ticket == ngroups - 1) {
+                        __threadfence();
+                        if (tid == 0) p.seg_cnt[seg] = 0;
+                        for (int k = tid; k < ngroups; k += blockDim.x)
+                            s_slots[k] = p.part2 + (size_t)(clo + (long long)k * GS + seg) * p.slot_floats;
+                        __syncthreads();
+                        merge_slots<VENC, D, G>(p, s_slots, ngroups, nullptr, true, b, hq0, sm_w, o, tid);
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        x = xe;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+cudaError_t decode_upload_levels(const float* lv3, const float* lv4) {
+    float lv[2][16] = {};
+    for (int j = 0; j < 8; ++j) lv[0][j] = lv3[j];
+    for (int j = 0; j < 16; ++j) lv[1][j] = lv4[j];
+    return cudaMemcpyToSymbol(c_dec_levels, lv, sizeof(lv));
+}
+
+cudaError_t decode_read_error(unsigned* out, bool clear) {
+    cudaError_t e = cudaMemcpyFromSymbol(out, g_err_decode, sizeof(unsigned));
+    if (e != cudaSuccess || !clear) return e;
+    unsigned z = 0;
+    return cudaMemcpyToSymbol(g_err_decode, &z, sizeof(unsigned));
+}
+
+int decode_heads_per_cta(int Gtot) { return Gtot >= 8 ? 8 : Gtot; }
+int decode_max_batch() { return kMaxBatch; }
+
+template <int KE, int VE, int D, int G>
+static cudaError_t launch_one(int grid, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, cudaStream_t st) {
+    using K = DecodeKernel<KE, VE, D, G>;
+    auto fn = decode_kernel<KE, VE, D, G>;
+    static bool configured = false;   // per instantiation; attribute is per-device-context
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, K::SMEM + 1024);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    fn<<<grid, kNW * 32, K::SMEM + 1024, st>>>(tk, tv, p);
+    return cudaGetLastError();
+}
+
+template <int KE, int VE, int D>
+static cudaError_t launch_g(int G, int grid, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, cudaStream_t st) {
+    switch (G) {
+        case 1: return launch_one<KE, VE, D, 1>(grid, tk, tv, p, st);
+        case 2: return launch_one<KE, VE, D, 2>(grid, tk, tv, p, st);
+        case 4: return launch_one<KE, VE, D, 4>(grid, tk, tv, p, st);
+        case 8: return launch_one<KE, VE, D, 8>(grid, tk, tv, p, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t decode_launch(int fmt, int D, int G, int grid, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const DecodeParams& p, cudaStream_t st) {
+    if (fmt == 0 && D == 256) return launch_g<ENC_INT8, ENC_INT8, 256>(G, grid, tk, tv, p, st);
+    if (fmt == 0 && D == 128) return launch_g<ENC_INT8, ENC_INT8, 128>(G, grid, tk, tv, p, st);
+    if (fmt == 1 && D == 256) return launch_g<ENC_INT8, ENC_Q4, 256>(G, grid, tk, tv, p, st);
+    if (fmt == 2 && D == 128) return launch_g<ENC_ISO3, ENC_ISO3, 128>(G, grid, tk, tv, p, st);
+    if (fmt == 2 && D == 256) return launch_g<ENC_ISO3, ENC_ISO3, 256>(G, grid, tk, tv, p, st);
+    if (fmt == 3 && D == 128) return launch_g<ENC_ISO4, ENC_ISO4, 128>(G, grid, tk, tv, p, st);
+    if (fmt == 3 && D == 256) return launch_g<ENC_ISO4, ENC_ISO4, 256>(G, grid, tk, tv, p, st);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace qkv

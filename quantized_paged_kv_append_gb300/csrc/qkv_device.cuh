@@ -1,0 +1,138 @@
+// qkv_device.cuh -- device-side building blocks shared by the library's kernels:
+// row geometry of the packed planes, IEEE-exact fp32 helpers, and thin inline
+// PTX wrappers for mbarrier, TMA / bulk copies and the warp-level mma.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace qkv {
+
+// Store encodings (a format is one encoding for K and one for V).
+enum Enc : int { ENC_INT8 = 0, ENC_Q4 = 1, ENC_ISO3 = 2, ENC_ISO4 = 3 };
+
+constexpr int kPage = 16;  // tokens per page
+
+__host__ __device__ constexpr int code_row_bytes(int enc, int D) {
+    return enc == ENC_INT8 ? D : enc == ENC_Q4 ? D / 2 : enc == ENC_ISO3 ? (D / 128) * 48 : (D / 128) * 64;
+}
+__host__ __device__ constexpr int scale_row_bytes(int enc, int D) {
+    return enc == ENC_INT8 ? (D / 64) * 2 : enc == ENC_Q4 ? (D / 32) * 2 : enc == ENC_ISO3 ? (D / 128) * 2 : (D / 128) * 4;
+}
+// values sharing one scale
+__host__ __device__ constexpr int group_size(int enc) { return enc == ENC_INT8 ? 64 : enc == ENC_Q4 ? 32 : 128; }
+
+// Device error word bits (see qkv_device_error in qkv.h).
+constexpr unsigned kErrPage = 1u, kErrPos = 2u, kErrWait = 4u;
+
+// ---------------------------------------------------------------------------
+// fp16 helpers
+// ---------------------------------------------------------------------------
+// Round to nearest even; overflow saturates to the largest finite half.
+__device__ __forceinline__ uint16_t f32_to_f16_sat(float x) {
+    __half h = __float2half_rn(x);
+    uint16_t b = __half_as_ushort(h);
+    if ((b & 0x7fffu) == 0x7c00u) b = (uint16_t)((b & 0x8000u) | 0x7bffu);
+    return b;
+}
+__device__ __forceinline__ float f16_bits_to_f32(uint32_t b) { return __half2float(__ushort_as_half((uint16_t)b)); }
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
+
+// ---------------------------------------------------------------------------
+// shared-memory / async-copy PTX
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait: gives up after `limit` polls and reports false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t limit = (1u << 20)) {
+    for (uint32_t i = 0; i < limit; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+// 2-D tiled TMA load (box given by the tensor map) completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+            smem_addr(dst)),
+        "l"(map), "r"(smem_addr(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+// Contiguous bulk copy global -> shared (16-byte aligned, size multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// warp-level tensor-core product: D(16x8, f32) += A(16x16, f16) * B(16x8, f16)
+// Fragment ownership (g = lane / 4, t = lane % 4):
+//   A: a[0] = rows g  , cols 2t..2t+1   a[1] = rows g+8, cols 2t..2t+1
+//      a[2] = rows g  , cols 2t+8..+9   a[3] = rows g+8, cols 2t+8..+9
+//   B: b[0] = rows 2t..2t+1, col g      b[1] = rows 2t+8..2t+9, col g
+//   C: c[0..1] = row g, cols 2t..2t+1   c[2..3] = row g+8, cols 2t..2t+1
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mma_f16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+__device__ __forceinline__ uint32_t lop3_and_xor(uint32_t a, uint32_t mask, uint32_t c) {
+    // (a & mask) ^ c
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(r) : "r"(a), "r"(mask), "r"(c));
+    return r;
+}
+__device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
+    __half2 r = __hsub2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+    return *reinterpret_cast<uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
+    __half2 r = __hfma2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b), *reinterpret_cast<__half2*>(&c));
+    return *reinterpret_cast<uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t f32x2_to_h2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ float2 h2_to_f32x2(uint32_t v) {
+    return __half22float2(*reinterpret_cast<__half2*>(&v));
+}
+__device__ __forceinline__ float fast_exp2(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+}  // namespace qkv

@@ -1,0 +1,56 @@
+// qkv_params.h -- kernel parameter blocks and the host-side entry points of the
+// kernel translation units (append.cu, decode.cu), shared with abi.cu.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace qkv {
+
+struct AppendParams {
+    uint8_t* codes[2];       // [store]: 0 = K, 1 = V
+    uint8_t* scales[2];
+    const uint16_t* src[2];  // bf16 [n][Hkv][D]
+    const int32_t* seq_id;
+    const int32_t* pos;
+    const int32_t* page_table;
+    int n_tokens, Hkv, num_pages, num_seqs, max_pages;
+    float quat[4];
+};
+
+struct DecodeParams {
+    const uint8_t* kc;
+    const uint8_t* ks;
+    const uint8_t* vc;
+    const uint8_t* vs;
+    int num_pages, Hkv;
+    const uint16_t* q;   // bf16 [B][Hq][D]
+    int B, Hq, Gtot;     // Gtot = Hq / Hkv
+    int NH;              // head groups per sequence = Hkv * Gtot / G
+    const int32_t* page_table;
+    int max_pages;
+    const int32_t* seq_lens;
+    float scale_log2;    // softmax scale * log2(e)
+    void* out;
+    int out_f32;
+    float quat[4];
+    float* part1;        // (C + S) partial slots
+    float* part2;        // (C + S) group slots
+    int* seg_cnt;        // [S]
+    int* grp_cnt;        // [C + S]
+    int slot_floats;     // 16 + 8 * D
+};
+
+cudaError_t append_upload_levels(const float* lv3, const float* lv4);
+cudaError_t append_read_error(unsigned* out, bool clear);
+cudaError_t append_launch(int fmt, int D, const AppendParams& p, cudaStream_t st);
+
+cudaError_t decode_upload_levels(const float* lv3, const float* lv4);
+cudaError_t decode_read_error(unsigned* out, bool clear);
+cudaError_t decode_launch(int fmt, int D, int G, int grid, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const DecodeParams& p, cudaStream_t st);
+int decode_heads_per_cta(int Gtot);
+int decode_max_batch();
+
+}  // namespace qkv

@@ -1,0 +1,155 @@
+"""GPU parity of paged split-K decode attention against the CPU oracle.
+
+The GPU reads the oracle's own packed planes (so decode is tested independently
+of append). Tolerance: fp32 output within max-abs 2e-3 and cosine > 0.9999 of
+the oracle's double-precision attention over the same dequantized K/V."""
+
+import numpy as np
+import pytest
+
+from _workload import Workload, bf16_dev, compare_attention, gpu_cache, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import quantized_paged_kv_append_gb300 as qkv
+    from quantized_paged_kv_append_gb300 import build
+    build.build()
+    return torch, qkv
+
+
+def _run(torch, qkv, w, pool, out_dtype=None, table=None, lens=None, workspace=None, repeat=1):
+    out_dtype = out_dtype or torch.float32
+    cache = gpu_cache(qkv, w, torch, planes=pool.planes())
+    t = to_dev(w.table if table is None else table, torch)
+    sl = to_dev(w.lens if lens is None else lens, torch)
+    q = bf16_dev(w.q, torch)
+    outs = []
+    for _ in range(repeat):
+        o = qkv.decode(cache, q, t, sl, max(1, w.max_len()), scale=w.scale, out_dtype=out_dtype, workspace=workspace)
+        outs.append(o.float().cpu().numpy())
+    torch.cuda.synchronize()
+    assert qkv.device_error() == 0
+    return outs if repeat > 1 else outs[0]
+
+
+SMALL = [
+    # fmt, D, Hkv, Hq
+    ("int8", 256, 2, 16), ("int8", 128, 2, 8), ("int8", 256, 4, 4), ("int8", 256, 1, 2),
+    ("int8", 256, 2, 32), ("k8v4", 256, 2, 16), ("k8v4", 256, 1, 4),
+    ("iso3", 128, 4, 16), ("iso4", 128, 4, 16), ("iso3", 256, 2, 16), ("iso4", 256, 2, 4),
+    ("iso4", 128, 2, 2),
+]
+
+
+@pytest.mark.parametrize("fmt,d,hkv,hq", SMALL)
+def test_decode_small_ragged(env, orc, fmt, d, hkv, hq):
+    torch, qkv = env
+    w = Workload(fmt, [1, 37, 300, 16, 1000], hkv, hq, d, seed=21)
+    pool = w.oracle_pool(orc)
+    ref = pool.decode(w.q, w.table, w.lens, w.scale)
+    got = _run(torch, qkv, w, pool)
+    r = compare_attention(got, ref)
+    assert r["ok"], r
+
+
+@pytest.mark.parametrize("fmt,d,hkv,hq,L", [
+    ("int8", 256, 2, 16, 2048),      # tiny config
+    ("int8", 256, 2, 16, 131072),    # 128K
+    ("k8v4", 256, 2, 16, 118750),
+    ("iso3", 128, 4, 16, 81920),
+    ("iso4", 128, 4, 16, 81920),
+])
+def test_decode_full_size(env, orc, fmt, d, hkv, hq, L):
+    torch, qkv = env
+    w = Workload(fmt, [L], hkv, hq, d, seed=0)
+    pool = w.oracle_pool(orc)
+    ref = pool.decode(w.q, w.table, w.lens, w.scale)
+    got = _run(torch, qkv, w, pool)
+    r = compare_attention(got, ref)
+    assert r["ok"], r
+    gotb = _run(torch, qkv, w, pool, out_dtype=torch.bfloat16)
+    rb = compare_attention(gotb, ref, bf16=True)
+    assert rb["ok"], rb
+
+
+def test_decode_mixed_batch_subset(env, orc):
+    """32 sequences, lengths uniform in [4096, 65536] (the serving mix); the
+    oracle checks a subset of 6 sequences against the full GPU batch."""
+    torch, qkv = env
+    from quantized_paged_kv_append_gb300 import synth
+    lens = synth.seq_lengths(0, 32, 4096, 65536)
+    w = Workload("int8", lens, 2, 16, 256, seed=0, spare=0)
+    pool = w.oracle_pool(orc)
+    got = _run(torch, qkv, w, pool)
+    pick = np.array([0, 5, 11, 17, 26, 31])
+    ref = pool.decode(w.q[pick], w.table[pick], w.lens[pick], w.scale)
+    r = compare_attention(got[pick], ref)
+    assert r["ok"], r
+
+
+def test_decode_empty_and_single_token(env, orc):
+    torch, qkv = env
+    w = Workload("int8", [0, 1, 17, 0], 2, 16, 256, seed=4)
+    pool = w.oracle_pool(orc)
+    got = _run(torch, qkv, w, pool)
+    ref = pool.decode(w.q, w.table, w.lens, w.scale)
+    assert np.all(got[0] == 0) and np.all(got[3] == 0)
+    r = compare_attention(got, ref)
+    assert r["ok"], r
+
+
+def test_decode_page_table_permutation_bitwise(env, orc):
+    """Moving the same pages to other physical slots changes nothing: the
+    output is bit-identical."""
+    torch, qkv = env
+    w = Workload("k8v4", [900, 333], 2, 16, 256, seed=8, spare=10)
+    pool = w.oracle_pool(orc)
+    a = _run(torch, qkv, w, pool)
+    # relocate every page of the pool by a seeded permutation
+    from quantized_paged_kv_append_gb300 import synth
+    perm = synth.permutation(99, w.num_pages)
+    planes2 = []
+    for pl in pool.planes():
+        rows = pl.reshape(w.num_pages, -1)
+        moved = np.empty_like(rows)
+        moved[perm] = rows
+        planes2.append(moved.reshape(-1))
+    table2 = np.where(w.table >= 0, perm[np.maximum(w.table, 0)], -1).astype(np.int32)
+
+    class P2:
+        def planes(self):
+            return planes2
+    b = _run(torch, qkv, w, P2(), table=table2)
+    assert np.array_equal(a, b)
+
+
+def test_decode_deterministic_and_workspace_reuse(env, orc):
+    """Repeated calls with one workspace give identical bits (the counters are
+    returned to zero by each call)."""
+    torch, qkv = env
+    w = Workload("int8", [5000, 20000, 70], 2, 16, 256, seed=9)
+    pool = w.oracle_pool(orc)
+    cache = gpu_cache(qkv, w, torch, planes=pool.planes())
+    ws = qkv.decode_workspace(cache, w.B, w.hq, w.max_len())
+    outs = _run(torch, qkv, w, pool, workspace=ws, repeat=3)
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
+    ref = pool.decode(w.q, w.table, w.lens, w.scale)
+    assert compare_attention(outs[0], ref)["ok"]
+
+
+def test_decode_bad_page_entry_flags_without_fault(env, orc):
+    torch, qkv = env
+    w = Workload("int8", [64], 2, 16, 256, seed=10)
+    pool = w.oracle_pool(orc)
+    bad = w.table.copy()
+    bad[0, 2] = 10 ** 6
+    cache = gpu_cache(qkv, w, torch, planes=pool.planes())
+    qkv.decode(cache, bf16_dev(w.q, torch), to_dev(bad, torch), to_dev(w.lens, torch), 64, scale=w.scale)
+    torch.cuda.synchronize()
+    assert qkv.device_error() & 1
