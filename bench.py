@@ -30,7 +30,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "decode-attn packed-KV HBM GB/s (% of peak) and steps/s at 128K ctx, 1 GB300"
 B, HQ, HKV, D, L = 1, 16, 2, 256, 131072
-LAYERS = 8
+LAYERS = 8   # default; --layers overrides
 KV_BYTES_PER_TOKEN = 2 * HKV * (D + 2 * D // 64)        # int8 codes + fp16 scales, K and V: 1056
 DECODE_BYTES = L * KV_BYTES_PER_TOKEN                     # 138,412,032 packed bytes read per step
 WORKLOAD = ("int8 KV decode at 128K context: batch 1, 16 q heads / 2 KV heads, head_dim 256, "
@@ -181,8 +181,9 @@ def run_gpu(args):
         with torch.cuda.graph(graph, stream=stream):
             for i in range(args.steps):
                 step(i, evs[i])
-        graph.replay()
-        stream.synchronize()
+        with torch.cuda.stream(stream):
+            graph.replay()
+        torch.cuda.synchronize()
         _ = evs[0][0].elapsed_time(evs[0][1])
     except Exception:
         per_launch = False
@@ -191,8 +192,9 @@ def run_gpu(args):
         with torch.cuda.graph(graph, stream=stream):
             for i in range(args.steps):
                 step(i)
-        graph.replay()
-        stream.synchronize()
+        with torch.cuda.stream(stream):
+            graph.replay()
+        torch.cuda.synchronize()
     if not per_launch:
         # decode-only graph: average launch duration = graph time / K
         dgraph = torch.cuda.CUDAGraph()
@@ -201,8 +203,9 @@ def run_gpu(args):
                 layer = i % LAYERS
                 qkv.decode(caches[layer], q_d[layer], tabs[layer], lens, L, scale=scale, out=out, workspace=ws,
                            stream=stream)
-        dgraph.replay()
-        stream.synchronize()
+        with torch.cuda.stream(stream):
+            dgraph.replay()
+        torch.cuda.synchronize()
 
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
@@ -211,19 +214,21 @@ def run_gpu(args):
     proc, cpath = _clock_sampler()
     time.sleep(0.3)
     reps = max(1, args.reps)
-    t0.record(stream)
-    for _ in range(reps):
-        graph.replay()
-    t1.record(stream)
-    t1.synchronize()
+    with torch.cuda.stream(stream):     # CUDAGraph.replay launches on the current stream
+        t0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        t1.record(stream)
+    torch.cuda.synchronize()
     if per_launch:
         dec_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)   # last replay's launches
     else:
         d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        d0.record(stream)
-        dgraph.replay()
-        d1.record(stream)
-        d1.synchronize()
+        with torch.cuda.stream(stream):
+            d0.record(stream)
+            dgraph.replay()
+            d1.record(stream)
+        torch.cuda.synchronize()
         dec_ms = d0.elapsed_time(d1) / args.steps
     torch.cuda.synchronize()
     clocks = _clock_summary(proc, cpath, local)
@@ -236,42 +241,44 @@ def run_gpu(args):
     ms_per_step = total_ms / nsteps
     value = DECODE_BYTES * nsteps * world / (total_ms / 1e3) / 1e9
 
-    # end to end through the public API with host buffers (pinned), copies inside the timed region
-    h_q = torch.from_numpy(np.ascontiguousarray(q[0]).view(np.int16)).view(torch.bfloat16).pin_memory()
-    h_kn = torch.from_numpy(np.ascontiguousarray(kn[0]).view(np.int16)).view(torch.bfloat16).pin_memory()
-    h_vn = torch.from_numpy(np.ascontiguousarray(vn[0]).view(np.int16)).view(torch.bfloat16).pin_memory()
-    h_meta = torch.tensor([0, L - 1, L], dtype=torch.int32).pin_memory()
-    h_out = torch.empty((B, HQ, D), dtype=torch.bfloat16).pin_memory()
-    d_q, d_kn, d_vn = torch.empty_like(q_d[0]), torch.empty_like(kn_d[0]), torch.empty_like(vn_d[0])
-    d_meta = torch.empty(3, dtype=torch.int32, device=dev)
-    h2d = h_q.numel() * 2 + h_kn.numel() * 2 + h_vn.numel() * 2 + h_meta.numel() * 4
-    d2h = h_out.numel() * 2
+    e2e = None
+    if not args.no_e2e:
+        # end to end through the public API with host buffers (pinned), copies inside the timed region
+        h_q = torch.from_numpy(np.ascontiguousarray(q[0]).view(np.int16)).view(torch.bfloat16).pin_memory()
+        h_kn = torch.from_numpy(np.ascontiguousarray(kn[0]).view(np.int16)).view(torch.bfloat16).pin_memory()
+        h_vn = torch.from_numpy(np.ascontiguousarray(vn[0]).view(np.int16)).view(torch.bfloat16).pin_memory()
+        h_meta = torch.tensor([0, L - 1, L], dtype=torch.int32).pin_memory()
+        h_out = torch.empty((B, HQ, D), dtype=torch.bfloat16).pin_memory()
+        d_q, d_kn, d_vn = torch.empty_like(q_d[0]), torch.empty_like(kn_d[0]), torch.empty_like(vn_d[0])
+        d_meta = torch.empty(3, dtype=torch.int32, device=dev)
+        h2d = h_q.numel() * 2 + h_kn.numel() * 2 + h_vn.numel() * 2 + h_meta.numel() * 4
+        d2h = h_out.numel() * 2
 
-    def e2e_step(i):
-        layer = i % LAYERS
-        d_q.copy_(h_q, non_blocking=True)
-        d_kn.copy_(h_kn, non_blocking=True)
-        d_vn.copy_(h_vn, non_blocking=True)
-        d_meta.copy_(h_meta, non_blocking=True)
-        qkv.append(caches[layer], d_kn, d_vn, d_meta[0:1], d_meta[1:2], tabs[layer], stream=stream)
-        qkv.decode(caches[layer], d_q, tabs[layer], d_meta[2:3], L, scale=scale, out=out, workspace=ws, stream=stream)
-        h_out.copy_(out, non_blocking=True)
+        def e2e_step(i):
+            layer = i % LAYERS
+            d_q.copy_(h_q, non_blocking=True)
+            d_kn.copy_(h_kn, non_blocking=True)
+            d_vn.copy_(h_vn, non_blocking=True)
+            d_meta.copy_(h_meta, non_blocking=True)
+            qkv.append(caches[layer], d_kn, d_vn, d_meta[0:1], d_meta[1:2], tabs[layer], stream=stream)
+            qkv.decode(caches[layer], d_q, tabs[layer], d_meta[2:3], L, scale=scale, out=out, workspace=ws, stream=stream)
+            h_out.copy_(out, non_blocking=True)
 
-    with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            e2e_step(i)
-        stream.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        w0 = time.perf_counter()
-        e0.record(stream)
-        for i in range(args.steps):
-            e2e_step(i)
-        e1.record(stream)
-        e1.synchronize()
-        wall = time.perf_counter() - w0
-    e2e_ms = max(e0.elapsed_time(e1), wall * 1e3) / args.steps
-    assert qkv.device_error() == 0
-
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup):
+                e2e_step(i)
+            stream.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            w0 = time.perf_counter()
+            e0.record(stream)
+            for i in range(args.steps):
+                e2e_step(i)
+            e1.record(stream)
+            e1.synchronize()
+            wall = time.perf_counter() - w0
+        e2e_ms = max(e0.elapsed_time(e1), wall * 1e3) / args.steps
+        assert qkv.device_error() == 0
+        e2e = {"value": round(DECODE_BYTES / (e2e_ms / 1e3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -285,7 +292,8 @@ def run_gpu(args):
         "data": "synthetic (seeded splitmix64 + Box-Muller, bf16)",
         "config": {"workload": WORKLOAD, "batch": B, "q_heads": HQ, "kv_heads": HKV, "head_dim": D,
                    "context": L, "page_size": 16, "format": "int8", "layer_copies": LAYERS,
-                   "l2": "inputs larger than L2: 8 layer caches (1.1 GB) cycled", "parallelism": f"replicas x{world}"},
+                   "l2": f"inputs larger than L2: {LAYERS} layer caches ({LAYERS * DECODE_BYTES / 1e9:.2f} GB) cycled",
+                   "parallelism": f"replicas x{world}"},
         "steps_per_s": round(1e3 / ms_per_step, 1),
         "pct_of_peak": round(100.0 * value / peak, 2),
         "decode_us": round(dec_ms * 1e3, 2),
@@ -294,8 +302,7 @@ def run_gpu(args):
                      "kernel": "decode_kernel<int8,int8,256,8>", "bytes_per_launch": DECODE_BYTES,
                      "timing": "events around each launch in the timed graph" if per_launch
                      else "decode-only graph time / launches"},
-        "e2e": {"value": round(DECODE_BYTES / (e2e_ms / 1e3) / 1e9, 1), "unit": "GB/s",
-                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": e2e,
         "gpu_launches": 2 * nsteps,
         "clocks": clocks,
     }
@@ -373,7 +380,11 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--layers", type=int, default=8, help="layer caches cycled (8 keeps the working set >> L2)")
     args = ap.parse_args()
+    global LAYERS
+    LAYERS = max(1, args.layers)
     if args.impl == "reference":
         if args.steps > 10:
             args.steps = 10   # each oracle step is seconds of CPU work
