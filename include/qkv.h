@@ -132,23 +132,31 @@ QKV_API int iso_kv_append(const qkv_cache_desc* cache, const void* k, const void
 
 /*
  * kv_decode_attn -- decode attention, one query per sequence [S8 "What it
- * does"; K4 "How"]. q: bf16 [batch][num_q_heads][head_dim]; query head h reads
- * KV head h / (num_q_heads / num_kv_heads). Sequence b attends positions
- * [0, seq_lens[b]) (seq_lens: int32 device [batch]); under quantize-on-write the
- * caller appends the current token first. max_seq_len is a host-side upper
- * bound on seq_lens used to size the split-K schedule. out: [batch][num_q_heads]
- * [head_dim] in bf16 or fp32. scale is the softmax scale (usually
- * 1/sqrt(head_dim)). An empty sequence gives a zero output row.
+ * does"; K4 "How"], with optional quantize-on-write of the step's own token
+ * [FT "What": decode is quantize-on-write].
+ * q: bf16 [batch][num_q_heads][head_dim]; query head h reads KV head
+ * h / (num_q_heads / num_kv_heads). Sequence b attends positions
+ * [0, seq_lens[b]) (seq_lens: int32 device [batch]).
+ * k_new, v_new: NULL, or bf16 [batch][num_kv_heads][head_dim]: before
+ * attending, position seq_lens[b] - 1 of every sequence is quantized from them
+ * and written to the pool (the same bytes iso_kv_append writes), and the
+ * attention reads it back packed. With num_q_heads / num_kv_heads > 8 several
+ * blocks write the same row with identical bytes. Without them the caller
+ * appends the current token first.
+ * max_seq_len: host-side upper bound on seq_lens used to size the schedule.
+ * out: [batch][num_q_heads][head_dim] in bf16 or fp32. scale is the softmax
+ * scale (usually 1/sqrt(head_dim)). An empty sequence gives a zero row.
  * workspace: device scratch of at least kv_decode_workspace_size() bytes,
  * zero-filled before its first use; every call leaves its counter region
  * zeroed again. Calls sharing a workspace must not overlap in time.
+ * batch <= 1024; num_q_heads / num_kv_heads in {1, 2, 4} or a multiple of 8.
  */
 QKV_API size_t kv_decode_workspace_size(const qkv_cache_desc* cache, int batch, int num_q_heads, int max_seq_len);
 
-QKV_API int kv_decode_attn(const qkv_cache_desc* cache, const void* q, int batch, int num_q_heads,
-                   const int32_t* page_table, int max_pages_per_seq, const int32_t* seq_lens,
-                   int max_seq_len, float scale, void* out, int out_dtype, void* workspace,
-                   size_t workspace_bytes, void* stream);
+QKV_API int kv_decode_attn(const qkv_cache_desc* cache, const void* q, const void* k_new, const void* v_new,
+                           int batch, int num_q_heads, const int32_t* page_table, int max_pages_per_seq,
+                           const int32_t* seq_lens, int max_seq_len, float scale, void* out, int out_dtype,
+                           void* workspace, size_t workspace_bytes, void* stream);
 
 /* Human-readable text for a QKV_* return code. */
 QKV_API const char* qkv_strerror(int code);

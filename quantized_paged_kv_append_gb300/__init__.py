@@ -106,8 +106,12 @@ def decode_workspace(cache: PagedKVCache, batch: int, num_q_heads: int, max_seq_
 
 
 def decode(cache: PagedKVCache, q, page_table, seq_lens, max_seq_len: int, scale=None, out=None,
-           out_dtype=None, workspace=None, stream=None):
-    """Decode attention: q bf16 [B, Hq, D] -> out [B, Hq, D] (bf16 or fp32)."""
+           out_dtype=None, workspace=None, stream=None, k_new=None, v_new=None):
+    """Decode attention: q bf16 [B, Hq, D] -> out [B, Hq, D] (bf16 or fp32).
+
+    With k_new / v_new (bf16 [B, Hkv, D]) the step's own token is quantized and
+    written at position seq_lens[b] - 1 inside the same kernel launch
+    (quantize-on-write) before it is attended."""
     torch = _torch()
     B, Hq, D = q.shape
     if scale is None:
@@ -117,7 +121,8 @@ def decode(cache: PagedKVCache, q, page_table, seq_lens, max_seq_len: int, scale
     odt = _lib.QKV_OUT_F32 if out.dtype == torch.float32 else _lib.QKV_OUT_BF16
     if workspace is None:
         workspace = decode_workspace(cache, B, Hq, max_seq_len, device=q.device)
-    rc = _lib.lib().kv_decode_attn(C.byref(cache.desc), _ptr(q), B, Hq, _ptr(page_table), int(page_table.shape[1]),
+    rc = _lib.lib().kv_decode_attn(C.byref(cache.desc), _ptr(q), _ptr(k_new), _ptr(v_new), B, Hq, _ptr(page_table),
+                                   int(page_table.shape[1]),
                                    _ptr(seq_lens), int(max_seq_len), float(scale), _ptr(out), odt, _ptr(workspace),
                                    workspace.numel(), _stream(stream))
     _lib.check(rc, "kv_decode_attn")

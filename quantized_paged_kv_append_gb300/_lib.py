@@ -63,7 +63,7 @@ def lib():
         L.iso_kv_append.restype = I
         L.kv_decode_workspace_size.argtypes = [C.POINTER(CacheDesc), I, I, I]
         L.kv_decode_workspace_size.restype = SZ
-        L.kv_decode_attn.argtypes = [C.POINTER(CacheDesc), P, I, I, P, I, P, I, C.c_float, P, I, P, SZ, P]
+        L.kv_decode_attn.argtypes = [C.POINTER(CacheDesc), P, P, P, I, I, P, I, P, I, C.c_float, P, I, P, SZ, P]
         L.kv_decode_attn.restype = I
         L.qkv_strerror.argtypes = [I]
         L.qkv_strerror.restype = C.c_char_p

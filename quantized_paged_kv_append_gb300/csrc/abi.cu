@@ -282,9 +282,10 @@ size_t kv_decode_workspace_size(const qkv_cache_desc* cache, int batch, int num_
     return L.bytes;
 }
 
-int kv_decode_attn(const qkv_cache_desc* cache, const void* q, int batch, int num_q_heads, const int32_t* page_table,
-                   int max_pages_per_seq, const int32_t* seq_lens, int max_seq_len, float scale, void* out,
-                   int out_dtype, void* workspace, size_t workspace_bytes, void* stream) {
+int kv_decode_attn(const qkv_cache_desc* cache, const void* q, const void* k_new, const void* v_new, int batch,
+                   int num_q_heads, const int32_t* page_table, int max_pages_per_seq, const int32_t* seq_lens,
+                   int max_seq_len, float scale, void* out, int out_dtype, void* workspace, size_t workspace_bytes,
+                   void* stream) {
     int rc = check_desc(cache);
     if (rc) return rc;
     if (batch < 0 || max_seq_len < 0) return QKV_ERR_ARG;
@@ -293,6 +294,8 @@ int kv_decode_attn(const qkv_cache_desc* cache, const void* q, int batch, int nu
     if (!q || !page_table || !seq_lens || !out || max_pages_per_seq <= 0) return QKV_ERR_ARG;
     if (out_dtype != QKV_OUT_BF16 && out_dtype != QKV_OUT_F32) return QKV_ERR_ARG;
     if (!aligned16(q) || !aligned16(out)) return QKV_ERR_ARG;
+    if ((k_new == nullptr) != (v_new == nullptr)) return QKV_ERR_ARG;
+    if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return QKV_ERR_ARG;
     if (!std::isfinite(scale)) return QKV_ERR_ARG;
     int dev;
     if ((rc = device_setup(&dev))) return rc;
@@ -340,6 +343,8 @@ int kv_decode_attn(const qkv_cache_desc* cache, const void* q, int batch, int nu
     p.seg_cnt = (int*)(ws + L.off_seg);
     p.grp_cnt = (int*)(ws + L.off_grp);
     p.slot_floats = L.slot_floats;
+    p.k_new = (const uint16_t*)k_new;
+    p.v_new = (const uint16_t*)v_new;
     cudaError_t e = decode_launch(cache->format, D, L.G, grid, tk, tv, p, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e);
     return QKV_OK;

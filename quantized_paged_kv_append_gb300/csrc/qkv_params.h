@@ -40,6 +40,8 @@ struct DecodeParams {
     int* seg_cnt;        // [S]
     int* grp_cnt;        // [C + S]
     int slot_floats;     // 16 + 8 * D
+    const uint16_t* k_new;   // optional bf16 [B][Hkv][D]: quantize-on-write of position seq_lens[b] - 1
+    const uint16_t* v_new;
 };
 
 cudaError_t append_upload_levels(const float* lv3, const float* lv4);

@@ -80,8 +80,8 @@ def test_validation_rejects_before_launch(qlib):
 
     def call(desc=d, **kw):
         a = args(**kw)
-        return L.kv_decode_attn(desc, a["q"], a["B"], a["Hq"], a["pt"], a["mp"], a["sl"], a["msl"], a["scale"],
-                                a["out"], a["odt"], a["ws"], a["wsb"], None)
+        return L.kv_decode_attn(desc, a["q"], a.get("kn"), a.get("vn"), a["B"], a["Hq"], a["pt"], a["mp"], a["sl"],
+                                a["msl"], a["scale"], a["out"], a["odt"], a["ws"], a["wsb"], None)
 
     assert call(desc=None) == -1
     assert call(B=-1) == -1
@@ -90,6 +90,7 @@ def test_validation_rejects_before_launch(qlib):
     assert call(odt=5) == -1
     assert call(scale=float("nan")) == -1
     assert call(B=5000) == -8
+    assert call(kn=good) == -1            # k_new without v_new
 
 
 def test_strerror_covers_codes(qlib):

@@ -153,3 +153,32 @@ def test_decode_bad_page_entry_flags_without_fault(env, orc):
     qkv.decode(cache, bf16_dev(w.q, torch), to_dev(bad, torch), to_dev(w.lens, torch), 64, scale=w.scale)
     torch.cuda.synchronize()
     assert qkv.device_error() & 1
+
+
+@pytest.mark.parametrize("fmt,d,hkv,hq", [("int8", 256, 2, 16), ("k8v4", 256, 2, 16), ("iso3", 128, 4, 16),
+                                          ("iso4", 128, 4, 16), ("int8", 256, 2, 32), ("iso4", 256, 2, 4)])
+def test_decode_fused_quantize_on_write(env, orc, fmt, d, hkv, hq):
+    """kv_decode_attn with k_new/v_new: the newest token (position L - 1) is
+    quantized inside the decode launch. The pool bytes must equal the oracle's
+    append of all tokens, and the output the oracle's decode over them."""
+    torch, qkv = env
+    lens = [1, 37, 300, 16, 1000]
+    w = Workload(fmt, lens, hkv, hq, d, seed=31)
+    full = w.oracle_pool(orc)
+    ref = full.decode(w.q, w.table, w.lens, w.scale)
+    # the pool before the step: every token except each sequence's last one
+    last = np.cumsum(w.lens) - 1
+    keep = np.ones(w.seq_id.size, bool)
+    keep[last] = False
+    pre = orc.Pool(w.fmt, w.num_pages, w.hkv, w.d, quat=w.quat)
+    pre.append(w.k[keep], w.v[keep], w.seq_id[keep], w.pos[keep], w.table)
+    cache = gpu_cache(qkv, w, torch, planes=pre.planes())
+    out = qkv.decode(cache, bf16_dev(w.q, torch), to_dev(w.table, torch), to_dev(w.lens, torch), w.max_len(),
+                     scale=w.scale, out_dtype=torch.float32, k_new=bf16_dev(w.k[last], torch),
+                     v_new=bf16_dev(w.v[last], torch))
+    torch.cuda.synchronize()
+    assert qkv.device_error() == 0
+    for got, want, nm in zip([p.cpu().numpy() for p in cache.planes()], full.planes(), ["kc", "ks", "vc", "vs"]):
+        assert np.array_equal(got, want), nm
+    r = compare_attention(out.cpu().numpy(), ref)
+    assert r["ok"], r
