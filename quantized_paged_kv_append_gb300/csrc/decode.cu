@@ -24,8 +24,8 @@
 //     through shared memory) and half of the PV output columns. This halves the
 //     per-warp registers (accumulators, query fragments) so 16 warps fit.
 //   * QK^T and PV are warp-level fp16 tensor-core products (m16n8k16) on exact
-//     operands: int8 codes enter as 1152 + c (exact in fp16; the constant is
-//     removed once per group through the query sums / probability sums), q4 and
+//     operands: int8 K codes enter as 1152 + c (exact in fp16; the constant is
+//     removed per page and group through the query sums), V codes exactly, q4 and
 //     Lloyd-Max levels are exact fp16, the (rotated) query is split into fp16
 //     hi + lo rows, per-(token, group) scales multiply fp32 scores (K) or are
 //     folded into fp16 hi + lo probabilities (V). Online softmax in fp32 (base
@@ -97,7 +97,9 @@ struct Cfg {
     static constexpr bool VISO = (VENC == ENC_ISO3 || VENC == ENC_ISO4);
     static constexpr bool QLO = KISO;               // rotated query needs an fp16 lo part
     static constexpr bool KBIAS = (KENC == ENC_INT8);
-    static constexpr bool VBIAS = (VENC == ENC_INT8);
+    // V codes enter exactly (c, not 1152 + c): O accumulates over a whole page run, and a
+    // removed offset would amplify the accumulation rounding by ~1152 / |mean code|.
+    static constexpr bool VBIAS = false;
     static constexpr int KS = D / 16;               // k-steps over the head dimension
     static constexpr int KSH = KS / 2;              // per warp of a pair
     static constexpr int KSPG = group_size(KENC) / 16;
@@ -683,8 +685,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t wa = (u < 2) ? va.x : va.y, wb = (u < 2) ? vb.x : vb.y;
                         const uint32_t wc = (u < 2) ? vc2.x : vc2.y, wd = (u < 2) ? vd.x : vd.y;
                         const int bi = (2 * u) & 3;
-                        const uint32_t a0 = i8pair_to_h2_biased(wa, wb, bi), a1 = i8pair_to_h2_biased(wa, wb, bi + 1);
-                        const uint32_t a2 = i8pair_to_h2_biased(wc, wd, bi), a3 = i8pair_to_h2_biased(wc, wd, bi + 1);
+                        const uint32_t a0 = hsub2_u32(i8pair_to_h2_biased(wa, wb, bi), 0x64806480u);
+                        const uint32_t a1 = hsub2_u32(i8pair_to_h2_biased(wa, wb, bi + 1), 0x64806480u);
+                        const uint32_t a2 = hsub2_u32(i8pair_to_h2_biased(wc, wd, bi), 0x64806480u);
+                        const uint32_t a3 = hsub2_u32(i8pair_to_h2_biased(wc, wd, bi + 1), 0x64806480u);
                         const int ml = q * 4 + u;
                         mma_f16_16816(oacc[ml], a0, a1, a2, a3, bA0, bA1);
                         if constexpr (G > 4 && PLO) mma_f16_16816(oacc[ml], a0, a1, a2, a3, bB0, bB1);

@@ -62,6 +62,16 @@ def gpu_cache(qkv, w, torch, planes=None):
     return qkv.PagedKVCache(w.fmt, w.num_pages, w.hkv, w.d, quat=w.quat.tolist(), planes=dev)
 
 
+def _log_metrics(res):
+    import json
+    import os
+    path = os.environ.get("QKV_PARITY_LOG")
+    if path:
+        test = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+        with open(path, "a") as f:
+            f.write(json.dumps(dict(res, test=test, ok=bool(res["ok"]))) + "\n")
+
+
 def compare_attention(gpu, ref, atol=2e-3, cos_min=0.9999, bf16=False):
     """max-abs and cosine against the double-precision oracle. fp32 output is
     held to |err| <= atol; bf16 output to atol + 2^-8 |ref| (half a bf16 ulp
@@ -77,5 +87,7 @@ def compare_attention(gpu, ref, atol=2e-3, cos_min=0.9999, bf16=False):
     den = np.linalg.norm(rows_g, axis=1) * np.linalg.norm(rows_r, axis=1)
     nz = den > 0
     cos = num[nz] / den[nz]
-    return {"max_abs": float(err.max()) if err.size else 0.0, "excess": worst,
-            "min_cos": float(cos.min()) if cos.size else 1.0, "ok": worst <= 0 and (cos.size == 0 or cos.min() > cos_min)}
+    res = {"max_abs": float(err.max()) if err.size else 0.0, "excess": worst,
+           "min_cos": float(cos.min()) if cos.size else 1.0, "ok": worst <= 0 and (cos.size == 0 or cos.min() > cos_min)}
+    _log_metrics(res)
+    return res
