@@ -158,6 +158,28 @@ QKV_API int kv_decode_attn(const qkv_cache_desc* cache, const void* q, const voi
                            const int32_t* seq_lens, int max_seq_len, float scale, void* out, int out_dtype,
                            void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * kv_extend_attn -- extend (prefill-chunk) attention [FT "What": extend attends
+ * the packed prefix plus the bf16 new tokens and packs them after attention;
+ * S8 "What it does": prompt chunks dequantize the cache on the fly].
+ * For sequence b the chunk's new tokens are rows [cu_seqlens[b],
+ * cu_seqlens[b+1]) of q (bf16 [total][num_q_heads][head_dim]) and of k_new /
+ * v_new (bf16 [total][num_kv_heads][head_dim]); its packed prefix is positions
+ * [0, prefix_lens[b]) of the pool. New token i attends the dequantized prefix
+ * and the raw bf16 new tokens 0..i (causal != 0) or all of them (causal == 0).
+ * cu_seqlens (int32 [batch + 1]) and prefix_lens (int32 [batch]) are device
+ * arrays; max_q_len is a host upper bound on the per-sequence new-token count.
+ * out: [total][num_q_heads][head_dim], bf16 or fp32. The caller packs the new
+ * tokens afterwards with iso_kv_append (deferred packing). No workspace.
+ * This build covers the int8 format, head_dim 128 or 256, num_q_heads /
+ * num_kv_heads in {1, 2, 4} or a multiple of 8; other requests return
+ * QKV_ERR_UNSUPPORTED.
+ */
+QKV_API int kv_extend_attn(const qkv_cache_desc* cache, const void* q, const void* k_new, const void* v_new,
+                           int num_q_heads, const int32_t* cu_seqlens, const int32_t* prefix_lens, int batch,
+                           int max_q_len, const int32_t* page_table, int max_pages_per_seq, float scale, int causal,
+                           void* out, int out_dtype, void* stream);
+
 /* Human-readable text for a QKV_* return code. */
 QKV_API const char* qkv_strerror(int code);
 

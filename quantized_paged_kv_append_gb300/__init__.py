@@ -15,7 +15,8 @@ import math
 from . import _lib
 from ._lib import FORMATS, QKV_INT8, QKV_K8V4, QKV_ISO3, QKV_ISO4, QkvError  # noqa: F401
 
-__all__ = ["PagedKVCache", "append", "decode", "decode_workspace", "row_bytes", "iso_levels", "device_error"]
+__all__ = ["PagedKVCache", "append", "decode", "decode_workspace", "extend", "row_bytes", "iso_levels",
+           "device_error"]
 
 
 def _torch():
@@ -126,4 +127,24 @@ def decode(cache: PagedKVCache, q, page_table, seq_lens, max_seq_len: int, scale
                                    _ptr(seq_lens), int(max_seq_len), float(scale), _ptr(out), odt, _ptr(workspace),
                                    workspace.numel(), _stream(stream))
     _lib.check(rc, "kv_decode_attn")
+    return out
+
+
+def extend(cache: PagedKVCache, q, k_new, v_new, cu_seqlens, prefix_lens, page_table, max_q_len: int, scale=None,
+           causal=True, out=None, out_dtype=None, stream=None):
+    """Extend attention: q bf16 [total, Hq, D], k_new / v_new bf16 [total, Hkv, D]
+    (rows of sequence b are cu_seqlens[b]..cu_seqlens[b+1]) over the packed
+    prefix [0, prefix_lens[b]) plus the new tokens. Returns out [total, Hq, D]."""
+    torch = _torch()
+    total, Hq, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((total, Hq, D), dtype=out_dtype or torch.bfloat16, device=q.device)
+    odt = _lib.QKV_OUT_F32 if out.dtype == torch.float32 else _lib.QKV_OUT_BF16
+    rc = _lib.lib().kv_extend_attn(C.byref(cache.desc), _ptr(q), _ptr(k_new), _ptr(v_new), Hq, _ptr(cu_seqlens),
+                                   _ptr(prefix_lens), int(prefix_lens.numel()), int(max_q_len), _ptr(page_table),
+                                   int(page_table.shape[1]), float(scale), int(bool(causal)), _ptr(out), odt,
+                                   _stream(stream))
+    _lib.check(rc, "kv_extend_attn")
     return out

@@ -350,6 +350,54 @@ int kv_decode_attn(const qkv_cache_desc* cache, const void* q, const void* k_new
     return QKV_OK;
 }
 
+int kv_extend_attn(const qkv_cache_desc* cache, const void* q, const void* k_new, const void* v_new, int num_q_heads,
+                   const int32_t* cu_seqlens, const int32_t* prefix_lens, int batch, int max_q_len,
+                   const int32_t* page_table, int max_pages_per_seq, float scale, int causal, void* out,
+                   int out_dtype, void* stream) {
+    int rc = check_desc(cache);
+    if (rc) return rc;
+    if (batch < 0 || max_q_len < 0) return QKV_ERR_ARG;
+    if (batch == 0 || max_q_len == 0) return QKV_OK;
+    if (!q || !k_new || !v_new || !cu_seqlens || !prefix_lens || !page_table || !out || max_pages_per_seq <= 0)
+        return QKV_ERR_ARG;
+    if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(out)) return QKV_ERR_ARG;
+    if (out_dtype != QKV_OUT_BF16 && out_dtype != QKV_OUT_F32) return QKV_ERR_ARG;
+    if (!std::isfinite(scale)) return QKV_ERR_ARG;
+    if (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads) return QKV_ERR_GQA;
+    const int Gtot = num_q_heads / cache->num_kv_heads;
+    if (!(Gtot == 1 || Gtot == 2 || Gtot == 4 || Gtot % 8 == 0)) return QKV_ERR_GQA;
+    if (cache->format != QKV_INT8) return QKV_ERR_UNSUPPORTED;
+    int dev;
+    if ((rc = device_setup(&dev))) return rc;
+    const int G = Gtot >= 8 ? 8 : Gtot;
+    ExtendParams p;
+    p.kc = (const uint8_t*)cache->k_codes;
+    p.ks = (const uint8_t*)cache->k_scales;
+    p.vc = (const uint8_t*)cache->v_codes;
+    p.vs = (const uint8_t*)cache->v_scales;
+    p.num_pages = cache->num_pages;
+    p.Hkv = cache->num_kv_heads;
+    p.q = (const uint16_t*)q;
+    p.k_new = (const uint16_t*)k_new;
+    p.v_new = (const uint16_t*)v_new;
+    p.Hq = num_q_heads;
+    p.Gtot = Gtot;
+    p.cu = cu_seqlens;
+    p.prefix_lens = prefix_lens;
+    p.B = batch;
+    p.page_table = page_table;
+    p.max_pages = max_pages_per_seq;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.causal = causal != 0;
+    p.out = out;
+    p.out_f32 = out_dtype == QKV_OUT_F32;
+    const int NH = cache->num_kv_heads * (Gtot / G);
+    cudaError_t e = extend_launch(cache->format, cache->head_dim, G, max_q_len, NH, batch, p, (cudaStream_t)stream);
+    if (e == cudaErrorInvalidValue) return QKV_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return cuda_fail(e);
+    return QKV_OK;
+}
+
 const char* qkv_strerror(int code) {
     switch (code) {
         case QKV_OK: return "ok";
@@ -373,7 +421,10 @@ int qkv_device_error(int clear) {
     if (e != cudaSuccess) return cuda_fail(e);
     e = decode_read_error(&b, clear != 0);
     if (e != cudaSuccess) return cuda_fail(e);
-    return (int)(a | b);
+    unsigned x = 0;
+    e = extend_read_error(&x, clear != 0);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return (int)(a | b | x);
 }
 
 }  // extern "C"

@@ -44,6 +44,27 @@ struct DecodeParams {
     const uint16_t* v_new;
 };
 
+struct ExtendParams {
+    const uint8_t* kc;
+    const uint8_t* ks;
+    const uint8_t* vc;
+    const uint8_t* vs;
+    int num_pages, Hkv;
+    const uint16_t* q;       // bf16 [Tsum][Hq][D]
+    const uint16_t* k_new;   // bf16 [Tsum][Hkv][D]
+    const uint16_t* v_new;
+    int Hq, Gtot;
+    const int32_t* cu;           // [B + 1] new-token offsets
+    const int32_t* prefix_lens;  // [B]
+    int B;
+    const int32_t* page_table;
+    int max_pages;
+    float scale_log2;
+    int causal;
+    void* out;
+    int out_f32;
+};
+
 cudaError_t append_upload_levels(const float* lv3, const float* lv4);
 cudaError_t append_read_error(unsigned* out, bool clear);
 cudaError_t append_launch(int fmt, int D, const AppendParams& p, cudaStream_t st);
@@ -53,6 +74,9 @@ cudaError_t decode_read_error(unsigned* out, bool clear);
 cudaError_t decode_launch(int fmt, int D, int G, int grid, const CUtensorMap& tk, const CUtensorMap& tv,
                           const DecodeParams& p, cudaStream_t st);
 int decode_heads_per_cta(int Gtot);
+
+cudaError_t extend_read_error(unsigned* out, bool clear);
+cudaError_t extend_launch(int fmt, int D, int G, int max_q_len, int NH, int B, const ExtendParams& p, cudaStream_t st);
 int decode_max_batch();
 
 }  // namespace qkv
