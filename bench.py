@@ -86,6 +86,28 @@ def _clock_summary(proc, path, gpu_index):
             "samples": len(sm)}
 
 
+def rank_env():
+    """(world, rank, local_rank) from the torchrun environment (1, 0, 0 alone)."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(value, world, device="cpu"):
+    """The largest `value` over all ranks (identity when alone)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(bytes_per_step, steps_per_rank, world, elapsed_ms):
+    """Whole-job GB/s: every rank's steps over the slowest rank's time."""
+    return bytes_per_step * steps_per_rank * world / (elapsed_ms / 1e3) / 1e9
+
+
 _INPUT_CACHE = {}
 
 
@@ -114,9 +136,7 @@ def run_gpu(args):
     import quantized_paged_kv_append_gb300 as qkv
     from quantized_paged_kv_append_gb300 import build as qbuild
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = rank_env()
     if world > 1:
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
@@ -233,14 +253,10 @@ def run_gpu(args):
         dec_ms = d0.elapsed_time(d1) / args.steps
     torch.cuda.synchronize()
     clocks = _clock_summary(proc, cpath, local)
-    total_ms = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(t0.elapsed_time(t1), world, device=dev)
     nsteps = args.steps * reps
     ms_per_step = total_ms / nsteps
-    value = DECODE_BYTES * nsteps * world / (total_ms / 1e3) / 1e9
+    value = job_throughput(DECODE_BYTES, nsteps, world, total_ms)
 
     e2e = None
     if not args.no_e2e:

@@ -1,0 +1,126 @@
+"""GPU parity of extend (prefill-chunk) attention over a packed prefix plus
+bf16 new tokens, against the CPU oracle (double precision). Tolerance as for
+decode: fp32 output within max-abs 2e-3 and cosine > 0.9999."""
+
+import numpy as np
+import pytest
+
+from _workload import Workload, bf16_dev, compare_attention, gpu_cache, to_dev
+from quantized_paged_kv_append_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import quantized_paged_kv_append_gb300 as qkv
+    from quantized_paged_kv_append_gb300 import build
+    build.build()
+    return torch, qkv
+
+
+def _case(orc, prefix, chunk, hkv, hq, d, seed, spare_pages=2):
+    """Pool holding `prefix[b]` packed tokens per sequence (table sized for
+    prefix + chunk), plus the chunk's bf16 q / k_new / v_new."""
+    total_pages = [max(1, (p + c + 15) // 16) for p, c in zip(prefix, chunk)]
+    w = Workload("int8", prefix, hkv, hq, d, seed=seed)
+    table, npages = synth.page_table(seed, total_pages, num_pages=sum(total_pages) + spare_pages)
+    w.table, w.num_pages = table, npages
+    pool = orc.Pool(0, npages, hkv, d)
+    if w.seq_id.size:
+        pool.append(w.k, w.v, w.seq_id, w.pos, table)
+    T = int(sum(chunk))
+    q = synth.tensor_bf16(seed, "q", (T, hq, d))
+    kn = synth.tensor_bf16(seed, "k_new", (T, hkv, d), outlier_scale=20.0)
+    vn = synth.tensor_bf16(seed, "v_new", (T, hkv, d))
+    cu = np.concatenate([[0], np.cumsum(chunk)]).astype(np.int32)
+    return w, pool, table, q, kn, vn, cu, np.asarray(prefix, np.int32)
+
+
+def _run(torch, qkv, w, pool, table, q, kn, vn, cu, pre, causal=True, out_dtype=None, scale=None):
+    cache = gpu_cache(qkv, w, torch, planes=pool.planes())
+    chunk = np.diff(cu)
+    out = qkv.extend(cache, bf16_dev(q, torch), bf16_dev(kn, torch), bf16_dev(vn, torch), to_dev(cu, torch),
+                     to_dev(pre, torch), to_dev(table, torch), int(chunk.max()), scale=scale, causal=causal,
+                     out_dtype=out_dtype or torch.float32)
+    torch.cuda.synchronize()
+    assert qkv.device_error() == 0
+    return out.float().cpu().numpy()
+
+
+@pytest.mark.parametrize("prefix,chunk,hkv,hq,d", [
+    ([100], [37], 2, 16, 256),
+    ([0], [45], 2, 16, 256),
+    ([64], [64], 2, 16, 256),
+    ([0, 200, 33], [20, 70, 1], 2, 16, 256),
+    ([150], [40], 2, 8, 256),
+    ([90], [33], 4, 4, 128),
+    ([77], [19], 2, 32, 128),
+    ([130], [50], 1, 2, 256),
+])
+def test_extend_small(env, orc, prefix, chunk, hkv, hq, d):
+    torch, qkv = env
+    w, pool, table, q, kn, vn, cu, pre = _case(orc, prefix, chunk, hkv, hq, d, seed=41)
+    scale = float(np.float32(1.0 / np.sqrt(d)))
+    ref = pool.extend(q, kn, vn, cu, pre, table, scale, causal=True)
+    got = _run(torch, qkv, w, pool, table, q, kn, vn, cu, pre, scale=scale)
+    r = compare_attention(got, ref)
+    assert r["ok"], r
+
+
+def test_extend_non_causal_and_bf16(env, orc):
+    torch, qkv = env
+    w, pool, table, q, kn, vn, cu, pre = _case(orc, [120, 5], [30, 66], 2, 16, 256, seed=42)
+    scale = float(np.float32(1.0 / 16))
+    ref = pool.extend(q, kn, vn, cu, pre, table, scale, causal=False)
+    got = _run(torch, qkv, w, pool, table, q, kn, vn, cu, pre, causal=False, scale=scale)
+    assert compare_attention(got, ref)["ok"]
+    refc = pool.extend(q, kn, vn, cu, pre, table, scale, causal=True)
+    gotb = _run(torch, qkv, w, pool, table, q, kn, vn, cu, pre, out_dtype=torch.bfloat16, scale=scale)
+    r = compare_attention(gotb, refc, bf16=True)
+    assert r["ok"], r
+
+
+def test_extend_serving_chunk_sampled(env, orc):
+    """The serving-step chunk: 2048 new tokens over a 32768-token prefix,
+    Hq 16 / Hkv 2, D 256; the oracle computes a sample of rows one by one."""
+    torch, qkv = env
+    w, pool, table, q, kn, vn, cu, pre = _case(orc, [32768], [2048], 2, 16, 256, seed=0)
+    scale = float(np.float32(1.0 / 16))
+    got = _run(torch, qkv, w, pool, table, q, kn, vn, cu, pre, scale=scale)
+    rows = np.array([0, 1, 15, 16, 127, 128, 1000, 2046, 2047], np.int32)
+    ref = pool.extend(q, kn, vn, cu, pre, table, scale, causal=True, rows=rows)
+    r = compare_attention(got[rows], ref)
+    assert r["ok"], r
+
+
+def test_extend_then_deferred_pack_matches_oracle(env, orc):
+    """After extend, the chunk is packed with append (deferred packing): the
+    planes equal the oracle's append of prefix + chunk."""
+    torch, qkv = env
+    w, pool, table, q, kn, vn, cu, pre = _case(orc, [40], [30], 2, 16, 256, seed=43)
+    cache = gpu_cache(qkv, w, torch, planes=pool.planes())
+    qkv.extend(cache, bf16_dev(q, torch), bf16_dev(kn, torch), bf16_dev(vn, torch), to_dev(cu, torch),
+               to_dev(pre, torch), to_dev(table, torch), 30)
+    seq = np.zeros(30, np.int32)
+    pos = (40 + np.arange(30)).astype(np.int32)
+    qkv.append(cache, bf16_dev(kn, torch), bf16_dev(vn, torch), to_dev(seq, torch), to_dev(pos, torch),
+               to_dev(table, torch))
+    torch.cuda.synchronize()
+    pool.append(kn, vn, seq, pos, table)
+    for g, r in zip([p.cpu().numpy() for p in cache.planes()], pool.planes()):
+        assert np.array_equal(g, r)
+
+
+def test_extend_rejects_other_formats(env):
+    torch, qkv = env
+    c = qkv.PagedKVCache("k8v4", 4, 2, 256)
+    z = torch.zeros((4, 16, 256), dtype=torch.bfloat16, device="cuda")
+    zk = torch.zeros((4, 2, 256), dtype=torch.bfloat16, device="cuda")
+    i32 = lambda a: torch.tensor(a, dtype=torch.int32, device="cuda")
+    with pytest.raises(qkv.QkvError) as e:
+        qkv.extend(c, z, zk, zk, i32([0, 4]), i32([0]), i32([[0, 1, 2, 3]]), 4)
+    assert e.value.code == -8
