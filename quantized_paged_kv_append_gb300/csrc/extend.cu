@@ -397,6 +397,7 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(const ExtendParams
             const int buf = j & 1;
             const bool prefix = j < NTP;
             const float* sg = sig + buf * 64 * 4;
+            wait(B_KVF0 + buf, (j >> 1) & 1);   // the producers' key scales of this tile
             wait(B_SFULL, j & 1);
             tc_fence_after();
             float s[kXT];
@@ -433,27 +434,33 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(const ExtendParams
             // PV(j - 1) must be done before P is overwritten and before O is rescaled
             if (j >= 1) wait(B_PVDONE, (j - 1) & 1);
             tc_fence_after();
-            if (rmax > m_used + 8.0f) {
-                const float alpha = (m_used == -INFINITY) ? 0.0f : exp2f(m_used - rmax);
-                if (j >= 1 && m_used != -INFINITY) {
-#pragma unroll 1
-                    for (int c = 0; c < D / 16; ++c) {
-                        float v[16];
-                        tmem_ld16(tmem_O + lane_base + 16 * c, v);
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) v[e] *= alpha;
-                        tmem_st16(tmem_O + lane_base + 16 * c, v);
-                    }
-                }
+            // frame update per row; the TMEM rescale of O is a whole-warp operation
+            // (tcgen05.ld/st are .sync.aligned), so it runs warp-uniformly with
+            // factor 1 for rows whose frame did not move
+            const bool move = rmax > m_used + 8.0f;
+            float alpha = 1.0f;
+            if (move) {
+                alpha = (m_used == -INFINITY) ? 0.0f : fast_exp2(m_used - rmax);
                 l *= alpha;
                 m_used = rmax;
             }
+            if (j >= 1 && __any_sync(0xffffffffu, move)) {
+#pragma unroll 1
+                for (int c = 0; c < D / 16; ++c) {
+                    float v[16];
+                    tmem_ld16(tmem_O + lane_base + 16 * c, v);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) v[e] *= alpha;
+                    tmem_st16(tmem_O + lane_base + 16 * c, v);
+                }
+            }
+            const float mref = (m_used == -INFINITY) ? 0.0f : m_used;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 uint32_t h[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    const float p0 = exp2f(s[8 * c + 2 * u] - m_used), p1 = exp2f(s[8 * c + 2 * u + 1] - m_used);
+                    const float p0 = fast_exp2(s[8 * c + 2 * u] - mref), p1 = fast_exp2(s[8 * c + 2 * u + 1] - mref);
                     h[u] = f32x2_to_h2(p0, p1);
                     const float2 f = h2_to_f32x2(h[u]);
                     l += f.x + f.y;
