@@ -180,6 +180,29 @@ QKV_API int kv_extend_attn(const qkv_cache_desc* cache, const void* q, const voi
                            int max_q_len, const int32_t* page_table, int max_pages_per_seq, float scale, int causal,
                            void* out, int out_dtype, void* stream);
 
+/*
+ * kv_decode_attn_noalloc -- kv_decode_attn without a caller-provided workspace.
+ * The reference pages have no counterpart to this entry point; it exists for
+ * callers that cannot allocate device memory: code running while a stream is
+ * captured into a CUDA graph (allocation is not allowed during capture), hosts
+ * whose device memory is owned by another pool or framework, and loops that
+ * must never allocate. The library allocates nothing here either: it uses a
+ * fixed 8 MiB scratch array in static device memory, reserved on every GPU that
+ * loads the library until the process exits.
+ * Arguments and results are those of kv_decode_attn. A request whose workspace
+ * (kv_decode_workspace_size) exceeds 8 MiB returns QKV_ERR_WORKSPACE and
+ * launches nothing. Each call clears the scratch span it uses on `stream`
+ * first. All calls on a device share the one array, so calls that can overlap
+ * on the GPU (different streams, or threads without ordering) race and must
+ * not be issued. The first call on each device resolves the array's device
+ * address (cudaGetSymbolAddress); make that first call before any stream
+ * capture.
+ */
+QKV_API int kv_decode_attn_noalloc(const qkv_cache_desc* cache, const void* q, const void* k_new, const void* v_new,
+                                   int batch, int num_q_heads, const int32_t* page_table, int max_pages_per_seq,
+                                   const int32_t* seq_lens, int max_seq_len, float scale, void* out, int out_dtype,
+                                   void* stream);
+
 /* Human-readable text for a QKV_* return code. */
 QKV_API const char* qkv_strerror(int code);
 
