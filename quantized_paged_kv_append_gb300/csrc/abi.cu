@@ -197,7 +197,7 @@ struct DecodeLayout {
     int S;          // segments
     int Cmax;       // CTA upper bound
     int slot_floats;
-    size_t off_p2, off_seg, off_grp, bytes;
+    size_t off_p2, off_seg, off_grp, off_rec, bytes;
 };
 
 int decode_layout(const qkv_cache_desc* d, int batch, int num_q_heads, int sms, DecodeLayout* L) {
@@ -215,7 +215,8 @@ int decode_layout(const qkv_cache_desc* d, int batch, int num_q_heads, int sms, 
     L->off_p2 = part;
     L->off_seg = 2 * part;
     L->off_grp = L->off_seg + al((size_t)L->S * sizeof(int));
-    L->bytes = L->off_grp + al(slots * sizeof(int));
+    L->off_rec = L->off_grp + al(slots * sizeof(int));
+    L->bytes = L->off_rec + al((size_t)L->Cmax * 8 * sizeof(int));
     return QKV_OK;
 }
 
@@ -342,10 +343,12 @@ int kv_decode_attn(const qkv_cache_desc* cache, const void* q, const void* k_new
     p.part2 = (float*)(ws + L.off_p2);
     p.seg_cnt = (int*)(ws + L.off_seg);
     p.grp_cnt = (int*)(ws + L.off_grp);
+    p.rec = (int*)(ws + L.off_rec);
     p.slot_floats = L.slot_floats;
     p.k_new = (const uint16_t*)k_new;
     p.v_new = (const uint16_t*)v_new;
-    cudaError_t e = decode_launch(cache->format, D, L.G, grid, tk, tv, p, (cudaStream_t)stream);
+    cudaError_t e = cache->format == QKV_INT8 ? decode_tc_launch(D, L.G, grid, tk, tv, p, (cudaStream_t)stream)
+                                              : decode_launch(cache->format, D, L.G, grid, tk, tv, p, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e);
     return QKV_OK;
 }
@@ -421,10 +424,12 @@ int qkv_device_error(int clear) {
     if (e != cudaSuccess) return cuda_fail(e);
     e = decode_read_error(&b, clear != 0);
     if (e != cudaSuccess) return cuda_fail(e);
-    unsigned x = 0;
+    unsigned x = 0, t = 0;
     e = extend_read_error(&x, clear != 0);
     if (e != cudaSuccess) return cuda_fail(e);
-    return (int)(a | b | x);
+    e = decode_tc_read_error(&t, clear != 0);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return (int)(a | b | x | t);
 }
 
 }  // extern "C"

@@ -1,0 +1,917 @@
+// decode_tc.cu -- paged decode attention over an int8 KV cache on tcgen05 tensor
+// cores (TMEM accumulators), with the newest token's quantize-on-write fused in.
+//
+// Method (page title, section): "qwen35/q36: --kv - int8 K/V caches", "What it
+// does" (int8 K/V planes, one fp16 absmax/127 scale per 64 values, dequantized on
+// the fly by the attention kernels; the decode step quantizes the new token into
+// its page before attending); "Paged KV-cache decode with a split-K partial
+// softmax merge", "Algorithm" (each thread block attends a contiguous range of
+// one sequence's pages and the partial results are merged with the log-sum-exp
+// rule).
+//
+// GB300 design (one CTA of 14 warps per SM, persistent over an equal share of
+// the (sequence, KV-head group, page) units -- stream-K):
+//   * tile = 8 pages = 128 tokens of one (sequence, head group);
+//   * warp 12 (producer) stages the int8 code planes of each tile with 2-D TMA
+//     (128-byte swizzle) and the scale rows with bulk copies, two tiles deep;
+//     it also quantizes the newest token into the pool and the staged copy;
+//   * warps 4-11 (converters) turn int8 codes into exact fp16: K as 1152 + c
+//     straight into TMEM (the A operand of Q K^T, one token per TMEM lane), V
+//     as c into an MN-major shared-memory tile (the A operand of V^T P);
+//   * warp 13 (one thread) issues tcgen05.mma: S_g = K'_g Q_g^T per 64-dim
+//     scale group g (M = 128 tokens, N = 16 query columns; 16 MMAs per tile at
+//     D = 256) and O += P'^T V' (M = 64 P' columns: 16 per scale group = 8
+//     heads hi + lo, N = D, K = 16 tokens; 8 MMAs per tile). Small MMAs cost
+//     about the same issue time whatever their N, so the tile is laid out to
+//     need as few instructions as possible;
+//   * warps 0-3 (softmax) own one token each: they combine the group scores in
+//     fp32 with the exact K scales (removing the 1152 offset through the query
+//     sums), run a lazy online softmax (the frame max moves only when a score
+//     exceeds it by 2^8; all four warps agree on it once per tile), and write P'
+//     = p * V-scale * 2^E as fp16 hi + lo parts;
+//   * pieces that do not cover a whole sequence are merged through the caller's
+//     workspace by the last-arriving CTA (atomic ticket, two levels).
+#include "qkv_device.cuh"
+#include "qkv_params.h"
+#include "quant_rows.cuh"
+#include "tcgen05.cuh"
+
+namespace qkv {
+
+__device__ unsigned int g_err_dtc;
+
+namespace {
+
+constexpr int kTok = 128;                   // tokens per tile
+constexpr int kTP = kTok / kPage;           // pages per tile
+constexpr int kSoftW = 4, kConvW = 8;
+constexpr int kWProd = kSoftW + kConvW;     // producer warp
+constexpr int kWMma = kWProd + 1;           // MMA warp
+constexpr int kThr = (kWMma + 1) * 32;      // 448 threads
+
+template <int D>
+struct TG {
+    static constexpr int NA = D / 64;             // 64-dim atoms = int8 scale groups
+    static constexpr int NHf = D / 128;           // PV halves of 128 dims
+    static constexpr int PAGE_B = D * kPage;      // staged codes of one page: D / 128 boxes of 2048 B
+    static constexpr int SC_B = kPage * 2 * NA;   // staged scales of one page
+    static constexpr int OFF_KST = 0;                               // [2][8][PAGE_B]
+    static constexpr int OFF_VST = OFF_KST + 2 * kTP * PAGE_B;      // [2][8][PAGE_B]
+    static constexpr int OFF_VP = OFF_VST + 2 * kTP * PAGE_B;       // V' [NA][128 rows][128 B]
+    static constexpr int OFF_PP = OFF_VP + NA * 16384;              // P' [128 rows][128 B]
+    static constexpr int OFF_Q = OFF_PP + 16384;                    // Q [NA][16 rows][128 B]
+    static constexpr int OFF_KSC = OFF_Q + NA * 2048;               // [2][8][SC_B]
+    static constexpr int OFF_VSC = OFF_KSC + 2 * kTP * SC_B;        // [2][8][SC_B]
+    static constexpr int OFF_BIAS = OFF_VSC + 2 * kTP * SC_B;       // float [NA][8]
+    static constexpr int OFF_RED = OFF_BIAS + 256;                  // softmax-warp reductions
+    static constexpr int OFF_ROW = OFF_RED + 512;                   // quantize-on-write rows [2][512]
+    static constexpr int OFF_BAR = OFF_ROW + 1024;
+    static constexpr int OFF_MISC = OFF_BAR + 32 * 8;
+    static constexpr int SMEM = OFF_MISC + 64;
+    static constexpr int KCOL = 0;                     // K' columns: D / 2 (fp16 pairs)
+    static constexpr int SCOL = D / 2;                 // two score buffers of NA x 16 columns
+    static constexpr int OCOL = SCOL + 2 * NA * 16;    // O (M = 64 rows in lanes 32 (r / 16) + r % 16, N = D)
+    static constexpr int TCOLS = (OCOL + D) <= 256 ? 256 : 512;
+    static_assert(OCOL + D <= 512, "TMEM budget");
+    static_assert(SMEM + 1024 <= 232448 - 1024, "shared memory budget");
+    static_assert(2 * kTP * SC_B <= 4096, "scale staging");
+};
+
+enum {
+    B_KF = 0,    // [2] K codes + K scales of a tile landed (2 arrivals + tx)
+    B_KE = 2,    // [2] K slot free (8 converter warps + 4 softmax warps)
+    B_VF = 4,    // [2]
+    B_VE = 6,    // [2]
+    B_KCV = 8,   // K' written to TMEM (8 converter warps)
+    B_VCV = 9,   // V' written (8 converter warps)
+    B_QKD = 10,  // [2] QK^T of a tile complete (commit)
+    B_PVD = 12,  // [2] PV of a tile complete (commit)
+    B_SF = 16,   // [2] score buffer read (4 softmax warps)
+    B_PFL = 18,  // P' written (4 softmax warps)
+    B_QRD = 19,  // query tile of a piece written (1)
+    B_PAT = 20,  // producer: the newest token's page landed (1 + tx)
+    B_N = 21
+};
+static_assert(B_N <= 32, "barrier area holds 32 barriers");
+
+__device__ __forceinline__ void soft_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ float exp2i(int n) { return __int_as_float((n + 127) << 23); }
+// position inside an aligned group of 4 <-> dimension: the converters emit (d0, d2), (d1, d3)
+__device__ __forceinline__ int perm4(int e) { return (e & ~3) | ((e & 1) << 1) | ((e >> 1) & 1); }
+
+__device__ __forceinline__ int seq_len_clamped(const DecodeParams& p, int b) {
+    return max(0, min(p.seq_lens[b], p.max_pages * kPage));
+}
+
+struct Piece {
+    int b, hg, p0, p1, L;
+    long long soff, np;
+};
+
+// The CTA's pieces, in order: contiguous page ranges of one (sequence, head group).
+struct Walker {
+    int b;
+    long long pref, x, end;
+    __device__ bool next(const DecodeParams& p, Piece& pc) {
+        while (x < end && b < p.B) {
+            const int L = seq_len_clamped(p, b);
+            const long long np = (L + kPage - 1) / kPage;
+            const long long seg0 = pref * p.NH;
+            if (np == 0 || x >= seg0 + np * p.NH) {
+                pref += np;
+                ++b;
+                continue;
+            }
+            const int hg = (int)((x - seg0) / np);
+            const long long soff = seg0 + (long long)hg * np;
+            const long long xe = min(end, soff + np);
+            pc.b = b;
+            pc.hg = hg;
+            pc.p0 = (int)(x - soff);
+            pc.p1 = (int)(xe - soff);
+            pc.L = L;
+            pc.soff = soff;
+            pc.np = np;
+            x = xe;
+            return true;
+        }
+        return false;
+    }
+};
+
+__device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity) {
+    if (mbar_wait_bounded(bar, parity)) return true;
+    atomicOr(&g_err_dtc, kErrWait);
+    return false;
+}
+
+template <int D, int G>
+__device__ void write_out(const DecodeParams& p, int b, int hq0, int i, float v) {
+    const size_t o = ((size_t)b * p.Hq + hq0) * D + i;
+    if (p.out_f32) reinterpret_cast<float*>(p.out)[o] = v;
+    else reinterpret_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(v);
+}
+
+}  // namespace
+
+template <int D, int G>
+__global__ void __launch_bounds__(kThr, 1)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                     const DecodeParams p) {
+    using X = TG<D>;
+    constexpr int NA = X::NA;
+    extern __shared__ __align__(1024) uint8_t dsm_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int C = gridDim.x, c = blockIdx.x;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + X::OFF_BAR);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + X::OFF_MISC);
+    int* s_b0 = reinterpret_cast<int*>(sm + X::OFF_MISC + 8);
+    long long* s_pref0 = reinterpret_cast<long long*>(sm + X::OFF_MISC + 16);
+    long long* s_total = reinterpret_cast<long long*>(sm + X::OFF_MISC + 24);
+    __shared__ long long s_wsum[kThr / 32];
+
+    // ---------------- set-up: barriers, TMEM, this CTA's share of the units ----------------
+    if (tid == 0) {
+        mbar_init(&bars[B_KF], 2);
+        mbar_init(&bars[B_KF + 1], 2);
+        mbar_init(&bars[B_VF], 2);
+        mbar_init(&bars[B_VF + 1], 2);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars[B_KE + i], kConvW + kSoftW);
+            mbar_init(&bars[B_VE + i], kConvW + kSoftW);
+            mbar_init(&bars[B_QKD + i], 1);
+            mbar_init(&bars[B_PVD + i], 1);
+            mbar_init(&bars[B_SF + i], kSoftW);
+        }
+        mbar_init(&bars[B_KCV], kConvW);
+        mbar_init(&bars[B_VCV], kConvW);
+        mbar_init(&bars[B_PFL], kSoftW);
+        mbar_init(&bars[B_QRD], 1);
+        mbar_init(&bars[B_PAT], 1);
+        fence_mbar_init();
+        *s_b0 = p.B;
+        *s_pref0 = 0;
+    }
+    if (warp == kWMma) tmem_alloc(tslot, X::TCOLS);
+    // inputs may come from the previous kernel in the stream (programmatic dependent launch)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+    if (tid == 0) p.rec[c * 8] = 0;   // this CTA closes no multi-piece segment (yet)
+    {
+        // pages per sequence, prefix over the block, total units
+        const int per = (p.B + kThr - 1) / kThr;
+        const int b_lo = min(p.B, tid * per), b_hi = min(p.B, b_lo + per);
+        long long local = 0;
+        for (int b = b_lo; b < b_hi; ++b) {
+            const int Lr = p.seq_lens[b];
+            if (Lr < 0 || Lr > p.max_pages * kPage) atomicOr(&g_err_dtc, kErrPos);
+            local += (seq_len_clamped(p, b) + kPage - 1) / kPage;
+        }
+        long long incl = local;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const long long v = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += v;
+        }
+        if (lane == 31) s_wsum[warp] = incl;
+        __syncthreads();
+        long long wpre = 0, total = 0;
+        for (int w = 0; w < kThr / 32; ++w) {
+            if (w < warp) wpre += s_wsum[w];
+            total += s_wsum[w];
+        }
+        const long long T = total * p.NH;
+        const long long beg = T * c / C;
+        long long pref = wpre + incl - local;
+        for (int b = b_lo; b < b_hi; ++b) {
+            const long long np = (seq_len_clamped(p, b) + kPage - 1) / kPage;
+            if (np > 0 && pref * p.NH <= beg && beg < (pref + np) * p.NH) {
+                *s_b0 = b;
+                *s_pref0 = pref;
+            }
+            pref += np;
+        }
+        if (tid == 0) *s_total = T;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const long long Tunits = *s_total;
+    const long long beg = Tunits * c / C, end = Tunits * (c + 1) / C;
+    auto cta_of = [&](long long x) -> long long { return ((x + 1) * C + Tunits - 1) / Tunits - 1; };
+
+    // empty sequences: zero rows, written by CTA (s mod C)
+    for (long long s = c; s < (long long)p.B * p.NH; s += C) {
+        const int b = (int)(s / p.NH);
+        if (seq_len_clamped(p, b) == 0) {
+            const int hg = (int)(s % p.NH);
+            const int kvh = hg / (p.Gtot / G), hgi = hg % (p.Gtot / G);
+            const int hq0 = kvh * p.Gtot + hgi * G;
+            for (int i = tid; i < G * D; i += kThr) write_out<D, G>(p, b, hq0, i, 0.0f);
+        }
+    }
+    Walker walker{*s_b0, *s_pref0, beg, end};
+
+    if (warp == kWProd) {
+        // =============================== producer ===============================
+        uint32_t T = 0, pat_phase = 0;
+        Piece pc;
+        while (walker.next(p, pc)) {
+            const int kvh = pc.hg / (p.Gtot / G);
+            const int32_t* ptrow = p.page_table + (size_t)pc.b * p.max_pages;
+            const int last_page = (pc.L - 1) / kPage;
+            for (int pg0 = pc.p0; pg0 < pc.p1; pg0 += kTP, ++T) {
+                const int npg = min(kTP, pc.p1 - pg0);
+                const int buf = T & 1;
+                const int jp = (p.k_new != nullptr && last_page >= pg0 && last_page < pg0 + npg) ? last_page - pg0 : -1;
+                int pid = 0;
+                if (lane < npg) {
+                    pid = ptrow[pg0 + lane];
+                    if (pid < 0 || pid >= p.num_pages) {
+                        atomicOr(&g_err_dtc, kErrPage);
+                        pid = 0;
+                    }
+                }
+                const int pid_patch = __shfl_sync(0xffffffffu, pid, jp < 0 ? 0 : jp);
+                for (int kind = 0; kind < 2; ++kind) {
+                    if (T >= 2) wait_or_flag(&bars[(kind ? B_VE : B_KE) + buf], ((T >> 1) - 1) & 1);
+                    uint64_t* full = &bars[(kind ? B_VF : B_KF) + buf];
+                    const CUtensorMap* tm = kind ? &tmV : &tmK;
+                    const uint8_t* scl = kind ? p.vs : p.ks;
+                    uint8_t* st = sm + (kind ? X::OFF_VST : X::OFF_KST) + buf * kTP * X::PAGE_B;
+                    uint8_t* ss = sm + (kind ? X::OFF_VSC : X::OFF_KSC) + buf * kTP * X::SC_B;
+                    const int nload = npg - (jp >= 0 ? 1 : 0);
+                    if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)nload * (X::PAGE_B + X::SC_B));
+                    __syncwarp();
+                    if (lane < npg && lane != jp) {
+                        const int row = (pid * p.Hkv + kvh) * kPage;
+#pragma unroll
+                        for (int bx = 0; bx < D / 128; ++bx)
+                            tma_load_2d(st + lane * X::PAGE_B + bx * 2048, tm, full, bx * 128, row);
+                        bulk_load(ss + lane * X::SC_B, scl + (size_t)row * 2 * NA, X::SC_B, full);
+                    }
+                    if (jp >= 0) {
+                        // the sequence's newest token: load its page, quantize the new row into the
+                        // pool and into the staged copy, then release the tile
+                        const int row = (pid_patch * p.Hkv + kvh) * kPage;
+                        uint64_t* pb = &bars[B_PAT];
+                        if (lane == 0) {
+                            mbar_arrive_expect_tx(pb, X::PAGE_B + X::SC_B);
+#pragma unroll
+                            for (int bx = 0; bx < D / 128; ++bx)
+                                tma_load_2d(st + jp * X::PAGE_B + bx * 2048, tm, pb, bx * 128, row);
+                            bulk_load(ss + jp * X::SC_B, scl + (size_t)row * 2 * NA, X::SC_B, pb);
+                        }
+                        wait_or_flag(pb, pat_phase);
+                        pat_phase ^= 1;
+                        uint8_t* rowbuf = sm + X::OFF_ROW + kind * 512;
+                        const uint16_t* src = (kind ? p.v_new : p.k_new) + ((size_t)pc.b * p.Hkv + kvh) * D;
+                        quantize_row<ENC_INT8, D>(src, rowbuf, rowbuf + 256, lane, nullptr, nullptr, nullptr);
+                        __syncwarp();
+                        const int rr = (pc.L - 1) % kPage;
+                        const long long grow = (long long)row + rr;
+                        uint8_t* gcode = const_cast<uint8_t*>(kind ? p.vc : p.kc) + grow * D;
+                        uint8_t* gscale = const_cast<uint8_t*>(scl) + grow * 2 * NA;
+                        uint8_t* scode = st + jp * X::PAGE_B;
+                        if (lane < D / 16) {
+                            const uint4 v = *reinterpret_cast<const uint4*>(rowbuf + 16 * lane);
+                            *reinterpret_cast<uint4*>(gcode + 16 * lane) = v;
+                            *reinterpret_cast<uint4*>(scode + (lane >> 3) * 2048 + sw_off(rr, lane & 7)) = v;
+                        }
+                        if (lane < NA) {
+                            const uint16_t v = reinterpret_cast<const uint16_t*>(rowbuf + 256)[lane];
+                            reinterpret_cast<uint16_t*>(gscale)[lane] = v;
+                            reinterpret_cast<uint16_t*>(ss + jp * X::SC_B + rr * 2 * NA)[lane] = v;
+                        }
+                        fence_proxy_async();   // before later TMA refills of these bytes
+                        __syncwarp();
+                    }
+                    if (lane == 0) mbar_arrive(full);
+                }
+            }
+        }
+        // every copy issued above has landed before the CTA exits
+        for (uint32_t t = (T >= 2 ? T - 2 : 0); t < T; ++t) {
+            wait_or_flag(&bars[B_KF + (t & 1)], (t >> 1) & 1);
+            wait_or_flag(&bars[B_VF + (t & 1)], (t >> 1) & 1);
+        }
+    } else if (warp == kWMma) {
+        // =============================== MMA issue ===============================
+        if (lane == 0) {
+            constexpr uint32_t IDQK = idesc_f16(128, 16);
+            constexpr uint32_t IDPV = idesc_f16(64, D, 1, 1);
+            // base descriptors; every MMA adds a compile-time offset (16-byte units) to them
+            const uint64_t qd0 = sw128_desc(smem_addr(sm + X::OFF_Q));
+            const uint64_t vd0 = sw128_desc_lbo(smem_addr(sm + X::OFF_VP), 16384, 1024);
+            const uint64_t pd0 = sw128_desc_lbo(smem_addr(sm + X::OFF_PP), 16384, 1024);
+            const uint32_t tk = tmem + X::KCOL, to = tmem + X::OCOL;
+            // two cursors over the same tiles: QK^T runs ahead of PV
+            Walker wq = walker, wv = walker;
+            Piece pq, pv;
+            bool hq = wq.next(p, pq), hv = wv.next(p, pv);
+            int tq = 0, tv = 0;           // tile index inside the current piece
+            uint32_t Tq = 0, Tv = 0, pieceq = 0;
+            uint32_t idle = 0;
+            while ((hq || hv) && idle < (1u << 28)) {
+                bool progressed = false;
+                if (hv && Tv < Tq) {
+                    bool ready = mbar_test_wait(&bars[B_PFL], Tv & 1);
+                    if (ready) ready = mbar_test_wait(&bars[B_VCV], Tv & 1);
+                    if (ready) {
+                        tc_fence_after();
+                        // O[64 P' columns][D] += P'^T (MN-major, token rows) x V' (MN-major, token rows)
+#pragma unroll
+                        for (int u = 0; u < kTok / 16; ++u)
+                            umma_f16(to, pd0 + (uint64_t)((u * 2048) >> 4), vd0 + (uint64_t)((u * 2048) >> 4), IDPV,
+                                     (tv > 0 || u > 0));
+                        umma_commit(&bars[B_PVD + (Tv & 1)]);
+                        ++Tv;
+                        if (pv.p0 + kTP * (tv + 1) < pv.p1) {
+                            ++tv;
+                        } else {
+                            tv = 0;
+                            hv = wv.next(p, pv);
+                        }
+                        progressed = true;
+                    }
+                }
+                if (hq) {
+                    const bool first = tq == 0;
+                    bool ready = mbar_test_wait(&bars[B_KCV], Tq & 1);
+                    if (ready && Tq >= 2) ready = mbar_test_wait(&bars[B_SF + (Tq & 1)], ((Tq >> 1) - 1) & 1);
+                    if (ready && first) ready = mbar_test_wait(&bars[B_QRD], pieceq & 1);
+                    if (ready) {
+                        tc_fence_after();
+                        const uint32_t sd = tmem + X::SCOL + (Tq & 1) * NA * 16;
+#pragma unroll
+                        for (int g = 0; g < NA; ++g)
+#pragma unroll
+                            for (int u = 0; u < 4; ++u)
+                                umma_f16_ta(sd + 16 * g, tk + 8 * (4 * g + u), qd0 + (uint64_t)((g * 2048 + 32 * u) >> 4), IDQK,
+                                            u > 0);
+                        umma_commit(&bars[B_QKD + (Tq & 1)]);
+                        ++Tq;
+                        if (pq.p0 + kTP * (tq + 1) < pq.p1) {
+                            ++tq;
+                        } else {
+                            tq = 0;
+                            ++pieceq;
+                            hq = wq.next(p, pq);
+                        }
+                        progressed = true;
+                    }
+                }
+                idle = progressed ? 0 : idle + 1;
+            }
+            if (hq || hv) atomicOr(&g_err_dtc, kErrWait);
+        }
+        __syncwarp();
+    } else if (warp >= kSoftW) {
+        // =============================== converters ===============================
+        const int cw = warp - kSoftW, sub = cw & 3, hf = cw >> 2;
+        const int r = 32 * sub + lane, jpage = r >> 4, rr = r & 15;
+        constexpr int NCH = D / 32;   // 16-code chunks per thread (half of the head dimension)
+        const uint32_t lb = (uint32_t)(32 * sub) << 16;
+        uint32_t T = 0;
+        Piece pc;
+        while (walker.next(p, pc)) {
+            for (int pg0 = pc.p0; pg0 < pc.p1; pg0 += kTP, ++T) {
+                const int buf = T & 1;
+                const uint32_t ph = (T >> 1) & 1;
+                // ---- K: exact fp16 1152 + c, one token per TMEM lane ----
+                wait_or_flag(&bars[B_KF + buf], ph);
+                if (T >= 1) wait_or_flag(&bars[B_QKD + ((T - 1) & 1)], ((T - 1) >> 1) & 1);
+                tc_fence_after();
+                {
+                    const uint8_t* slot = sm + X::OFF_KST + (buf * kTP + jpage) * X::PAGE_B;
+#pragma unroll
+                    for (int i0 = 0; i0 < NCH; i0 += 4) {
+                        uint32_t w[32];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int gc = hf * NCH + i0 + i;
+                            const uint4 x = *reinterpret_cast<const uint4*>(slot + (gc >> 3) * 2048 + sw_off(rr, gc & 7));
+                            const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                w[8 * i + 2 * k] = lop3_and_xor(xs[k], 0x00ff00ffu, 0x64806480u);
+                                w[8 * i + 2 * k + 1] = lop3_and_xor(xs[k] >> 8, 0x00ff00ffu, 0x64806480u);
+                            }
+                        }
+                        tmem_st32_nowait(tmem + lb + X::KCOL + 8 * (hf * NCH + i0), w);
+                    }
+                    tmem_wait_st();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&bars[B_KCV]);
+                    mbar_arrive(&bars[B_KE + buf]);
+                }
+                // ---- V: exact fp16 c into the MN-major tile (row = token) ----
+                wait_or_flag(&bars[B_VF + buf], ph);
+                // V' rows of this warp's dims are free once PV of the previous tile read them
+                if (T >= 1) wait_or_flag(&bars[B_PVD + ((T - 1) & 1)], ((T - 1) >> 1) & 1);
+                {
+                    const uint8_t* slot = sm + X::OFF_VST + (buf * kTP + jpage) * X::PAGE_B;
+                    uint8_t* vp = sm + X::OFF_VP;
+#pragma unroll
+                    for (int i = 0; i < NCH; ++i) {
+                        const int gc = hf * NCH + i;
+                        const uint4 x = *reinterpret_cast<const uint4*>(slot + (gc >> 3) * 2048 + sw_off(rr, gc & 7));
+                        const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+                        uint32_t w[8];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            w[2 * k] = hsub2_u32(lop3_and_xor(xs[k], 0x00ff00ffu, 0x64806480u), 0x64806480u);
+                            w[2 * k + 1] = hsub2_u32(lop3_and_xor(xs[k] >> 8, 0x00ff00ffu, 0x64806480u), 0x64806480u);
+                        }
+                        uint8_t* atom = vp + (gc >> 2) * 16384;
+                        const int ch = 2 * (gc & 3);
+                        *reinterpret_cast<uint4*>(atom + sw_off(r, ch)) = make_uint4(w[0], w[1], w[2], w[3]);
+                        *reinterpret_cast<uint4*>(atom + sw_off(r, ch + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+                    }
+                }
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&bars[B_VCV]);
+                    mbar_arrive(&bars[B_VE + buf]);
+                }
+            }
+        }
+    } else {
+        // =============================== softmax ===============================
+        const int r = tid;   // token row of the tile = TMEM lane
+        const uint32_t lb = (uint32_t)(32 * warp) << 16;
+        float* bias_s = reinterpret_cast<float*>(sm + X::OFF_BIAS);
+        int* red_flag = reinterpret_cast<int*>(sm + X::OFF_RED);                 // [2][4]
+        int* red_e = red_flag + 8;                                               // [2][4]
+        float* red_m = reinterpret_cast<float*>(sm + X::OFF_RED + 64);           // [2][4][8]
+        float* red_l = red_m + 64;                                               // [4][8]
+        float* sML = red_l + 32;                                                 // M[8], L[8]
+        uint32_t T = 0, piece = 0;
+        Piece pc;
+        while (walker.next(p, pc)) {
+            const int kvh = pc.hg / (p.Gtot / G), hgi = pc.hg % (p.Gtot / G);
+            const int hq0 = kvh * p.Gtot + hgi * G;
+            // ---- query tile (B operand, K-major, dims in converter order) and the offset sums ----
+            {
+                uint8_t* qsm = sm + X::OFF_Q;
+                for (int idx = r; idx < 16 * NA * 8; idx += 128) {
+                    const int n = idx / (NA * 8), rem = idx % (NA * 8), a = rem >> 3, cc = rem & 7;
+                    uint32_t w[4] = {0u, 0u, 0u, 0u};
+                    if (n < G) {
+                        const uint16_t* qrow = p.q + ((size_t)pc.b * p.Hq + hq0 + n) * D + 64 * a + 8 * cc;
+                        const uint4 raw = *reinterpret_cast<const uint4*>(qrow);
+                        const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
+                        float v[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int d = perm4(e);
+                            v[e] = bf16_bits_to_f32((rw[d >> 1] >> (16 * (d & 1))) & 0xffffu);
+                        }
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) w[k] = f32x2_to_h2(v[2 * k], v[2 * k + 1]);
+                    }
+                    *reinterpret_cast<uint4*>(qsm + a * 2048 + sw_off(n, cc)) = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+                // 1152 * (sum of the fp16 query over each 64-dim group): thread -> (head, D / 16 dims)
+                constexpr int DPT = D / 16, TPG = 64 / DPT;
+                const int h = r >> 4, s0 = (r & 15) * DPT;
+                float part = 0.0f;
+                if (h < G) {
+                    const uint16_t* qrow = p.q + ((size_t)pc.b * p.Hq + hq0 + h) * D + s0;
+                    for (int d = 0; d < DPT; ++d)
+                        part += __half2float(__float2half_rn(bf16_bits_to_f32(qrow[d])));
+                }
+#pragma unroll
+                for (int off = 1; off < TPG; off <<= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+                if (h < G && (r & 15) % TPG == 0) bias_s[(s0 / 64) * 8 + h] = 1152.0f * part;
+            }
+            fence_proxy_async();
+            soft_sync();
+            if (r == 0) mbar_arrive(&bars[B_QRD]);
+            float bias[NA][G];
+#pragma unroll
+            for (int g = 0; g < NA; ++g)
+#pragma unroll
+                for (int h = 0; h < G; ++h) bias[g][h] = bias_s[g * 8 + h];
+
+            float m[G], l[G];
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                m[h] = -INFINITY;
+                l[h] = 0.0f;
+            }
+            int E = 1000;   // range exponent of the frame ("unset")
+            for (int pg0 = pc.p0, t = 0; pg0 < pc.p1; pg0 += kTP, ++t, ++T) {
+                const int npg = min(kTP, pc.p1 - pg0);
+                const int buf = T & 1;
+                const uint32_t ph = (T >> 1) & 1;
+                const int jpage = r >> 4;
+                const int pos = (pg0 + jpage) * kPage + (r & 15);
+                const bool valid = jpage < npg && pos < pc.L;
+                // ---- scores ----
+                wait_or_flag(&bars[B_KF + buf], ph);
+                float ks[NA];
+                {
+                    const uint8_t* ksr = sm + X::OFF_KSC + (buf * kTP + jpage) * X::SC_B + (r & 15) * 2 * NA;
+#pragma unroll
+                    for (int g = 0; g < NA; ++g) ks[g] = f16_bits_to_f32(reinterpret_cast<const uint16_t*>(ksr)[g]);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[B_KE + buf]);
+                wait_or_flag(&bars[B_QKD + buf], ph);
+                tc_fence_after();
+                float s[G];
+#pragma unroll
+                for (int h = 0; h < G; ++h) s[h] = 0.0f;
+#pragma unroll
+                for (int g = 0; g < NA; ++g) {
+                    float v[16];
+                    tmem_ld16(tmem + lb + X::SCOL + buf * NA * 16 + 16 * g, v);
+#pragma unroll
+                    for (int h = 0; h < G; ++h) s[h] += ks[g] * (v[h] - bias[g][h]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[B_SF + buf]);
+#pragma unroll
+                for (int h = 0; h < G; ++h) s[h] = valid ? s[h] * p.scale_log2 : -INFINITY;
+                // ---- V scales ----
+                wait_or_flag(&bars[B_VF + buf], ph);
+                float vsf[NA];
+                int e_row = 0;
+                {
+                    const uint8_t* vsr = sm + X::OFF_VSC + (buf * kTP + jpage) * X::SC_B + (r & 15) * 2 * NA;
+#pragma unroll
+                    for (int g = 0; g < NA; ++g) {
+                        const uint32_t hb = reinterpret_cast<const uint16_t*>(vsr)[g];
+                        vsf[g] = f16_bits_to_f32(hb);
+                        e_row = max(e_row, (int)((hb & 0x7fffu) >> 10));
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[B_VE + buf]);
+                if (!valid) e_row = 0;
+                // ---- frame: all 128 threads agree on the max and the range exponent ----
+                bool need = false;
+#pragma unroll
+                for (int h = 0; h < G; ++h) need |= s[h] > m[h] + 8.0f;
+                need |= valid && (20 - max(e_row, 1)) < E;
+                const unsigned any_w = __ballot_sync(0xffffffffu, need);
+                if (lane == 0) red_flag[buf * 4 + warp] = any_w != 0;
+                soft_sync();
+                const bool any = (red_flag[buf * 4] | red_flag[buf * 4 + 1] | red_flag[buf * 4 + 2] | red_flag[buf * 4 + 3]) != 0;
+                bool rescale = false;
+                float fac[8];
+#pragma unroll
+                for (int h = 0; h < 8; ++h) fac[h] = 1.0f;
+                if (any) {
+#pragma unroll
+                    for (int h = 0; h < G; ++h) {
+                        float v = s[h];
+#pragma unroll
+                        for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+                        if (lane == 0) red_m[buf * 32 + warp * 8 + h] = v;
+                    }
+                    const int ew = __reduce_max_sync(0xffffffffu, (unsigned)e_row);
+                    if (lane == 0) red_e[buf * 4 + warp] = ew;
+                    soft_sync();
+                    const int et = max(max(red_e[buf * 4], red_e[buf * 4 + 1]), max(red_e[buf * 4 + 2], red_e[buf * 4 + 3]));
+                    const int Enew = min(E, 20 - max(et, 1));
+                    const float ef = (E == 1000) ? 1.0f : exp2i(Enew - E);
+#pragma unroll
+                    for (int h = 0; h < G; ++h) {
+                        const float M = fmaxf(fmaxf(red_m[buf * 32 + h], red_m[buf * 32 + 8 + h]),
+                                              fmaxf(red_m[buf * 32 + 16 + h], red_m[buf * 32 + 24 + h]));
+                        const float mn = (M > m[h] + 8.0f) ? M : m[h];
+                        const float alpha = (m[h] == -INFINITY) ? 0.0f : (mn == m[h] ? 1.0f : fast_exp2(m[h] - mn));
+                        l[h] *= alpha;
+                        fac[h] = alpha * ef;
+                        m[h] = mn;
+                    }
+                    rescale = t > 0;
+                    E = Enew;
+                }
+                // ---- probabilities ----
+                float pr[G];
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    pr[h] = valid ? fast_exp2(s[h] - m[h]) : 0.0f;
+                    l[h] += pr[h];
+                }
+                // ---- P' (and the rare rescale of O) once PV of the previous tile is done ----
+                if (T >= 1) wait_or_flag(&bars[B_PVD + ((T - 1) & 1)], ((T - 1) >> 1) & 1);
+                tc_fence_after();
+                if (rescale && warp < NA) {
+                    // O rows 16 g + j (lane j of warp g: head j % 8, hi / lo) over the dims of group g
+                    float f = fac[0];
+#pragma unroll
+                    for (int h = 1; h < 8; ++h) f = ((lane & 7) == h) ? fac[h] : f;
+#pragma unroll 1
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        float v[16];
+                        const uint32_t ta = tmem + lb + X::OCOL + 64 * warp + 16 * c4;
+                        tmem_ld16(ta, v);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) v[j] *= f;
+                        tmem_st16(ta, v);
+                    }
+                }
+                {
+                    const float e2 = (E == 1000) ? 1.0f : exp2i(E);
+                    uint8_t* pp = sm + X::OFF_PP;
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        uint32_t hw[4] = {0u, 0u, 0u, 0u}, lw[4] = {0u, 0u, 0u, 0u};
+                        if (g < NA && valid) {
+                            const float sc = vsf[g < NA ? g : 0] * e2;
+                            float P[8];
+#pragma unroll
+                            for (int h = 0; h < 8; ++h) P[h] = h < G ? pr[h < G ? h : 0] * sc : 0.0f;
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                hw[k] = f32x2_to_h2(P[2 * k], P[2 * k + 1]);
+                                const float2 f = h2_to_f32x2(hw[k]);
+                                lw[k] = f32x2_to_h2(P[2 * k] - f.x, P[2 * k + 1] - f.y);
+                            }
+                        }
+                        *reinterpret_cast<uint4*>(pp + sw_off(r, 2 * g)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                        *reinterpret_cast<uint4*>(pp + sw_off(r, 2 * g + 1)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                    }
+                }
+                fence_proxy_async();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[B_PFL]);
+            }
+            // ---- end of the piece: O out of TMEM, row sums, merge ----
+            wait_or_flag(&bars[B_PVD + ((T - 1) & 1)], ((T - 1) >> 1) & 1);
+            tc_fence_after();
+            float* obuf = reinterpret_cast<float*>(sm + X::OFF_PP);   // [G][D]; P' is free now
+            if (warp < NA) {
+                // warp g: lanes h and 8 + h hold the hi and lo rows of head h over the dims of group g
+                const float inv = (E == 1000) ? 0.0f : exp2i(-E);
+#pragma unroll 1
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    float v[16];
+                    tmem_ld16(tmem + lb + X::OCOL + 64 * warp + 16 * c4, v);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v[j] += __shfl_xor_sync(0xffffffffu, v[j], 8);
+                    if (lane < G) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) obuf[lane * D + 64 * warp + perm4(16 * c4 + j)] = v[j] * inv;
+                    }
+                }
+            }
+            tc_fence_before();
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                float v = l[h];
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+                if (lane == 0) red_l[warp * 8 + h] = v;
+            }
+            soft_sync();
+            if (r < G) {
+                float mr = m[0];
+#pragma unroll
+                for (int h = 1; h < G; ++h) mr = (r == h) ? m[h] : mr;
+                sML[r] = mr;
+                sML[8 + r] = red_l[r] + red_l[8 + r] + red_l[16 + r] + red_l[24 + r];
+            }
+            soft_sync();
+            const long long clo = cta_of(pc.soff), chi = cta_of(pc.soff + pc.np - 1);
+            const int npieces = (int)(chi - clo + 1);
+            const long long seg = (long long)pc.b * p.NH + pc.hg;
+            if (npieces == 1) {
+                for (int i = r; i < G * D; i += 128) {
+                    const float Lh = sML[8 + i / D];
+                    write_out<D, G>(p, pc.b, hq0, i, Lh > 0.0f ? obuf[i] / Lh : 0.0f);
+                }
+            } else {
+                // partial slot of this piece; the combine kernel merges the segment's slots
+                float* mine = p.part1 + (size_t)(c + seg) * p.slot_floats;
+                for (int i = 4 * r; i < G * D; i += 4 * 128)
+                    *reinterpret_cast<float4*>(mine + 16 + i) = *reinterpret_cast<const float4*>(obuf + i);
+                if (r < G) {
+                    mine[r] = sML[r];
+                    mine[8 + r] = sML[8 + r];
+                }
+                if (r == 0 && c == chi) {
+                    int* rc = p.rec + c * 8;
+                    rc[1] = (int)clo;
+                    rc[2] = (int)seg;
+                    rc[3] = pc.b;
+                    rc[4] = hq0;
+                    rc[0] = npieces;
+                }
+            }
+            soft_sync();
+            ++piece;
+        }
+    }
+
+    // ---------------- tear-down ----------------
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kWMma) tmem_dealloc(tmem, X::TCOLS);
+}
+
+// ---------------------------------------------------------------------------
+// combine: merge the partial slots of every segment split across CTAs.
+// Grid (G * D / 64, C): block (s, c) merges output floats [64 s, 64 s + 64) of
+// the segment recorded by decode CTA c, with the partial-softmax rule
+// M = max m_j, O = sum 2^(m_j - M) O_j / sum 2^(m_j - M) l_j (base-2 scores).
+// ---------------------------------------------------------------------------
+constexpr int kCombThr = 128;
+constexpr int kMaxGrid = 256;   // decode CTAs (pieces of one segment) the combine step can merge
+
+template <int D, int G>
+__global__ void __launch_bounds__(kCombThr) decode_tc_combine(const DecodeParams p) {
+    __shared__ float s_w[kMaxGrid], s_l[kMaxGrid];
+    __shared__ float4 s_acc[8][16];
+    __shared__ float s_red[8];
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // the decode grid has completed
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int* rc = p.rec + blockIdx.y * 8;
+    const int n = rc[0];
+    if (n < 2) return;
+    const int clo = rc[1], seg = rc[2], b = rc[3], hq0 = rc[4];
+    const int t = threadIdx.x, s = blockIdx.x;
+    const int f0 = 64 * s, h = f0 / D;
+    auto slot = [&](int j) { return p.part1 + (size_t)(clo + j + seg) * p.slot_floats; };
+    // O loads first (independent of the weights): thread -> float4 e, slots j = sg, sg + 8, ...
+    const int e = t & 15, sg = t >> 4;
+    float4 v[20];
+#pragma unroll
+    for (int k = 0; k < 20; ++k) {
+        const int j = sg + 8 * k;
+        v[k] = j < n ? *reinterpret_cast<const float4*>(slot(j) + 16 + f0 + 4 * e) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float mloc = -INFINITY;
+    for (int j = t; j < n; j += kCombThr) {
+        const float mj = slot(j)[h];
+        s_w[j] = mj;
+        s_l[j] = slot(j)[8 + h];
+        mloc = fmaxf(mloc, mj);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, off));
+    if ((t & 31) == 0) s_red[t >> 5] = mloc;
+    __syncthreads();
+    const float M = fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3]));
+    float lloc = 0.0f;
+    for (int j = t; j < n; j += kCombThr) {
+        const float w = s_w[j] == -INFINITY ? 0.0f : exp2f(s_w[j] - M);
+        s_w[j] = w;
+        lloc += w * s_l[j];
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) lloc += __shfl_xor_sync(0xffffffffu, lloc, off);
+    __syncthreads();
+    if ((t & 31) == 0) s_red[4 + (t >> 5)] = lloc;
+    __syncthreads();
+    const float L = s_red[4] + s_red[5] + s_red[6] + s_red[7];
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < 20; ++k) {
+        const int j = sg + 8 * k;
+        if (j < n) {
+            const float w = s_w[j];
+            acc.x += w * v[k].x;
+            acc.y += w * v[k].y;
+            acc.z += w * v[k].z;
+            acc.w += w * v[k].w;
+        }
+    }
+    for (int j = sg + 160; j < n; j += 8) {   // segments split over more than 160 CTAs
+        const float w = s_w[j];
+        const float4 x = *reinterpret_cast<const float4*>(slot(j) + 16 + f0 + 4 * e);
+        acc.x += w * x.x;
+        acc.y += w * x.y;
+        acc.z += w * x.z;
+        acc.w += w * x.w;
+    }
+    s_acc[sg][e] = acc;
+    __syncthreads();
+    if (t < 64) {
+        const int q = t >> 2, c4 = t & 3;   // float4 q, component c4
+        float a = 0.0f;
+#pragma unroll
+        for (int g2 = 0; g2 < 8; ++g2) {
+            const float4 x = s_acc[g2][q];
+            a += c4 == 0 ? x.x : c4 == 1 ? x.y : c4 == 2 ? x.z : x.w;
+        }
+        write_out<D, G>(p, b, hq0, f0 + 4 * q + c4, L > 0.0f ? a / L : 0.0f);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+cudaError_t decode_tc_read_error(unsigned* out, bool clear) {
+    cudaError_t e = cudaMemcpyFromSymbol(out, g_err_dtc, sizeof(unsigned));
+    if (e != cudaSuccess || !clear) return e;
+    unsigned z = 0;
+    return cudaMemcpyToSymbol(g_err_dtc, &z, sizeof(unsigned));
+}
+
+// Both kernels are launched with programmatic stream serialization: each may
+// start while its predecessor in the stream drains, and waits for it
+// (griddepcontrol.wait) before touching memory.
+template <int D, int G>
+static cudaError_t launch_tc(int grid, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
+                             cudaStream_t st) {
+    using X = TG<D>;
+    auto fn = decode_tc_kernel<D, G>;
+    static bool configured = false;   // per instantiation; the attribute is per device context
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, X::SMEM + 1024);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThr);
+    cfg.dynamicSmemBytes = X::SMEM + 1024;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, fn, tk, tv, p);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(G * D / 64, grid);
+    cfg.blockDim = dim3(kCombThr);
+    cfg.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&cfg, decode_tc_combine<D, G>, p);
+}
+
+template <int D>
+static cudaError_t launch_tc_g(int G, int grid, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
+                               cudaStream_t st) {
+    switch (G) {
+        case 1: return launch_tc<D, 1>(grid, tk, tv, p, st);
+        case 2: return launch_tc<D, 2>(grid, tk, tv, p, st);
+        case 4: return launch_tc<D, 4>(grid, tk, tv, p, st);
+        case 8: return launch_tc<D, 8>(grid, tk, tv, p, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t decode_tc_launch(int D, int G, int grid, const CUtensorMap& tk, const CUtensorMap& tv,
+                             const DecodeParams& p, cudaStream_t st) {
+    grid = grid < kMaxGrid ? grid : kMaxGrid;
+    if (D == 256) return launch_tc_g<256>(G, grid, tk, tv, p, st);
+    if (D == 128) return launch_tc_g<128>(G, grid, tk, tv, p, st);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace qkv

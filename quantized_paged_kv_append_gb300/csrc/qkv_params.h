@@ -40,6 +40,7 @@ struct DecodeParams {
     int* seg_cnt;        // [S]
     int* grp_cnt;        // [C + S]
     int slot_floats;     // 16 + 8 * D
+    int* rec;            // [C][8]: the multi-piece segment each CTA closes (int8 tensor-core path)
     const uint16_t* k_new;   // optional bf16 [B][Hkv][D]: quantize-on-write of position seq_lens[b] - 1
     const uint16_t* v_new;
 };
@@ -74,6 +75,10 @@ cudaError_t decode_read_error(unsigned* out, bool clear);
 cudaError_t decode_launch(int fmt, int D, int G, int grid, const CUtensorMap& tk, const CUtensorMap& tv,
                           const DecodeParams& p, cudaStream_t st);
 int decode_heads_per_cta(int Gtot);
+// int8 K/V on tcgen05 tensor cores (decode_tc.cu): D 128 or 256, G in {1, 2, 4, 8}
+cudaError_t decode_tc_launch(int D, int G, int grid, const CUtensorMap& tk, const CUtensorMap& tv,
+                             const DecodeParams& p, cudaStream_t st);
+cudaError_t decode_tc_read_error(unsigned* out, bool clear);
 
 cudaError_t extend_read_error(unsigned* out, bool clear);
 cudaError_t extend_launch(int fmt, int D, int G, int max_q_len, int NH, int B, const ExtendParams& p, cudaStream_t st);
