@@ -9,15 +9,17 @@
 // one sequence's pages and the partial results are merged with the log-sum-exp
 // rule).
 //
-// GB300 design (one CTA of 14 warps per SM, persistent over an equal share of
+// GB300 design (one CTA of 15 warps per SM, persistent over an equal share of
 // the (sequence, KV-head group, page) units -- stream-K):
 //   * tile = 8 pages = 128 tokens of one (sequence, head group);
-//   * warp 12 (producer) stages the int8 code planes of each tile with 2-D TMA
-//     (128-byte swizzle) and the scale rows with bulk copies, two tiles deep;
-//     it also quantizes the newest token into the pool and the staged copy;
+//   * warps 12 (K) and 14 (V) stage the int8 code planes of each tile with
+//     2-D TMA (128-byte swizzle) and the scale rows with bulk copies, two tiles
+//     deep, each on its own schedule; they also quantize the newest token into
+//     the pool and the staged copy;
 //   * warps 4-11 (converters) turn int8 codes into exact fp16: K as 1152 + c
 //     straight into TMEM (the A operand of Q K^T, one token per TMEM lane), V
-//     as c into an MN-major shared-memory tile (the A operand of V^T P);
+//     as c into an MN-major shared-memory tile (the B operand of P'^T V'); K of
+//     tile T is converted before V of tile T - 1, so Q K^T runs a tile ahead;
 //   * warp 13 (one thread) issues tcgen05.mma: S_g = K'_g Q_g^T per 64-dim
 //     scale group g (M = 128 tokens, N = 16 query columns; 16 MMAs per tile at
 //     D = 256) and O += P'^T V' (M = 64 P' columns: 16 per scale group = 8
@@ -45,9 +47,10 @@ namespace {
 constexpr int kTok = 128;                   // tokens per tile
 constexpr int kTP = kTok / kPage;           // pages per tile
 constexpr int kSoftW = 4, kConvW = 8;
-constexpr int kWProd = kSoftW + kConvW;     // producer warp
+constexpr int kWProd = kSoftW + kConvW;     // producer warp of the K planes
 constexpr int kWMma = kWProd + 1;           // MMA warp
-constexpr int kThr = (kWMma + 1) * 32;      // 448 threads
+constexpr int kWProdV = kWMma + 1;          // producer warp of the V planes
+constexpr int kThr = (kWProdV + 1) * 32;    // 480 threads
 
 template <int D>
 struct TG {
@@ -89,8 +92,8 @@ enum {
     B_SF = 16,   // [2] score buffer read (4 softmax warps)
     B_PFL = 18,  // P' written (4 softmax warps)
     B_QRD = 19,  // query tile of a piece written (1)
-    B_PAT = 20,  // producer: the newest token's page landed (1 + tx)
-    B_N = 21
+    B_PAT = 20,  // [kind] producer: the newest token's page landed (1 + tx)
+    B_N = 22
 };
 static_assert(B_N <= 32, "barrier area holds 32 barriers");
 
@@ -139,9 +142,17 @@ struct Walker {
     }
 };
 
-__device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity) {
-    if (mbar_wait_bounded(bar, parity)) return true;
+// Bounded wait on an mbarrier phase. A wait that runs out sets the device error
+// bit and the CTA-wide abort flag; every later wait of the CTA then returns at
+// once, so a broken launch ends after one time-out instead of one per wait
+// (its results are garbage and the error word says so).
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+    for (uint32_t i = 0; i < (1u << 20); ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63) == 63 && *abort_flag) return false;
+    }
     atomicOr(&g_err_dtc, kErrWait);
+    *abort_flag = 1;
     return false;
 }
 
@@ -169,6 +180,8 @@ __global__ void __launch_bounds__(kThr, 1)
     int* s_b0 = reinterpret_cast<int*>(sm + X::OFF_MISC + 8);
     long long* s_pref0 = reinterpret_cast<long long*>(sm + X::OFF_MISC + 16);
     long long* s_total = reinterpret_cast<long long*>(sm + X::OFF_MISC + 24);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(sm + X::OFF_MISC + 32);
+    auto wait_or_flag = [&](uint64_t* bar, uint32_t parity) { return wait_or_abort(bar, parity, s_abort); };
     __shared__ long long s_wsum[kThr / 32];
 
     // ---------------- set-up: barriers, TMEM, this CTA's share of the units ----------------
@@ -189,9 +202,11 @@ __global__ void __launch_bounds__(kThr, 1)
         mbar_init(&bars[B_PFL], kSoftW);
         mbar_init(&bars[B_QRD], 1);
         mbar_init(&bars[B_PAT], 1);
+        mbar_init(&bars[B_PAT + 1], 1);
         fence_mbar_init();
         *s_b0 = p.B;
         *s_pref0 = 0;
+        *s_abort = 0;
     }
     if (warp == kWMma) tmem_alloc(tslot, X::TCOLS);
     // inputs may come from the previous kernel in the stream (programmatic dependent launch)
@@ -254,89 +269,98 @@ __global__ void __launch_bounds__(kThr, 1)
     }
     Walker walker{*s_b0, *s_pref0, beg, end};
 
-    if (warp == kWProd) {
-        // =============================== producer ===============================
+    if (warp == kWProd || warp == kWProdV) {
+        // ============================ producers (K, V) ============================
+        // One warp per plane, so that the K stream runs ahead of the V stream (PV of a
+        // tile comes much later than its Q K^T). Page ids come from a 32-entry ring per
+        // lane, refilled a block ahead, so no tile waits for a page-table load.
+        const int kind = warp == kWProdV ? 1 : 0;
+        uint64_t* const fullb = &bars[kind ? B_VF : B_KF];
+        uint64_t* const emptyb = &bars[kind ? B_VE : B_KE];
+        const CUtensorMap* tm = kind ? &tmV : &tmK;
+        const uint8_t* scl = kind ? p.vs : p.ks;
+        const uint16_t* newsrc = kind ? p.v_new : p.k_new;
         uint32_t T = 0, pat_phase = 0;
         Piece pc;
         while (walker.next(p, pc)) {
             const int kvh = pc.hg / (p.Gtot / G);
             const int32_t* ptrow = p.page_table + (size_t)pc.b * p.max_pages;
             const int last_page = (pc.L - 1) / kPage;
+            const int npc = pc.p1 - pc.p0;
+            int bc = 0;
+            int pid_cur = lane < npc ? ptrow[pc.p0 + lane] : 0;
+            int pid_nxt = 32 + lane < npc ? ptrow[pc.p0 + 32 + lane] : 0;
             for (int pg0 = pc.p0; pg0 < pc.p1; pg0 += kTP, ++T) {
                 const int npg = min(kTP, pc.p1 - pg0);
                 const int buf = T & 1;
                 const int jp = (p.k_new != nullptr && last_page >= pg0 && last_page < pg0 + npg) ? last_page - pg0 : -1;
-                int pid = 0;
-                if (lane < npg) {
-                    pid = ptrow[pg0 + lane];
-                    if (pid < 0 || pid >= p.num_pages) {
-                        atomicOr(&g_err_dtc, kErrPage);
-                        pid = 0;
-                    }
+                const int pi = pg0 - pc.p0;   // page index inside the piece (a multiple of 8)
+                if ((pi >> 5) > bc) {
+                    pid_cur = pid_nxt;
+                    ++bc;
+                    pid_nxt = 32 * (bc + 1) + lane < npc ? ptrow[pc.p0 + 32 * (bc + 1) + lane] : 0;
+                }
+                int pid = __shfl_sync(0xffffffffu, pid_cur, (pi & 31) + (lane & 7));
+                if (lane < npg && (pid < 0 || pid >= p.num_pages)) {
+                    atomicOr(&g_err_dtc, kErrPage);
+                    pid = 0;
                 }
                 const int pid_patch = __shfl_sync(0xffffffffu, pid, jp < 0 ? 0 : jp);
-                for (int kind = 0; kind < 2; ++kind) {
-                    if (T >= 2) wait_or_flag(&bars[(kind ? B_VE : B_KE) + buf], ((T >> 1) - 1) & 1);
-                    uint64_t* full = &bars[(kind ? B_VF : B_KF) + buf];
-                    const CUtensorMap* tm = kind ? &tmV : &tmK;
-                    const uint8_t* scl = kind ? p.vs : p.ks;
-                    uint8_t* st = sm + (kind ? X::OFF_VST : X::OFF_KST) + buf * kTP * X::PAGE_B;
-                    uint8_t* ss = sm + (kind ? X::OFF_VSC : X::OFF_KSC) + buf * kTP * X::SC_B;
-                    const int nload = npg - (jp >= 0 ? 1 : 0);
-                    if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)nload * (X::PAGE_B + X::SC_B));
-                    __syncwarp();
-                    if (lane < npg && lane != jp) {
-                        const int row = (pid * p.Hkv + kvh) * kPage;
+                if (T >= 2) wait_or_flag(emptyb + buf, ((T >> 1) - 1) & 1);
+                uint64_t* full = fullb + buf;
+                uint8_t* st = sm + (kind ? X::OFF_VST : X::OFF_KST) + buf * kTP * X::PAGE_B;
+                uint8_t* ss = sm + (kind ? X::OFF_VSC : X::OFF_KSC) + buf * kTP * X::SC_B;
+                const int nload = npg - (jp >= 0 ? 1 : 0);
+                if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)nload * (X::PAGE_B + X::SC_B));
+                __syncwarp();
+                if (lane < npg && lane != jp) {
+                    const int row = (pid * p.Hkv + kvh) * kPage;
+#pragma unroll
+                    for (int bx = 0; bx < D / 128; ++bx)
+                        tma_load_2d(st + lane * X::PAGE_B + bx * 2048, tm, full, bx * 128, row);
+                    bulk_load(ss + lane * X::SC_B, scl + (size_t)row * 2 * NA, X::SC_B, full);
+                }
+                if (jp >= 0) {
+                    // the sequence's newest token: load its page, quantize the new row into the
+                    // pool and into the staged copy, then release the tile
+                    const int row = (pid_patch * p.Hkv + kvh) * kPage;
+                    uint64_t* pb = &bars[B_PAT + kind];
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(pb, X::PAGE_B + X::SC_B);
 #pragma unroll
                         for (int bx = 0; bx < D / 128; ++bx)
-                            tma_load_2d(st + lane * X::PAGE_B + bx * 2048, tm, full, bx * 128, row);
-                        bulk_load(ss + lane * X::SC_B, scl + (size_t)row * 2 * NA, X::SC_B, full);
+                            tma_load_2d(st + jp * X::PAGE_B + bx * 2048, tm, pb, bx * 128, row);
+                        bulk_load(ss + jp * X::SC_B, scl + (size_t)row * 2 * NA, X::SC_B, pb);
                     }
-                    if (jp >= 0) {
-                        // the sequence's newest token: load its page, quantize the new row into the
-                        // pool and into the staged copy, then release the tile
-                        const int row = (pid_patch * p.Hkv + kvh) * kPage;
-                        uint64_t* pb = &bars[B_PAT];
-                        if (lane == 0) {
-                            mbar_arrive_expect_tx(pb, X::PAGE_B + X::SC_B);
-#pragma unroll
-                            for (int bx = 0; bx < D / 128; ++bx)
-                                tma_load_2d(st + jp * X::PAGE_B + bx * 2048, tm, pb, bx * 128, row);
-                            bulk_load(ss + jp * X::SC_B, scl + (size_t)row * 2 * NA, X::SC_B, pb);
-                        }
-                        wait_or_flag(pb, pat_phase);
-                        pat_phase ^= 1;
-                        uint8_t* rowbuf = sm + X::OFF_ROW + kind * 512;
-                        const uint16_t* src = (kind ? p.v_new : p.k_new) + ((size_t)pc.b * p.Hkv + kvh) * D;
-                        quantize_row<ENC_INT8, D>(src, rowbuf, rowbuf + 256, lane, nullptr, nullptr, nullptr);
-                        __syncwarp();
-                        const int rr = (pc.L - 1) % kPage;
-                        const long long grow = (long long)row + rr;
-                        uint8_t* gcode = const_cast<uint8_t*>(kind ? p.vc : p.kc) + grow * D;
-                        uint8_t* gscale = const_cast<uint8_t*>(scl) + grow * 2 * NA;
-                        uint8_t* scode = st + jp * X::PAGE_B;
-                        if (lane < D / 16) {
-                            const uint4 v = *reinterpret_cast<const uint4*>(rowbuf + 16 * lane);
-                            *reinterpret_cast<uint4*>(gcode + 16 * lane) = v;
-                            *reinterpret_cast<uint4*>(scode + (lane >> 3) * 2048 + sw_off(rr, lane & 7)) = v;
-                        }
-                        if (lane < NA) {
-                            const uint16_t v = reinterpret_cast<const uint16_t*>(rowbuf + 256)[lane];
-                            reinterpret_cast<uint16_t*>(gscale)[lane] = v;
-                            reinterpret_cast<uint16_t*>(ss + jp * X::SC_B + rr * 2 * NA)[lane] = v;
-                        }
-                        fence_proxy_async();   // before later TMA refills of these bytes
-                        __syncwarp();
+                    wait_or_flag(pb, pat_phase);
+                    pat_phase ^= 1;
+                    uint8_t* rowbuf = sm + X::OFF_ROW + kind * 512;
+                    const uint16_t* src = newsrc + ((size_t)pc.b * p.Hkv + kvh) * D;
+                    quantize_row<ENC_INT8, D>(src, rowbuf, rowbuf + 256, lane, nullptr, nullptr, nullptr);
+                    __syncwarp();
+                    const int rr = (pc.L - 1) % kPage;
+                    const long long grow = (long long)row + rr;
+                    uint8_t* gcode = const_cast<uint8_t*>(kind ? p.vc : p.kc) + grow * D;
+                    uint8_t* gscale = const_cast<uint8_t*>(scl) + grow * 2 * NA;
+                    uint8_t* scode = st + jp * X::PAGE_B;
+                    if (lane < D / 16) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(rowbuf + 16 * lane);
+                        *reinterpret_cast<uint4*>(gcode + 16 * lane) = v;
+                        *reinterpret_cast<uint4*>(scode + (lane >> 3) * 2048 + sw_off(rr, lane & 7)) = v;
                     }
-                    if (lane == 0) mbar_arrive(full);
+                    if (lane < NA) {
+                        const uint16_t v = reinterpret_cast<const uint16_t*>(rowbuf + 256)[lane];
+                        reinterpret_cast<uint16_t*>(gscale)[lane] = v;
+                        reinterpret_cast<uint16_t*>(ss + jp * X::SC_B + rr * 2 * NA)[lane] = v;
+                    }
+                    fence_proxy_async();   // before later TMA refills of these bytes
+                    __syncwarp();
                 }
+                if (lane == 0) mbar_arrive(full);
             }
         }
         // every copy issued above has landed before the CTA exits
-        for (uint32_t t = (T >= 2 ? T - 2 : 0); t < T; ++t) {
-            wait_or_flag(&bars[B_KF + (t & 1)], (t >> 1) & 1);
-            wait_or_flag(&bars[B_VF + (t & 1)], (t >> 1) & 1);
-        }
+        for (uint32_t t = (T >= 2 ? T - 2 : 0); t < T; ++t) wait_or_flag(fullb + (t & 1), (t >> 1) & 1);
     } else if (warp == kWMma) {
         // =============================== MMA issue ===============================
         if (lane == 0) {
@@ -347,14 +371,17 @@ __global__ void __launch_bounds__(kThr, 1)
             const uint64_t vd0 = sw128_desc_lbo(smem_addr(sm + X::OFF_VP), 16384, 1024);
             const uint64_t pd0 = sw128_desc_lbo(smem_addr(sm + X::OFF_PP), 16384, 1024);
             const uint32_t tk = tmem + X::KCOL, to = tmem + X::OCOL;
-            // two cursors over the same tiles: QK^T runs ahead of PV
+            // two cursors over the same tiles. The tensor pipe runs MMAs in issue order; PV sits
+            // on the critical path (its V' and P' tiles are single-buffered), so PV goes first and
+            // QK^T runs at most one tile ahead of the next PV, overlapping the V' conversion.
             Walker wq = walker, wv = walker;
             Piece pq, pv;
             bool hq = wq.next(p, pq), hv = wv.next(p, pv);
             int tq = 0, tv = 0;           // tile index inside the current piece
             uint32_t Tq = 0, Tv = 0, pieceq = 0;
             uint32_t idle = 0;
-            while ((hq || hv) && idle < (1u << 28)) {
+            while ((hq || hv) && idle < (1u << 22)) {
+                if ((idle & 63) == 63 && *s_abort) break;
                 bool progressed = false;
                 if (hv && Tv < Tq) {
                     bool ready = mbar_test_wait(&bars[B_PFL], Tv & 1);
@@ -377,7 +404,7 @@ __global__ void __launch_bounds__(kThr, 1)
                         progressed = true;
                     }
                 }
-                if (hq) {
+                if (hq && (!hv || Tq <= Tv + 1)) {
                     const bool first = tq == 0;
                     bool ready = mbar_test_wait(&bars[B_KCV], Tq & 1);
                     if (ready && Tq >= 2) ready = mbar_test_wait(&bars[B_SF + (Tq & 1)], ((Tq >> 1) - 1) & 1);
@@ -405,23 +432,59 @@ __global__ void __launch_bounds__(kThr, 1)
                 }
                 idle = progressed ? 0 : idle + 1;
             }
-            if (hq || hv) atomicOr(&g_err_dtc, kErrWait);
+            if (hq || hv) {
+                atomicOr(&g_err_dtc, kErrWait);
+                *s_abort = 1;
+            }
         }
         __syncwarp();
     } else if (warp >= kSoftW) {
         // =============================== converters ===============================
+        // Eight warps: warp (sub, hf) owns token rows 32 sub .. 32 sub + 31 and half hf of
+        // the head dimension. Iteration T converts K of tile T (Q K^T of a tile may run one
+        // tile ahead of PV) and then V of tile T - 1, so V' waits for nothing but PV of the
+        // tile before it.
         const int cw = warp - kSoftW, sub = cw & 3, hf = cw >> 2;
         const int r = 32 * sub + lane, jpage = r >> 4, rr = r & 15;
         constexpr int NCH = D / 32;   // 16-code chunks per thread (half of the head dimension)
         const uint32_t lb = (uint32_t)(32 * sub) << 16;
+        auto convert_v = [&](uint32_t Tc) {
+            const int buf = Tc & 1;
+            wait_or_flag(&bars[B_VF + buf], (Tc >> 1) & 1);
+            // V' is free once PV of the tile before read it
+            if (Tc >= 1) wait_or_flag(&bars[B_PVD + ((Tc - 1) & 1)], ((Tc - 1) >> 1) & 1);
+            const uint8_t* slot = sm + X::OFF_VST + (buf * kTP + jpage) * X::PAGE_B;
+            uint8_t* vp = sm + X::OFF_VP;
+#pragma unroll
+            for (int i = 0; i < NCH; ++i) {
+                const int gc = hf * NCH + i;
+                const uint4 x = *reinterpret_cast<const uint4*>(slot + (gc >> 3) * 2048 + sw_off(rr, gc & 7));
+                const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+                uint32_t w[8];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    w[2 * k] = hsub2_u32(lop3_and_xor(xs[k], 0x00ff00ffu, 0x64806480u), 0x64806480u);
+                    w[2 * k + 1] = hsub2_u32(lop3_and_xor(xs[k] >> 8, 0x00ff00ffu, 0x64806480u), 0x64806480u);
+                }
+                uint8_t* atom = vp + (gc >> 2) * 16384;
+                const int ch = 2 * (gc & 3);
+                *reinterpret_cast<uint4*>(atom + sw_off(r, ch)) = make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint4*>(atom + sw_off(r, ch + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+            }
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&bars[B_VCV]);
+                mbar_arrive(&bars[B_VE + buf]);
+            }
+        };
         uint32_t T = 0;
         Piece pc;
         while (walker.next(p, pc)) {
             for (int pg0 = pc.p0; pg0 < pc.p1; pg0 += kTP, ++T) {
                 const int buf = T & 1;
-                const uint32_t ph = (T >> 1) & 1;
-                // ---- K: exact fp16 1152 + c, one token per TMEM lane ----
-                wait_or_flag(&bars[B_KF + buf], ph);
+                // ---- K of tile T: exact fp16 1152 + c, one token per TMEM lane ----
+                wait_or_flag(&bars[B_KF + buf], (T >> 1) & 1);
                 if (T >= 1) wait_or_flag(&bars[B_QKD + ((T - 1) & 1)], ((T - 1) >> 1) & 1);
                 tc_fence_after();
                 {
@@ -450,38 +513,11 @@ __global__ void __launch_bounds__(kThr, 1)
                     mbar_arrive(&bars[B_KCV]);
                     mbar_arrive(&bars[B_KE + buf]);
                 }
-                // ---- V: exact fp16 c into the MN-major tile (row = token) ----
-                wait_or_flag(&bars[B_VF + buf], ph);
-                // V' rows of this warp's dims are free once PV of the previous tile read them
-                if (T >= 1) wait_or_flag(&bars[B_PVD + ((T - 1) & 1)], ((T - 1) >> 1) & 1);
-                {
-                    const uint8_t* slot = sm + X::OFF_VST + (buf * kTP + jpage) * X::PAGE_B;
-                    uint8_t* vp = sm + X::OFF_VP;
-#pragma unroll
-                    for (int i = 0; i < NCH; ++i) {
-                        const int gc = hf * NCH + i;
-                        const uint4 x = *reinterpret_cast<const uint4*>(slot + (gc >> 3) * 2048 + sw_off(rr, gc & 7));
-                        const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
-                        uint32_t w[8];
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            w[2 * k] = hsub2_u32(lop3_and_xor(xs[k], 0x00ff00ffu, 0x64806480u), 0x64806480u);
-                            w[2 * k + 1] = hsub2_u32(lop3_and_xor(xs[k] >> 8, 0x00ff00ffu, 0x64806480u), 0x64806480u);
-                        }
-                        uint8_t* atom = vp + (gc >> 2) * 16384;
-                        const int ch = 2 * (gc & 3);
-                        *reinterpret_cast<uint4*>(atom + sw_off(r, ch)) = make_uint4(w[0], w[1], w[2], w[3]);
-                        *reinterpret_cast<uint4*>(atom + sw_off(r, ch + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
-                    }
-                }
-                fence_proxy_async();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&bars[B_VCV]);
-                    mbar_arrive(&bars[B_VE + buf]);
-                }
+                // ---- V of tile T - 1 ----
+                if (T >= 1) convert_v(T - 1);
             }
         }
+        if (T >= 1) convert_v(T - 1);
     } else {
         // =============================== softmax ===============================
         const int r = tid;   // token row of the tile = TMEM lane
