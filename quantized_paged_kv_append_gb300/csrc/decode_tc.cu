@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(kThr, 1)
     // inputs may come from the previous kernel in the stream (programmatic dependent launch)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
-    if (tid == 0) p.rec[c * 8] = 0;   // this CTA closes no multi-piece segment (yet)
+    if (tid == 0 && !p.rec_by_seg) p.rec[c * 8] = 0;   // this CTA closes no multi-piece segment (yet)
     {
         // pages per sequence, prefix over the block, total units
         const int per = (p.B + kThr - 1) / kThr;
@@ -265,6 +265,7 @@ __global__ void __launch_bounds__(kThr, 1)
             const int kvh = hg / (p.Gtot / G), hgi = hg % (p.Gtot / G);
             const int hq0 = kvh * p.Gtot + hgi * G;
             for (int i = tid; i < G * D; i += kThr) write_out<D, G>(p, b, hq0, i, 0.0f);
+            if (tid == 0 && p.rec_by_seg) p.rec[s * 8] = 0;
         }
     }
     Walker walker{*s_b0, *s_pref0, beg, end};
@@ -765,6 +766,7 @@ __global__ void __launch_bounds__(kThr, 1)
             const int npieces = (int)(chi - clo + 1);
             const long long seg = (long long)pc.b * p.NH + pc.hg;
             if (npieces == 1) {
+                if (r == 0 && p.rec_by_seg) p.rec[seg * 8] = 0;
                 for (int i = r; i < G * D; i += 128) {
                     const float Lh = sML[8 + i / D];
                     write_out<D, G>(p, pc.b, hq0, i, Lh > 0.0f ? obuf[i] / Lh : 0.0f);
@@ -779,7 +781,7 @@ __global__ void __launch_bounds__(kThr, 1)
                     mine[8 + r] = sML[8 + r];
                 }
                 if (r == 0 && c == chi) {
-                    int* rc = p.rec + c * 8;
+                    int* rc = p.rec + (p.rec_by_seg ? seg : (long long)c) * 8;
                     rc[1] = (int)clo;
                     rc[2] = (int)seg;
                     rc[3] = pc.b;
@@ -801,8 +803,9 @@ __global__ void __launch_bounds__(kThr, 1)
 
 // ---------------------------------------------------------------------------
 // combine: merge the partial slots of every segment split across CTAs.
-// Grid (G * D / 64, C): block (s, c) merges output floats [64 s, 64 s + 64) of
-// the segment recorded by decode CTA c, with the partial-softmax rule
+// Grid (G * D / 64, R): block (s, y) merges output floats [64 s, 64 s + 64) of
+// the segment in record y (records are per segment when there are no more
+// segments than decode CTAs, else per closing CTA), with the partial-softmax rule
 // M = max m_j, O = sum 2^(m_j - M) O_j / sum 2^(m_j - M) l_j (base-2 scores).
 // ---------------------------------------------------------------------------
 constexpr int kCombThr = 128;
@@ -902,8 +905,10 @@ cudaError_t decode_tc_read_error(unsigned* out, bool clear) {
 // start while its predecessor in the stream drains, and waits for it
 // (griddepcontrol.wait) before touching memory.
 template <int D, int G>
-static cudaError_t launch_tc(int grid, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
+static cudaError_t launch_tc(int grid, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p_in,
                              cudaStream_t st) {
+    DecodeParams p = p_in;
+    p.rec_by_seg = (long long)p.B * p.NH <= grid;
     using X = TG<D>;
     auto fn = decode_tc_kernel<D, G>;
     static bool configured = false;   // per instantiation; the attribute is per device context
@@ -924,7 +929,7 @@ static cudaError_t launch_tc(int grid, const CUtensorMap& tk, const CUtensorMap&
     cfg.numAttrs = 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, fn, tk, tv, p);
     if (e != cudaSuccess) return e;
-    cfg.gridDim = dim3(G * D / 64, grid);
+    cfg.gridDim = dim3(G * D / 64, p.rec_by_seg ? p.B * p.NH : grid);
     cfg.blockDim = dim3(kCombThr);
     cfg.dynamicSmemBytes = 0;
     return cudaLaunchKernelEx(&cfg, decode_tc_combine<D, G>, p);

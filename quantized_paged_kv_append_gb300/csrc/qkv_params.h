@@ -40,7 +40,8 @@ struct DecodeParams {
     int* seg_cnt;        // [S]
     int* grp_cnt;        // [C + S]
     int slot_floats;     // 16 + 8 * D
-    int* rec;            // [C][8]: the multi-piece segment each CTA closes (int8 tensor-core path)
+    int* rec;            // [C][8]: multi-piece segment records for the merge (int8 tensor-core path)
+    int rec_by_seg;      // records indexed by segment (when segments <= CTAs), else by the closing CTA
     const uint16_t* k_new;   // optional bf16 [B][Hkv][D]: quantize-on-write of position seq_lens[b] - 1
     const uint16_t* v_new;
 };
