@@ -379,6 +379,238 @@ def run_reference(args):
     print(json.dumps(res))
 
 
+# ---------------------------------------------------------------------------
+# the other workloads (--workload): one JSON line each, same timing rules
+# ---------------------------------------------------------------------------
+DECODE_CONFIGS = {
+    "int8_2k": dict(fmt="int8", HQ=16, HKV=2, D=256, L=2048),
+    "k8v4_119k": dict(fmt="k8v4", HQ=16, HKV=2, D=256, L=118750),
+    "iso3_82k": dict(fmt="iso3", HQ=16, HKV=4, D=128, L=81920),
+    "iso4_82k": dict(fmt="iso4", HQ=16, HKV=4, D=128, L=81920),
+}
+
+
+def kv_bytes_per_token(fmt, hkv, d):
+    """Packed bytes read per cached token by decode (K and V codes + scales; for
+    ISO4 the 2 reserved bytes per block are not counted)."""
+    if fmt == "int8":
+        return 2 * hkv * (d + 2 * d // 64)
+    if fmt == "k8v4":
+        return hkv * ((d + 2 * d // 64) + (d // 2 + 2 * d // 32))
+    per_block = 50 if fmt == "iso3" else 66
+    return 2 * hkv * (d // 128) * per_block
+
+
+def _time_graph(torch, stream, fn, steps, reps, bracket=False):
+    """Capture `steps` calls of fn(i) in a graph; return (ms per call over `reps`
+    replays, mean ms of one call bracketed by event records or None)."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(steps):
+            fn(i)
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        t1.record(stream)
+    torch.cuda.synchronize()
+    per = t0.elapsed_time(t1) / (steps * reps)
+    one = None
+    if bracket:
+        def ev():
+            try:
+                return torch.cuda.Event(enable_timing=True, external=True)
+            except TypeError:
+                return torch.cuda.Event(enable_timing=True)
+        evs = [(ev(), ev()) for _ in range(steps)]
+        g2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g2, stream=stream):
+            for i in range(steps):
+                evs[i][0].record(stream)
+                fn(i)
+                evs[i][1].record(stream)
+        with torch.cuda.stream(stream):
+            g2.replay()
+            g2.replay()
+        torch.cuda.synchronize()
+        one = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    return per, one
+
+
+def run_decode_config(args, name):
+    import torch
+
+    import quantized_paged_kv_append_gb300 as qkv
+    from quantized_paged_kv_append_gb300 import build as qbuild
+    from quantized_paged_kv_append_gb300 import synth
+
+    cfg = DECODE_CONFIGS[name]
+    fmt, hq, hkv, d, L_ = cfg["fmt"], cfg["HQ"], cfg["HKV"], cfg["D"], cfg["L"]
+    qbuild.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    bpt = kv_bytes_per_token(fmt, hkv, d)
+    step_bytes = L_ * bpt
+    copies = int(min(64, max(2, math.ceil(600e6 / step_bytes))))   # working set well above L2
+    pages = (L_ + 15) // 16
+    seed = args.seed
+    k = synth.tensor_bf16(seed, "k", (L_, hkv, d), outlier_scale=20.0)
+    v = synth.tensor_bf16(seed, "v", (L_, hkv, d))
+    quat = synth.unit_quaternion(seed).tolist() if fmt.startswith("iso") else None
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+    k_d, v_d = bf(k), bf(v)
+    seq_all, pos_all = i32(np.zeros(L_, np.int32)), i32(np.arange(L_, dtype=np.int32))
+    caches, tabs = [], []
+    for c in range(copies):
+        cache = qkv.PagedKVCache(fmt, pages, hkv, d, device=dev, quat=quat)
+        t = i32(synth.page_table(seed * 100 + c, [pages])[0])
+        qkv.append(cache, k_d, v_d, seq_all, pos_all, t)
+        caches.append(cache)
+        tabs.append(t)
+    del k_d, v_d
+    q_d = bf(synth.tensor_bf16(seed, "q", (copies, 1, hq, d)))
+    kn_d = bf(synth.tensor_bf16(seed, "k_new", (copies, 1, hkv, d), outlier_scale=20.0))
+    vn_d = bf(synth.tensor_bf16(seed, "v_new", (copies, 1, hkv, d)))
+    lens = i32(np.array([L_], np.int32))
+    out = torch.empty((1, hq, d), dtype=torch.bfloat16, device=dev)
+    ws = qkv.decode_workspace(caches[0], 1, hq, L_, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    scale = 1.0 / math.sqrt(d)
+
+    def step(i):
+        c = i % copies
+        qkv.decode(caches[c], q_d[c], tabs[c], lens, L_, scale=scale, out=out, workspace=ws, stream=stream,
+                   k_new=kn_d[c, 0], v_new=vn_d[c, 0])
+
+    with torch.cuda.stream(stream):
+        for i in range(max(3, args.warmup)):
+            step(i)
+    torch.cuda.synchronize()
+    assert qkv.device_error() == 0
+    proc, cpath = _clock_sampler()
+    per_ms, one_ms = _time_graph(torch, stream, step, args.steps, max(3, args.reps), bracket=True)
+    clocks = _clock_summary(proc, cpath, 0)
+    peak, peak_kind = peaks()
+    value = step_bytes / (per_ms / 1e3) / 1e9
+    achieved = step_bytes / (one_ms / 1e3) / 1e9
+    kernel = "decode_tc_kernel + decode_tc_combine" if fmt == "int8" else f"decode_kernel<{fmt}> (warp-level mma)"
+    res = {"metric": f"decode-attn packed-KV HBM GB/s, {name}", "value": round(value, 1), "unit": "GB/s",
+           "n_gpus": 1, "steps": args.steps * max(3, args.reps), "warmup": max(3, args.warmup),
+           "ms_per_step": round(per_ms, 5), "us_per_step": round(per_ms * 1e3, 2), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": fmt, "data": "synthetic (seeded splitmix64 + Box-Muller, bf16)",
+           "config": {"workload": f"{fmt} KV decode, batch 1, {hq} q heads / {hkv} KV heads, head_dim {d}, "
+                                  f"{L_} cached tokens, page 16, shuffled page table; step = quantize-on-write "
+                                  f"of 1 token + decode", "layer_copies": copies,
+                      "l2": f"inputs larger than L2: {copies} caches ({copies * step_bytes / 1e9:.2f} GB) cycled"},
+           "pct_of_peak": round(100.0 * value / peak, 2),
+           "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                        "frac": round(achieved / peak, 4), "traffic": None, "peak_kind": peak_kind, "kernel": kernel,
+                        "bytes_per_launch": step_bytes, "timing": "CUDA events around each decode call in a graph"},
+           "clocks": clocks}
+    print(json.dumps(res))
+
+
+def run_mixed(args):
+    """The serving step: 32 decode sequences (lengths uniform on [4096, 65536]),
+    one extend of 2048 tokens over a 32768-token prefix, then the append of the
+    2080 new tokens; int8, 16 q heads / 2 KV heads, head_dim 256. Each phase is
+    timed on its own graph."""
+    import torch
+
+    import quantized_paged_kv_append_gb300 as qkv
+    from quantized_paged_kv_append_gb300 import build as qbuild
+    from quantized_paged_kv_append_gb300 import synth
+
+    qbuild.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    hq, hkv, d, nb, T, L0 = 16, 2, 256, 32, 2048, 32768
+    seed = args.seed
+    lens = synth.seq_lengths(seed, nb, 4096, 65536)
+    lmax = int(lens.max())
+    pages = [int((x + 1 + 15) // 16) for x in lens] + [(L0 + T + 15) // 16]
+    table, npages = synth.page_table(seed, pages)
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+    cache = qkv.PagedKVCache("int8", npages, hkv, d, device=dev)
+    tab_d = i32(table)
+    kbase = bf(synth.tensor_bf16(seed, "k", (max(lmax, L0), hkv, d), outlier_scale=20.0))
+    vbase = bf(synth.tensor_bf16(seed, "v", (max(lmax, L0), hkv, d)))
+    for b in range(nb + 1):
+        n = int(lens[b]) if b < nb else L0
+        qkv.append(cache, kbase[:n], vbase[:n], i32(np.full(n, b, np.int32)), i32(np.arange(n, dtype=np.int32)), tab_d)
+    del kbase, vbase
+    # decode phase (sequences 0..31; row 32 is the extend sequence)
+    q_dec = bf(synth.tensor_bf16(seed, "q", (nb, hq, d)))
+    lens_d = i32(lens)
+    tab_dec = tab_d[:nb].contiguous()
+    ws = qkv.decode_workspace(cache, nb, hq, lmax, device=dev)
+    out_dec = torch.empty((nb, hq, d), dtype=torch.bfloat16, device=dev)
+    # extend phase
+    q_ext = bf(synth.tensor_bf16(seed, "q_ext", (T, hq, d)))
+    k_ext = bf(synth.tensor_bf16(seed, "k_ext", (T, hkv, d), outlier_scale=20.0))
+    v_ext = bf(synth.tensor_bf16(seed, "v_ext", (T, hkv, d)))
+    cu = i32(np.array([0, T], np.int32))
+    pre = i32(np.array([L0], np.int32))
+    tab_ext = tab_d[nb:nb + 1].contiguous()
+    out_ext = torch.empty((T, hq, d), dtype=torch.bfloat16, device=dev)
+    # append phase: the 32 decode tokens (position L_b) and the 2048 extend tokens
+    k_new = torch.cat([bf(synth.tensor_bf16(seed, "k_new", (nb, hkv, d), outlier_scale=20.0)), k_ext])
+    v_new = torch.cat([bf(synth.tensor_bf16(seed, "v_new", (nb, hkv, d))), v_ext])
+    seq_new = i32(np.concatenate([np.arange(nb), np.full(T, nb)]).astype(np.int32))
+    pos_new = i32(np.concatenate([lens, L0 + np.arange(T)]).astype(np.int32))
+    stream = torch.cuda.Stream(device=dev)
+    scale = 1.0 / math.sqrt(d)
+    phases = {
+        "decode": lambda i: qkv.decode(cache, q_dec, tab_dec, lens_d, lmax, scale=scale, out=out_dec, workspace=ws,
+                                       stream=stream),
+        "extend": lambda i: qkv.extend(cache, q_ext, k_ext, v_ext, cu, pre, tab_ext, T, scale=scale, out=out_ext,
+                                       stream=stream),
+        "append": lambda i: qkv.append(cache, k_new, v_new, seq_new, pos_new, tab_d, stream=stream),
+    }
+    for fn in phases.values():
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                fn(i)
+    torch.cuda.synchronize()
+    assert qkv.device_error() == 0
+    proc, cpath = _clock_sampler()
+    res_ph = {}
+    steps = max(10, min(args.steps, 50))
+    for name, fn in phases.items():
+        per_ms, _ = _time_graph(torch, stream, fn, steps, 3)
+        res_ph[name] = per_ms * 1e3
+    clocks = _clock_summary(proc, cpath, 0)
+    peak, _ = peaks()
+    tflops_peak = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["bf16_tflops"]) \
+        if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else 1900.0
+    dec_bytes = int(lens.sum()) * kv_bytes_per_token("int8", hkv, d)
+    ext_flop = 4.0 * T * hq * d * (L0 + (T + 1) / 2)
+    app_bytes = (nb + T) * hkv * (2 * d * 2 + 2 * (d + 2 * d // 64))   # bf16 K, V in; packed K, V out
+    total_us = sum(res_ph.values())
+    res = {"metric": "mixed serving step time (decode 32 seqs + extend 2048 over 32768 + append 2080), int8",
+           "value": round(total_us, 1), "unit": "us", "n_gpus": 1, "steps": steps * 3, "warmup": 3,
+           "ms_per_step": round(total_us / 1e3, 5), "higher_is_better": False, "scaling": "weak",
+           "vs_baseline": None, "dtype": "int8", "data": "synthetic (seeded splitmix64 + Box-Muller, bf16)",
+           "config": {"workload": "32 decode sequences, lengths uniform on [4096, 65536] (seeded), one extend of "
+                                  "2048 tokens over a 32768-token prefix, then the append of the 2080 new tokens; "
+                                  "int8, 16 q heads / 2 KV heads, head_dim 256, page 16",
+                      "decode_tokens": int(lens.sum()), "l2": "decode reads 1.2 GB per step (inputs larger than L2)"},
+           "phases_us": {k: round(v, 2) for k, v in res_ph.items()},
+           "decode_gbs": round(dec_bytes / (res_ph["decode"] / 1e6) / 1e9, 1),
+           "decode_pct_of_hbm_peak": round(100 * dec_bytes / (res_ph["decode"] / 1e6) / 1e9 / peak, 2),
+           "extend_tflops": round(ext_flop / (res_ph["extend"] / 1e6) / 1e12, 1),
+           "extend_pct_of_bf16_peak": round(100 * ext_flop / (res_ph["extend"] / 1e6) / 1e12 / tflops_peak, 2),
+           "append_gbs": round(app_bytes / (res_ph["append"] / 1e6) / 1e9, 1),
+           "clocks": clocks}
+    print(json.dumps(res))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -390,9 +622,18 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layers", type=int, default=8, help="layer caches cycled (8 keeps the working set >> L2)")
+    ap.add_argument("--workload", default="int8_128k",
+                    choices=["int8_128k", "mixed"] + sorted(DECODE_CONFIGS),
+                    help="int8_128k (default) is the headline line; the others print their own line")
     args = ap.parse_args()
     global LAYERS
     LAYERS = max(1, args.layers)
+    if args.workload != "int8_128k" and args.impl == "cuda":
+        if args.workload == "mixed":
+            run_mixed(args)
+        else:
+            run_decode_config(args, args.workload)
+        return
     if args.impl == "reference":
         if args.steps > 10:
             args.steps = 10   # each oracle step is seconds of CPU work
