@@ -729,23 +729,7 @@ __global__ void __launch_bounds__(kThr, 1)
             // ---- end of the piece: O out of TMEM, row sums, merge ----
             wait_or_flag(&bars[B_PVD + ((T - 1) & 1)], ((T - 1) >> 1) & 1);
             tc_fence_after();
-            float* obuf = reinterpret_cast<float*>(sm + X::OFF_PP);   // [G][D]; P' is free now
-            if (warp < NA) {
-                // warp g: lanes h and 8 + h hold the hi and lo rows of head h over the dims of group g
-                const float inv = (E == 1000) ? 0.0f : exp2i(-E);
-#pragma unroll 1
-                for (int c4 = 0; c4 < 4; ++c4) {
-                    float v[16];
-                    tmem_ld16(tmem + lb + X::OCOL + 64 * warp + 16 * c4, v);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) v[j] += __shfl_xor_sync(0xffffffffu, v[j], 8);
-                    if (lane < G) {
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) obuf[lane * D + 64 * warp + perm4(16 * c4 + j)] = v[j] * inv;
-                    }
-                }
-            }
-            tc_fence_before();
+            // row sums first, then O straight from TMEM to the output (or to the partial slot)
 #pragma unroll
             for (int h = 0; h < G; ++h) {
                 float v = l[h];
@@ -765,17 +749,39 @@ __global__ void __launch_bounds__(kThr, 1)
             const long long clo = cta_of(pc.soff), chi = cta_of(pc.soff + pc.np - 1);
             const int npieces = (int)(chi - clo + 1);
             const long long seg = (long long)pc.b * p.NH + pc.hg;
+            float* mine = p.part1 + (size_t)(c + seg) * p.slot_floats;
+            if (warp < NA) {
+                // warp g: lanes h and 8 + h hold the hi and lo rows of head h over the dims of group g
+                const float e_inv = (E == 1000) ? 0.0f : exp2i(-E);
+                const float Lh = lane < G ? sML[8 + lane] : 0.0f;
+                const float inv = npieces == 1 ? (Lh > 0.0f ? e_inv / Lh : 0.0f) : e_inv;
+#pragma unroll 1
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    float v[16];
+                    tmem_ld16(tmem + lb + X::OCOL + 64 * warp + 16 * c4, v);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v[j] += __shfl_xor_sync(0xffffffffu, v[j], 8);
+                    if (lane < G) {
+                        const int d0 = 64 * warp + 16 * c4;
+                        if (npieces == 1) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) write_out<D, G>(p, pc.b, hq0, lane * D + d0 + perm4(j), v[j] * inv);
+                        } else {
+                            float o[16];
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) o[perm4(j)] = v[j] * inv;
+                            float4* dst = reinterpret_cast<float4*>(mine + 16 + lane * D + d0);
+#pragma unroll
+                            for (int q4 = 0; q4 < 4; ++q4) dst[q4] = make_float4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
             if (npieces == 1) {
                 if (r == 0 && p.rec_by_seg) p.rec[seg * 8] = 0;
-                for (int i = r; i < G * D; i += 128) {
-                    const float Lh = sML[8 + i / D];
-                    write_out<D, G>(p, pc.b, hq0, i, Lh > 0.0f ? obuf[i] / Lh : 0.0f);
-                }
             } else {
                 // partial slot of this piece; the combine kernel merges the segment's slots
-                float* mine = p.part1 + (size_t)(c + seg) * p.slot_floats;
-                for (int i = 4 * r; i < G * D; i += 4 * 128)
-                    *reinterpret_cast<float4*>(mine + 16 + i) = *reinterpret_cast<const float4*>(obuf + i);
                 if (r < G) {
                     mine[r] = sML[r];
                     mine[8 + r] = sML[8 + r];
