@@ -634,20 +634,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_proxy_async();
                 mbar_arrive_expect_tx(bar, Geo::TX);
                 const long long row = ((long long)pid * p.Hkv + kvh) * kPage;
+                const uint64_t pol = l2_evict_first_policy();   // pages are read once per launch
                 if constexpr (Geo::K_TMA) {
 #pragma unroll
-                    for (int bx = 0; bx < (Geo::KCB + 127) / 128; ++bx) tma_load_2d(sc + Geo::OFF_KC + bx * 2048, &tmK, bar, bx * 128, (int)row);
+                    for (int bx = 0; bx < (Geo::KCB + 127) / 128; ++bx)
+                        tma_load_2d_hint(sc + Geo::OFF_KC + bx * 2048, &tmK, bar, bx * 128, (int)row, pol);
                 } else {
-                    bulk_load(sc + Geo::OFF_KC, p.kc + row * Geo::KCB, kPage * Geo::KCB, bar);
+                    bulk_load_hint(sc + Geo::OFF_KC, p.kc + row * Geo::KCB, kPage * Geo::KCB, bar, pol);
                 }
                 if constexpr (Geo::V_TMA) {
 #pragma unroll
-                    for (int bx = 0; bx < (Geo::VCB + 127) / 128; ++bx) tma_load_2d(sc + Geo::OFF_VC + bx * 2048, &tmV, bar, bx * 128, (int)row);
+                    for (int bx = 0; bx < (Geo::VCB + 127) / 128; ++bx)
+                        tma_load_2d_hint(sc + Geo::OFF_VC + bx * 2048, &tmV, bar, bx * 128, (int)row, pol);
                 } else {
-                    bulk_load(sc + Geo::OFF_VC, p.vc + row * Geo::VCB, kPage * Geo::VCB, bar);
+                    bulk_load_hint(sc + Geo::OFF_VC, p.vc + row * Geo::VCB, kPage * Geo::VCB, bar, pol);
                 }
-                bulk_load(ss + Geo::OFF_KS, p.ks + row * Geo::KSB, kPage * Geo::KSB, bar);
-                bulk_load(ss + Geo::OFF_VS, p.vs + row * Geo::VSB, kPage * Geo::VSB, bar);
+                bulk_load_hint(ss + Geo::OFF_KS, p.ks + row * Geo::KSB, kPage * Geo::KSB, bar, pol);
+                bulk_load_hint(ss + Geo::OFF_VS, p.vs + row * Geo::VSB, kPage * Geo::VSB, bar, pol);
             }
         };
         // wait for page j; if it holds the sequence's newest token and the call carries

@@ -315,11 +315,13 @@ __global__ void __launch_bounds__(kThr, 1)
                 if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)nload * (X::PAGE_B + X::SC_B));
                 __syncwarp();
                 if (lane < npg && lane != jp) {
+                    // pages are read once per launch: evict-first in L2
                     const int row = (pid * p.Hkv + kvh) * kPage;
+                    const uint64_t pol = l2_evict_first_policy();
 #pragma unroll
                     for (int bx = 0; bx < D / 128; ++bx)
-                        tma_load_2d(st + lane * X::PAGE_B + bx * 2048, tm, full, bx * 128, row);
-                    bulk_load(ss + lane * X::SC_B, scl + (size_t)row * 2 * NA, X::SC_B, full);
+                        tma_load_2d_hint(st + lane * X::PAGE_B + bx * 2048, tm, full, bx * 128, row, pol);
+                    bulk_load_hint(ss + lane * X::SC_B, scl + (size_t)row * 2 * NA, X::SC_B, full, pol);
                 }
                 if (jp >= 0) {
                     // the sequence's newest token: load its page, quantize the new row into the
