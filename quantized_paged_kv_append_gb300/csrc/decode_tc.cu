@@ -102,6 +102,29 @@ __device__ __forceinline__ float exp2i(int n) { return __int_as_float((n + 127) 
 // position inside an aligned group of 4 <-> dimension: the converters emit (d0, d2), (d1, d3)
 __device__ __forceinline__ int perm4(int e) { return (e & ~3) | ((e & 1) << 1) | ((e >> 1) & 1); }
 
+// Warp-wide max (MAX) or sum of each of 8 per-lane values with 9 shuffles instead of
+// 40: every step halves the values a lane carries. On return, lane l holds the result
+// for value (l >> 2) & 7 (all four lanes of a quad hold the same one).
+template <bool MAX>
+__device__ __forceinline__ float warp_reduce8(const float (&v)[8], int lane) {
+    auto op = [](float a, float b) { return MAX ? fmaxf(a, b) : a + b; };
+    float a[4], b2[2];
+    const bool u4 = (lane & 16) != 0, u3 = (lane & 8) != 0, u2 = (lane & 4) != 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float r = __shfl_xor_sync(0xffffffffu, u4 ? v[i] : v[i + 4], 16);
+        a[i] = op(u4 ? v[i + 4] : v[i], r);
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const float r = __shfl_xor_sync(0xffffffffu, u3 ? a[j] : a[j + 2], 8);
+        b2[j] = op(u3 ? a[j + 2] : a[j], r);
+    }
+    float c1 = op(u2 ? b2[1] : b2[0], __shfl_xor_sync(0xffffffffu, u2 ? b2[0] : b2[1], 4));
+    c1 = op(c1, __shfl_xor_sync(0xffffffffu, c1, 2));
+    return op(c1, __shfl_xor_sync(0xffffffffu, c1, 1));
+}
+
 __device__ __forceinline__ int seq_len_clamped(const DecodeParams& p, int b) {
     return max(0, min(p.seq_lens[b], p.max_pages * kPage));
 }
@@ -177,12 +200,8 @@ __global__ void __launch_bounds__(kThr, 1)
     const int C = gridDim.x, c = blockIdx.x;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + X::OFF_BAR);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + X::OFF_MISC);
-    int* s_b0 = reinterpret_cast<int*>(sm + X::OFF_MISC + 8);
-    long long* s_pref0 = reinterpret_cast<long long*>(sm + X::OFF_MISC + 16);
-    long long* s_total = reinterpret_cast<long long*>(sm + X::OFF_MISC + 24);
     volatile int* s_abort = reinterpret_cast<volatile int*>(sm + X::OFF_MISC + 32);
     auto wait_or_flag = [&](uint64_t* bar, uint32_t parity) { return wait_or_abort(bar, parity, s_abort); };
-    __shared__ long long s_wsum[kThr / 32];
 
     // ---------------- set-up: barriers, TMEM, this CTA's share of the units ----------------
     if (tid == 0) {
@@ -204,24 +223,30 @@ __global__ void __launch_bounds__(kThr, 1)
         mbar_init(&bars[B_PAT], 1);
         mbar_init(&bars[B_PAT + 1], 1);
         fence_mbar_init();
-        *s_b0 = p.B;
-        *s_pref0 = 0;
         *s_abort = 0;
     }
     if (warp == kWMma) tmem_alloc(tslot, X::TCOLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
     // inputs may come from the previous kernel in the stream (programmatic dependent launch)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
     if (tid == 0 && !p.rec_by_seg) p.rec[c * 8] = 0;   // this CTA closes no multi-piece segment (yet)
+    // Every warp derives this CTA's share of the (sequence, head group, page) units from
+    // seq_lens on its own, so no block-wide barrier follows the dependency wait and the
+    // producers reach the page table one global load later.
+    int b0 = p.B;
+    long long pref0 = 0, Tunits;
     {
-        // pages per sequence, prefix over the block, total units
-        const int per = (p.B + kThr - 1) / kThr;
-        const int b_lo = min(p.B, tid * per), b_hi = min(p.B, b_lo + per);
+        const int per = (p.B + 31) / 32;
+        const int b_lo = min(p.B, lane * per), b_hi = min(p.B, b_lo + per);
         long long local = 0;
         for (int b = b_lo; b < b_hi; ++b) {
             const int Lr = p.seq_lens[b];
-            if (Lr < 0 || Lr > p.max_pages * kPage) atomicOr(&g_err_dtc, kErrPos);
-            local += (seq_len_clamped(p, b) + kPage - 1) / kPage;
+            if (warp == 0 && (Lr < 0 || Lr > p.max_pages * kPage)) atomicOr(&g_err_dtc, kErrPos);
+            local += (max(0, min(Lr, p.max_pages * kPage)) + kPage - 1) / kPage;
         }
         long long incl = local;
 #pragma unroll
@@ -229,31 +254,25 @@ __global__ void __launch_bounds__(kThr, 1)
             const long long v = __shfl_up_sync(0xffffffffu, incl, off);
             if (lane >= off) incl += v;
         }
-        if (lane == 31) s_wsum[warp] = incl;
-        __syncthreads();
-        long long wpre = 0, total = 0;
-        for (int w = 0; w < kThr / 32; ++w) {
-            if (w < warp) wpre += s_wsum[w];
-            total += s_wsum[w];
-        }
-        const long long T = total * p.NH;
-        const long long beg = T * c / C;
-        long long pref = wpre + incl - local;
+        Tunits = __shfl_sync(0xffffffffu, incl, 31) * p.NH;
+        const long long beg = Tunits * c / C;
+        long long pref = incl - local, fpref = 0;
+        int fb = -1;
         for (int b = b_lo; b < b_hi; ++b) {
             const long long np = (seq_len_clamped(p, b) + kPage - 1) / kPage;
             if (np > 0 && pref * p.NH <= beg && beg < (pref + np) * p.NH) {
-                *s_b0 = b;
-                *s_pref0 = pref;
+                fb = b;
+                fpref = pref;
             }
             pref += np;
         }
-        if (tid == 0) *s_total = T;
+        const unsigned found = __ballot_sync(0xffffffffu, fb >= 0);
+        if (found) {
+            const int src = __ffs(found) - 1;
+            b0 = __shfl_sync(0xffffffffu, fb, src);
+            pref0 = __shfl_sync(0xffffffffu, fpref, src);
+        }
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tslot;
-    const long long Tunits = *s_total;
     const long long beg = Tunits * c / C, end = Tunits * (c + 1) / C;
     auto cta_of = [&](long long x) -> long long { return ((x + 1) * C + Tunits - 1) / Tunits - 1; };
 
@@ -268,7 +287,7 @@ __global__ void __launch_bounds__(kThr, 1)
             if (tid == 0 && p.rec_by_seg) p.rec[s * 8] = 0;
         }
     }
-    Walker walker{*s_b0, *s_pref0, beg, end};
+    Walker walker{b0, pref0, beg, end};
 
     if (warp == kWProd || warp == kWProdV) {
         // ============================ producers (K, V) ============================
@@ -650,12 +669,12 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll
                 for (int h = 0; h < 8; ++h) fac[h] = 1.0f;
                 if (any) {
+                    {
+                        float v8[8];
 #pragma unroll
-                    for (int h = 0; h < G; ++h) {
-                        float v = s[h];
-#pragma unroll
-                        for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-                        if (lane == 0) red_m[buf * 32 + warp * 8 + h] = v;
+                        for (int h = 0; h < 8; ++h) v8[h] = h < G ? s[h < G ? h : 0] : -INFINITY;
+                        const float wm = warp_reduce8<true>(v8, lane);
+                        if ((lane & 3) == 0 && (lane >> 2) < G) red_m[buf * 32 + warp * 8 + (lane >> 2)] = wm;
                     }
                     const int ew = __reduce_max_sync(0xffffffffu, (unsigned)e_row);
                     if (lane == 0) red_e[buf * 4 + warp] = ew;
@@ -732,12 +751,12 @@ __global__ void __launch_bounds__(kThr, 1)
             wait_or_flag(&bars[B_PVD + ((T - 1) & 1)], ((T - 1) >> 1) & 1);
             tc_fence_after();
             // row sums first, then O straight from TMEM to the output (or to the partial slot)
+            {
+                float v8[8];
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                float v = l[h];
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-                if (lane == 0) red_l[warp * 8 + h] = v;
+                for (int h = 0; h < 8; ++h) v8[h] = h < G ? l[h < G ? h : 0] : 0.0f;
+                const float ws = warp_reduce8<false>(v8, lane);
+                if ((lane & 3) == 0 && (lane >> 2) < G) red_l[warp * 8 + (lane >> 2)] = ws;
             }
             soft_sync();
             if (r < G) {
