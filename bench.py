@@ -34,6 +34,9 @@ B, HQ, HKV, D, L = 1, 16, 2, 256, 131072
 LAYERS = 8   # default; --layers overrides
 LAUNCHES_PER_STEP = 2   # int8 decode: the tensor-core kernel and the split-merge (combine) kernel
 KV_BYTES_PER_TOKEN = 2 * HKV * (D + 2 * D // 64)        # int8 codes + fp16 scales, K and V: 1056
+# dram__bytes_read.sum + dram__bytes_write.sum of one decode_tc_kernel<256,8> launch at this workload,
+# from an ncu capture of the current kernel build (138.56 MB read + 3.77 MB written)
+NCU_TRAFFIC_BYTES = 142_334_208
 DECODE_BYTES = L * KV_BYTES_PER_TOKEN                     # 138,412,032 packed bytes read per step
 WORKLOAD = ("int8 KV decode at 128K context: batch 1, 16 q heads / 2 KV heads, head_dim 256, "
             "131072 cached tokens, page 16, shuffled page table; step = quantize-on-write of 1 token + decode")
@@ -306,7 +309,7 @@ def run_gpu(args):
         "pct_of_peak": round(100.0 * value / peak, 2),
         "decode_us": round(dec_ms * 1e3, 2),
         "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(dec_gbs / peak, 4), "traffic": None, "peak_kind": peak_kind,
+                     "frac": round(dec_gbs / peak, 4), "traffic": NCU_TRAFFIC_BYTES, "peak_kind": peak_kind,
                      "kernel": "decode_tc_kernel<256,8> (+ decode_tc_combine)", "bytes_per_launch": DECODE_BYTES,
                      "timing": "CUDA events around each decode call (main + combine launch) in a graph of K steps"
                      if per_launch else "graph time / steps"},
