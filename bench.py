@@ -562,6 +562,7 @@ def run_mixed(args):
     pre = i32(np.array([L0], np.int32))
     tab_ext = tab_d[nb:nb + 1].contiguous()
     out_ext = torch.empty((T, hq, d), dtype=torch.bfloat16, device=dev)
+    ws_ext = qkv.extend_workspace(cache, 1, T, int(tab_ext.shape[1]), device=dev)
     # append phase: the 32 decode tokens (position L_b) and the 2048 extend tokens
     k_new = torch.cat([bf(synth.tensor_bf16(seed, "k_new", (nb, hkv, d), outlier_scale=20.0)), k_ext])
     v_new = torch.cat([bf(synth.tensor_bf16(seed, "v_new", (nb, hkv, d))), v_ext])
@@ -573,7 +574,7 @@ def run_mixed(args):
         "decode": lambda i: qkv.decode(cache, q_dec, tab_dec, lens_d, lmax, scale=scale, out=out_dec, workspace=ws,
                                        stream=stream),
         "extend": lambda i: qkv.extend(cache, q_ext, k_ext, v_ext, cu, pre, tab_ext, T, scale=scale, out=out_ext,
-                                       stream=stream),
+                                       stream=stream, workspace=ws_ext),
         "append": lambda i: qkv.append(cache, k_new, v_new, seq_new, pos_new, tab_d, stream=stream),
     }
     for fn in phases.values():

@@ -170,15 +170,23 @@ QKV_API int kv_decode_attn(const qkv_cache_desc* cache, const void* q, const voi
  * cu_seqlens (int32 [batch + 1]) and prefix_lens (int32 [batch]) are device
  * arrays; max_q_len is a host upper bound on the per-sequence new-token count.
  * out: [total][num_q_heads][head_dim], bf16 or fp32. The caller packs the new
- * tokens afterwards with iso_kv_append (deferred packing). No workspace.
+ * tokens afterwards with iso_kv_append (deferred packing).
+ * workspace: device scratch of at least kv_extend_workspace_size() bytes,
+ * 256-byte aligned, no initialization needed (smaller or misaligned:
+ * QKV_ERR_WORKSPACE). The call first dequantizes the prefix and the chunk's new
+ * keys and values into it (fp16 planes, read by the attention kernel with TMA);
+ * calls sharing a workspace must not overlap in time. A chunk longer than
+ * max_q_len sets the position bit of qkv_device_error and is cut at max_q_len.
  * This build covers the int8 format, head_dim 128 or 256, num_q_heads /
  * num_kv_heads in {1, 2, 4} or a multiple of 8; other requests return
  * QKV_ERR_UNSUPPORTED.
  */
+QKV_API size_t kv_extend_workspace_size(const qkv_cache_desc* cache, int batch, int max_q_len, int max_pages_per_seq);
+
 QKV_API int kv_extend_attn(const qkv_cache_desc* cache, const void* q, const void* k_new, const void* v_new,
                            int num_q_heads, const int32_t* cu_seqlens, const int32_t* prefix_lens, int batch,
                            int max_q_len, const int32_t* page_table, int max_pages_per_seq, float scale, int causal,
-                           void* out, int out_dtype, void* stream);
+                           void* out, int out_dtype, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * kv_decode_attn_noalloc -- kv_decode_attn without a caller-provided workspace.

@@ -15,7 +15,7 @@ import math
 from . import _lib
 from ._lib import FORMATS, QKV_INT8, QKV_K8V4, QKV_ISO3, QKV_ISO4, QkvError  # noqa: F401
 
-__all__ = ["PagedKVCache", "append", "decode", "decode_workspace", "extend", "row_bytes", "iso_levels",
+__all__ = ["PagedKVCache", "append", "decode", "decode_workspace", "extend", "extend_workspace", "row_bytes", "iso_levels",
            "device_error"]
 
 
@@ -130,8 +130,17 @@ def decode(cache: PagedKVCache, q, page_table, seq_lens, max_seq_len: int, scale
     return out
 
 
+def extend_workspace(cache: PagedKVCache, batch: int, max_q_len: int, max_pages_per_seq: int, device="cuda"):
+    """Scratch for extend (the dequantized prefix and chunk); no initialization needed."""
+    torch = _torch()
+    n = _lib.lib().kv_extend_workspace_size(C.byref(cache.desc), batch, max_q_len, max_pages_per_seq)
+    if n == 0:
+        raise QkvError(-1, "kv_extend_workspace_size")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
 def extend(cache: PagedKVCache, q, k_new, v_new, cu_seqlens, prefix_lens, page_table, max_q_len: int, scale=None,
-           causal=True, out=None, out_dtype=None, stream=None):
+           causal=True, out=None, out_dtype=None, stream=None, workspace=None):
     """Extend attention: q bf16 [total, Hq, D], k_new / v_new bf16 [total, Hkv, D]
     (rows of sequence b are cu_seqlens[b]..cu_seqlens[b+1]) over the packed
     prefix [0, prefix_lens[b]) plus the new tokens. Returns out [total, Hq, D]."""
@@ -142,9 +151,12 @@ def extend(cache: PagedKVCache, q, k_new, v_new, cu_seqlens, prefix_lens, page_t
     if out is None:
         out = torch.empty((total, Hq, D), dtype=out_dtype or torch.bfloat16, device=q.device)
     odt = _lib.QKV_OUT_F32 if out.dtype == torch.float32 else _lib.QKV_OUT_BF16
+    B, maxp = int(prefix_lens.numel()), int(page_table.shape[1])
+    if workspace is None and cache.desc.format == _lib.QKV_INT8 and B > 0 and max_q_len > 0:
+        workspace = extend_workspace(cache, B, int(max_q_len), maxp, device=q.device)
+    ws_ptr, ws_bytes = (_ptr(workspace), workspace.numel() * workspace.element_size()) if workspace is not None else (None, 0)
     rc = _lib.lib().kv_extend_attn(C.byref(cache.desc), _ptr(q), _ptr(k_new), _ptr(v_new), Hq, _ptr(cu_seqlens),
-                                   _ptr(prefix_lens), int(prefix_lens.numel()), int(max_q_len), _ptr(page_table),
-                                   int(page_table.shape[1]), float(scale), int(bool(causal)), _ptr(out), odt,
-                                   _stream(stream))
+                                   _ptr(prefix_lens), B, int(max_q_len), _ptr(page_table), maxp, float(scale),
+                                   int(bool(causal)), _ptr(out), odt, ws_ptr, ws_bytes, _stream(stream))
     _lib.check(rc, "kv_extend_attn")
     return out

@@ -160,6 +160,21 @@ int make_code_map(CUtensorMap* map, const void* base, long long rows, int row_by
     return QKV_OK;
 }
 
+// fp16 plane of `rows` rows x `inner` elements, boxes of 64 elements (128 B) x box_rows rows
+int make_f16_map(CUtensorMap* map, const void* base, long long rows, long long inner, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return cuda_fail(cudaErrorNotSupported);
+    cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
+    cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+    return QKV_OK;
+}
+
 // ---------------------------------------------------------------------------
 // validation
 // ---------------------------------------------------------------------------
@@ -217,6 +232,27 @@ int decode_layout(const qkv_cache_desc* d, int batch, int num_q_heads, int sms, 
     L->off_grp = L->off_seg + al((size_t)L->S * sizeof(int));
     L->off_rec = L->off_grp + al(slots * sizeof(int));
     L->bytes = L->off_rec + al((size_t)L->Cmax * 8 * sizeof(int));
+    return QKV_OK;
+}
+
+// Extend workspace: per (sequence, KV head) Lmax keys (the prefix padded to 64,
+// then the chunk padded to 64) of fp16 K' rows, fp16 V^T rows and fp32 key scales.
+struct ExtendLayout {
+    long long Lmax;
+    size_t off_v, off_s, bytes;
+};
+
+int extend_layout(const qkv_cache_desc* d, int batch, int max_q_len, int max_pages_per_seq, ExtendLayout* L) {
+    if (batch < 0 || max_q_len < 0 || max_pages_per_seq <= 0) return QKV_ERR_ARG;
+    auto r64 = [](long long x) { return (x + 63) / 64 * 64; };
+    auto al = [](size_t x) { return (x + 255) / 256 * 256; };
+    L->Lmax = r64((long long)max_pages_per_seq * kPage) + r64(max_q_len);
+    if (L->Lmax > (1LL << 30)) return QKV_ERR_ARG;
+    const size_t heads = (size_t)batch * d->num_kv_heads;
+    const size_t plane = al(heads * (size_t)L->Lmax * d->head_dim * 2);
+    L->off_v = plane;
+    L->off_s = 2 * plane;
+    L->bytes = 2 * plane + al(heads * (size_t)L->Lmax * (d->head_dim / 64) * 4);
     return QKV_OK;
 }
 
@@ -353,10 +389,17 @@ int kv_decode_attn(const qkv_cache_desc* cache, const void* q, const void* k_new
     return QKV_OK;
 }
 
+size_t kv_extend_workspace_size(const qkv_cache_desc* cache, int batch, int max_q_len, int max_pages_per_seq) {
+    if (check_desc(cache)) return 0;
+    ExtendLayout L;
+    if (extend_layout(cache, batch, max_q_len, max_pages_per_seq, &L)) return 0;
+    return L.bytes;
+}
+
 int kv_extend_attn(const qkv_cache_desc* cache, const void* q, const void* k_new, const void* v_new, int num_q_heads,
                    const int32_t* cu_seqlens, const int32_t* prefix_lens, int batch, int max_q_len,
                    const int32_t* page_table, int max_pages_per_seq, float scale, int causal, void* out,
-                   int out_dtype, void* stream) {
+                   int out_dtype, void* workspace, size_t workspace_bytes, void* stream) {
     int rc = check_desc(cache);
     if (rc) return rc;
     if (batch < 0 || max_q_len < 0) return QKV_ERR_ARG;
@@ -370,9 +413,20 @@ int kv_extend_attn(const qkv_cache_desc* cache, const void* q, const void* k_new
     const int Gtot = num_q_heads / cache->num_kv_heads;
     if (!(Gtot == 1 || Gtot == 2 || Gtot == 4 || Gtot % 8 == 0)) return QKV_ERR_GQA;
     if (cache->format != QKV_INT8) return QKV_ERR_UNSUPPORTED;
+    ExtendLayout XL;
+    if ((rc = extend_layout(cache, batch, max_q_len, max_pages_per_seq, &XL))) return rc;
+    if (!workspace || workspace_bytes < XL.bytes || ((uintptr_t)workspace & 255u)) return QKV_ERR_WORKSPACE;
     int dev;
     if ((rc = device_setup(&dev))) return rc;
     const int G = Gtot >= 8 ? 8 : Gtot;
+    const int D = cache->head_dim;
+    uint8_t* ws = (uint8_t*)workspace;
+    const long long heads = (long long)batch * cache->num_kv_heads;
+    CUtensorMap tk, tv;
+    std::memset(&tk, 0, sizeof(tk));
+    std::memset(&tv, 0, sizeof(tv));
+    if ((rc = make_f16_map(&tk, ws, heads * XL.Lmax, D, 64))) return rc;
+    if ((rc = make_f16_map(&tv, ws + XL.off_v, heads * D, XL.Lmax, D))) return rc;
     ExtendParams p;
     p.kc = (const uint8_t*)cache->k_codes;
     p.ks = (const uint8_t*)cache->k_scales;
@@ -394,8 +448,12 @@ int kv_extend_attn(const qkv_cache_desc* cache, const void* q, const void* k_new
     p.causal = causal != 0;
     p.out = out;
     p.out_f32 = out_dtype == QKV_OUT_F32;
+    p.Lmax = (int)XL.Lmax;
+    p.xk = (uint16_t*)ws;
+    p.xv = (uint16_t*)(ws + XL.off_v);
+    p.xs = (float*)(ws + XL.off_s);
     const int NH = cache->num_kv_heads * (Gtot / G);
-    cudaError_t e = extend_launch(cache->format, cache->head_dim, G, max_q_len, NH, batch, p, (cudaStream_t)stream);
+    cudaError_t e = extend_launch(cache->format, D, G, max_q_len, NH, batch, tk, tv, p, (cudaStream_t)stream);
     if (e == cudaErrorInvalidValue) return QKV_ERR_UNSUPPORTED;
     if (e != cudaSuccess) return cuda_fail(e);
     return QKV_OK;

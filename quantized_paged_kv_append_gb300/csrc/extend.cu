@@ -7,17 +7,26 @@
 // quantized KV); "qwen35/q36: --kv - int8 K/V caches", "What it does": prompt
 // chunks dequantize the int8 cache on the fly.
 //
-// GB300 design: one CTA per tile of 128 (token, query head) rows of one KV-head
-// group (GQA packing: 128/G tokens x G heads share every K/V tile), 9 warps:
-//   * warps 0-3 (softmax): thread r owns TMEM lane r = row r. It combines the
-//     per-group partial scores, applies the online softmax (lazy rescale: the
-//     running max only moves when it grows by more than 2^8), writes P (fp16)
-//     to shared memory and rescales the O row in TMEM when the max moves.
-//   * warps 4-7 (producer): fill double-buffered K and V^T tiles of 64 keys in
-//     the UMMA K-major, 128-byte-swizzled layout. Prefix keys come through the
-//     page table as int8 codes (exact fp16 1152 + c for K, fp16(c * scale) for
-//     V); new tokens are bf16 (converted to fp16).
-//   * warp 8 (MMA): owns the 512 TMEM columns and issues tcgen05.mma:
+// GB300 design. A prep kernel dequantizes the keys once per call into the
+// caller's workspace (L2-resident at prefill sizes): per (sequence, KV head),
+// K' rows in fp16 (the exact code c for the packed prefix, the bf16 new tokens
+// converted to fp16) with fp32 key scales beside them (the prefix's K scale per
+// 64-dim group, 1 for new tokens, both times the softmax scale), and V^T in
+// fp16 (c * scale rounded once for the prefix, the new tokens converted), keys
+// padded to 64 so that prefix and new tokens never share a tile. The attention
+// kernel then streams 64-key tiles of K' and V^T with TMA (128-byte swizzle,
+// exactly the UMMA operand layouts): one CTA per tile of 128 (token, query
+// head) rows of one KV-head group (GQA packing: 128/G tokens x G heads share
+// every K/V tile), 6 warps:
+//   * warps 0-7 (softmax): row r = TMEM lane r is shared by two threads, one
+//     per half of the 64 keys (warps w and w + 4). Each combines its keys'
+//     per-group partial scores (4 FMAs a key), the two exchange their row
+//     maxima once per tile, and both apply the same online-softmax frame (lazy
+//     rescale: the running max only moves when it grows by more than 2^8);
+//     each writes its half of P (fp16) and rescales its half of the O row.
+//   * warp 8 (producer, one thread): TMA of the K', V^T and key-scale tiles,
+//     double-buffered.
+//   * warp 9 (MMA): owns the 512 TMEM columns and issues tcgen05.mma:
 //     S_g = Q_g K_g^T per 64-dim group g into 4 x 64 TMEM columns (so the
 //     per-(key, group) K scales stay exact and are applied in fp32 by the
 //     softmax threads), and O += P V^T into 256 columns.
@@ -32,7 +41,9 @@ namespace qkv {
 __device__ unsigned int g_err_extend;
 
 constexpr int kXT = 64;          // keys per KV tile
-constexpr int kXThreads = 288;   // 4 softmax warps, 4 producer warps, 1 MMA warp
+constexpr int kXSoft = 256;      // 8 softmax warps: row r = lane + 32 (w % 4), key half w / 4
+constexpr int kXThreads = 320;   // + 1 producer warp + 1 MMA warp
+constexpr int kXProd = 8, kXMma = 9;
 
 // shared-memory map (bytes from a 1 KB aligned base)
 template <int D>
@@ -45,8 +56,10 @@ struct XGeo {
     static constexpr int OFF_V = OFF_K + 2 * K_BYTES;    // 2 buffers x D rows x 128 B
     static constexpr int V_BYTES = D * 128;
     static constexpr int OFF_P = OFF_V + 2 * V_BYTES;    // 128 rows x 128 B
-    static constexpr int OFF_SIG = OFF_P + 128 * 128;    // 2 x 64 keys x NA floats
-    static constexpr int OFF_BAR = OFF_SIG + 2 * 64 * 4 * 4;
+    static constexpr int KS_BYTES = kXT * NA * 4;        // fp32 K scales x softmax scale of a tile [64][NA]
+    static constexpr int OFF_KS = OFF_P + 128 * 128;     // 2 buffers
+    static constexpr int OFF_RED = OFF_KS + 2 * KS_BYTES;   // [2 tiles][2 halves][128 rows] row-max / row-sum exchange
+    static constexpr int OFF_BAR = OFF_RED + 4 * 128 * 4;
     static constexpr int OFF_TMEM = OFF_BAR + 16 * 8;
     static constexpr int SMEM = OFF_TMEM + 16;
     static constexpr int S_COLS = NA * 64;               // TMEM columns of the group scores
@@ -55,20 +68,134 @@ struct XGeo {
     static_assert(SMEM + 1024 <= 232448 - 1024, "shared memory budget");
 };
 
-enum { B_Q = 0, B_KVF0 = 1, B_KVF1 = 2, B_KVE0 = 3, B_KVE1 = 4, B_SFULL = 5, B_SFREE = 6, B_PFULL = 7, B_PVDONE = 8 };
+enum {
+    B_Q = 0, B_KVF0 = 1, B_KVF1 = 2, B_KVE0 = 3, B_KVE1 = 4, B_SFULL = 5, B_SFREE = 6, B_PFULL = 7, B_PVDONE = 8,
+    B_RMX = 9,    // [2] row maxima of both key halves written (256 softmax threads)
+    B_RSUM = 11   // row sums of both halves written (256)
+};
 
 __device__ __forceinline__ uint32_t bf16x2_to_h2(uint32_t w) {
     return f32x2_to_h2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
+// ---------------------------------------------------------------------------
+// prep: dequantize the keys of one 64-key tile of one (sequence, KV head) into
+// the workspace planes. Tile t < NTP covers prefix positions 64 t .. 64 t + 63
+// (read through the page table), tile NTP + u covers new tokens 64 u .. 64 u + 63.
+// Positions past the prefix or the chunk are zero (their scores are masked and
+// their P is 0, so V must be finite). Thread (i, qd): position i, dims
+// [qd D/4, (qd + 1) D/4). V^T goes through a transposed shared tile.
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) extend_prep_kernel(const ExtendParams p) {
+    constexpr int NA = D / 64, QD = D / 4;
+    __shared__ __align__(16) uint16_t vt[D][kXT + 8];
+    const int b = blockIdx.z, kvh = blockIdx.y, t = blockIdx.x;
+    const int cu0 = p.cu[b], T = max(0, p.cu[b + 1] - cu0);
+    int L0 = p.prefix_lens[b];
+    if (L0 < 0 || L0 > p.max_pages * kPage) L0 = max(0, min(L0, p.max_pages * kPage));   // flagged by the attention kernel
+    const int NTP = (L0 + kXT - 1) / kXT, NTN = (T + kXT - 1) / kXT;
+    if (t >= NTP + NTN) return;
+    const int tid = threadIdx.x, i = tid >> 2, qd = tid & 3;
+    const bool prefix = t < NTP;
+    const size_t krow = ((size_t)b * p.Hkv + kvh) * p.Lmax + (size_t)kXT * t + i;
+    uint32_t kw[QD / 2], vw[QD / 2];
+    float ksv[NA];
+#pragma unroll
+    for (int g = 0; g < NA; ++g) ksv[g] = 0.0f;
+#pragma unroll
+    for (int k = 0; k < QD / 2; ++k) kw[k] = vw[k] = 0u;
+    if (prefix) {
+        const int pos = kXT * t + i;
+        int page = -1;
+        if (pos < L0) {
+            page = p.page_table[(size_t)b * p.max_pages + (pos >> 4)];
+            if (page < 0 || page >= p.num_pages) {
+                atomicOr(&g_err_extend, kErrPage);
+                page = -1;
+            }
+        }
+        if (page >= 0) {
+            const long long row = ((long long)page * p.Hkv + kvh) * kPage + (pos & 15);
+            const uint8_t* ksrc = p.kc + row * D + QD * qd;
+            const uint8_t* vsrc = p.vc + row * D + QD * qd;
+            const uint32_t vsb = reinterpret_cast<const uint16_t*>(p.vs + row * NA * 2)[(QD * qd) / 64];
+            const uint32_t sv2 = vsb | (vsb << 16);
+#pragma unroll
+            for (int c = 0; c < QD / 16; ++c) {
+                const uint4 kx = *reinterpret_cast<const uint4*>(ksrc + 16 * c);
+                const uint4 vx = *reinterpret_cast<const uint4*>(vsrc + 16 * c);
+                const uint32_t ks4[4] = {kx.x, kx.y, kx.z, kx.w}, vs4[4] = {vx.x, vx.y, vx.z, vx.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t x = ks4[u] ^ 0x80808080u;   // 1152 + code, then the exact code
+                    kw[8 * c + 2 * u] = hsub2_u32(prmt(x, 0x64646464u, 0x4140u), 0x64806480u);
+                    kw[8 * c + 2 * u + 1] = hsub2_u32(prmt(x, 0x64646464u, 0x4342u), 0x64806480u);
+                    const uint32_t y = vs4[u] ^ 0x80808080u;
+                    const uint32_t c01 = hsub2_u32(prmt(y, 0x64646464u, 0x4140u), 0x64806480u);
+                    const uint32_t c23 = hsub2_u32(prmt(y, 0x64646464u, 0x4342u), 0x64806480u);
+                    vw[8 * c + 2 * u] = hfma2_u32(c01, sv2, 0u);       // fp16(code * scale), rounded once
+                    vw[8 * c + 2 * u + 1] = hfma2_u32(c23, sv2, 0u);
+                }
+            }
+            if (qd == 0) {
+#pragma unroll
+                for (int g = 0; g < NA; ++g)
+                    ksv[g] = f16_bits_to_f32(reinterpret_cast<const uint16_t*>(p.ks + row * NA * 2)[g]) * p.scale_log2;
+            }
+        }
+    } else {
+        const int n = kXT * (t - NTP) + i;
+        if (n < T) {
+            const uint16_t* ksrc = p.k_new + ((size_t)(cu0 + n) * p.Hkv + kvh) * D + QD * qd;
+            const uint16_t* vsrc = p.v_new + ((size_t)(cu0 + n) * p.Hkv + kvh) * D + QD * qd;
+#pragma unroll
+            for (int c = 0; c < QD / 8; ++c) {
+                const uint4 kx = *reinterpret_cast<const uint4*>(ksrc + 8 * c);
+                const uint4 vx = *reinterpret_cast<const uint4*>(vsrc + 8 * c);
+                kw[4 * c + 0] = bf16x2_to_h2(kx.x);
+                kw[4 * c + 1] = bf16x2_to_h2(kx.y);
+                kw[4 * c + 2] = bf16x2_to_h2(kx.z);
+                kw[4 * c + 3] = bf16x2_to_h2(kx.w);
+                vw[4 * c + 0] = bf16x2_to_h2(vx.x);
+                vw[4 * c + 1] = bf16x2_to_h2(vx.y);
+                vw[4 * c + 2] = bf16x2_to_h2(vx.z);
+                vw[4 * c + 3] = bf16x2_to_h2(vx.w);
+            }
+#pragma unroll
+            for (int g = 0; g < NA; ++g) ksv[g] = p.scale_log2;   // the new tokens carry no K scale
+        }
+    }
+    uint4* kdst = reinterpret_cast<uint4*>(p.xk + krow * D + QD * qd);
+#pragma unroll
+    for (int c = 0; c < QD / 8; ++c) kdst[c] = make_uint4(kw[4 * c], kw[4 * c + 1], kw[4 * c + 2], kw[4 * c + 3]);
+    if (qd == 0) {
+#pragma unroll
+        for (int g = 0; g < NA; ++g) p.xs[krow * NA + g] = ksv[g];
+    }
+#pragma unroll
+    for (int k = 0; k < QD / 2; ++k) {
+        vt[QD * qd + 2 * k][i] = (uint16_t)(vw[k] & 0xffffu);
+        vt[QD * qd + 2 * k + 1][i] = (uint16_t)(vw[k] >> 16);
+    }
+    __syncthreads();
+    for (int d = tid; d < D; d += 256) {
+        uint4* dst = reinterpret_cast<uint4*>(p.xv + (((size_t)b * p.Hkv + kvh) * D + d) * p.Lmax + (size_t)kXT * t);
+        const uint4* src = reinterpret_cast<const uint4*>(&vt[d][0]);
+#pragma unroll
+        for (int c = 0; c < kXT / 8; ++c) dst[c] = src[c];
+    }
+}
+
 template <int D, int G>
-__global__ void __launch_bounds__(kXThreads, 1) extend_kernel(const ExtendParams p) {
+__global__ void __launch_bounds__(kXThreads, 1)
+    extend_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const ExtendParams p) {
     using X = XGeo<D>;
     constexpr int NA = X::NA;
     constexpr int TPT = 128 / G;   // tokens per tile
     extern __shared__ __align__(1024) uint8_t xsmem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(xsmem_raw) + 1023) & ~uintptr_t(1023));
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x, warp = tid >> 5;
     const int b = blockIdx.z, hg = blockIdx.y;
     const int cu0 = p.cu[b], T = p.cu[b + 1] - cu0;
     const int tok0 = blockIdx.x * TPT;
@@ -81,25 +208,30 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(const ExtendParams
     const int kvh = hg / (p.Gtot / G), hq0 = kvh * p.Gtot + (hg % (p.Gtot / G)) * G;
     const int tok_last = min(T, tok0 + TPT) - 1;
     const int NTP = (L0 + kXT - 1) / kXT;
-    const int NTN = p.causal ? (tok_last + kXT) / kXT : (T + kXT - 1) / kXT;
+    int NTN = p.causal ? (tok_last + kXT) / kXT : (T + kXT - 1) / kXT;
+    if (NTP + NTN > p.Lmax / kXT) {   // more new tokens than max_q_len promised
+        if (tid == 0) atomicOr(&g_err_extend, kErrPos);
+        NTN = max(0, p.Lmax / kXT - NTP);
+    }
     const int NT = NTP + NTN;
-    const int32_t* ptrow = p.page_table + (size_t)b * p.max_pages;
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + X::OFF_BAR);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + X::OFF_TMEM);
-    float* sig = reinterpret_cast<float*>(sm + X::OFF_SIG);   // [2][64][4]
 
-    if (warp == 8) tmem_alloc(tmem_slot, X::TMEM_COLS);
+    if (warp == kXMma) tmem_alloc(tmem_slot, X::TMEM_COLS);
     if (tid == 0) {
-        mbar_init(&bars[B_Q], 128);
-        mbar_init(&bars[B_KVF0], 128);
-        mbar_init(&bars[B_KVF1], 128);
+        mbar_init(&bars[B_Q], kXSoft);
+        mbar_init(&bars[B_KVF0], 1);
+        mbar_init(&bars[B_KVF1], 1);
         mbar_init(&bars[B_KVE0], 1);
         mbar_init(&bars[B_KVE1], 1);
         mbar_init(&bars[B_SFULL], 1);
-        mbar_init(&bars[B_SFREE], 128);
-        mbar_init(&bars[B_PFULL], 128);
+        mbar_init(&bars[B_SFREE], kXSoft);
+        mbar_init(&bars[B_PFULL], kXSoft);
         mbar_init(&bars[B_PVDONE], 1);
+        mbar_init(&bars[B_RMX], kXSoft);
+        mbar_init(&bars[B_RMX + 1], kXSoft);
+        mbar_init(&bars[B_RSUM], kXSoft);
         fence_mbar_init();
     }
     tc_fence_before();
@@ -115,161 +247,30 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(const ExtendParams
         }
     };
 
-    if (warp >= 4 && warp < 8) {
+    if (warp == kXProd) {
         // =========================== producer ===========================
-        const int pt = tid - 128;
-        {
-            // Q tile: row r = (token r / G, head r % G), bf16 -> fp16
-            const int r = pt, tok = tok0 + r / G;
-            uint8_t* qs = sm + X::OFF_Q;
-            const uint16_t* qrow = p.q + ((size_t)(cu0 + min(tok, T - 1)) * p.Hq + hq0 + r % G) * D;
-#pragma unroll 4
-            for (int c = 0; c < D / 8; ++c) {
-                uint4 o = make_uint4(0, 0, 0, 0);
-                if (tok < T) {
-                    const uint4 w = *reinterpret_cast<const uint4*>(qrow + 8 * c);
-                    o = make_uint4(bf16x2_to_h2(w.x), bf16x2_to_h2(w.y), bf16x2_to_h2(w.z), bf16x2_to_h2(w.w));
-                }
-                *reinterpret_cast<uint4*>(qs + (c >> 3) * 16384 + sw_off(r, c & 7)) = o;
+        if ((tid & 31) == 0) {
+            const int hrow = b * p.Hkv + kvh;
+            int j = 0;
+            for (; j < NT && ok; ++j) {
+                const int buf = j & 1;
+                if (j >= 2) wait(B_KVE0 + buf, ((j - 2) >> 1) & 1);
+                uint64_t* bar = &bars[B_KVF0 + buf];
+                mbar_arrive_expect_tx(bar, X::K_BYTES + X::V_BYTES + X::KS_BYTES);
+                const int krow0 = hrow * p.Lmax + kXT * j;
+#pragma unroll
+                for (int g = 0; g < NA; ++g)
+                    tma_load_2d(sm + X::OFF_K + buf * X::K_BYTES + g * 8192, &tmK, bar, 64 * g, krow0);
+                tma_load_2d(sm + X::OFF_V + buf * X::V_BYTES, &tmV, bar, kXT * j, hrow * D);
+                bulk_load(sm + X::OFF_KS + buf * X::KS_BYTES, p.xs + (size_t)krow0 * NA, X::KS_BYTES, bar);
             }
-            fence_proxy_async();
-            mbar_arrive(&bars[B_Q]);
+            // every copy issued above has landed before the CTA exits
+            for (int t = (j >= 2 ? j - 2 : 0); t < j; ++t) wait(B_KVF0 + (t & 1), (t >> 1) & 1);
         }
-        for (int j = 0; j < NT && ok; ++j) {
-            const int buf = j & 1;
-            if (j >= 2) wait(B_KVE0 + buf, ((j - 2) >> 1) & 1);
-            uint8_t* ksm = sm + X::OFF_K + buf * X::K_BYTES;
-            uint8_t* vsm = sm + X::OFF_V + buf * X::V_BYTES;
-            float* sg = sig + buf * 64 * 4;
-            const bool prefix = j < NTP;
-            // ---- K tile: thread -> (key kk, half hf of the head dim) ----
-            {
-                constexpr int HALF = D / 2;
-                const int kk = pt >> 1, hf = pt & 1;
-                if (prefix) {
-                    const int pos = kXT * j + kk;
-                    int page = -1;
-                    if (pos < L0) {
-                        page = ptrow[pos >> 4];
-                        if (page < 0 || page >= p.num_pages) { atomicOr(&g_err_extend, kErrPage); page = -1; }
-                    }
-                    const long long row = ((long long)max(page, 0) * p.Hkv + kvh) * kPage + (pos & 15);
-                    const uint8_t* src = p.kc + row * D + HALF * hf;
-#pragma unroll
-                    for (int c = 0; c < HALF / 16; ++c) {
-                        uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
-                        if (page >= 0) {
-                            const uint4 w = *reinterpret_cast<const uint4*>(src + 16 * c);
-                            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-                            uint32_t h[8];
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                const uint32_t x = ws[u] ^ 0x80808080u;   // 1152 + code, exact in fp16
-                                h[2 * u] = prmt(x, 0x64646464u, 0x4140u);
-                                h[2 * u + 1] = prmt(x, 0x64646464u, 0x4342u);
-                            }
-                            o0 = make_uint4(h[0], h[1], h[2], h[3]);
-                            o1 = make_uint4(h[4], h[5], h[6], h[7]);
-                        }
-                        const int d0 = HALF * hf + 16 * c;
-                        uint8_t* atom = ksm + (d0 >> 6) * 8192;
-                        const int cc = (d0 & 63) >> 3;
-                        *reinterpret_cast<uint4*>(atom + sw_off(kk, cc)) = o0;
-                        *reinterpret_cast<uint4*>(atom + sw_off(kk, cc + 1)) = o1;
-                    }
-#pragma unroll
-                    for (int gq = 0; gq < NA / 2; ++gq) {
-                        const int gidx = (NA / 2) * hf + gq;
-                        float sv = 0.0f;
-                        if (page >= 0) sv = f16_bits_to_f32(reinterpret_cast<const uint16_t*>(p.ks + row * (D / 32))[gidx]);
-                        sg[kk * 4 + gidx] = sv;
-                    }
-                } else {
-                    const int n = kXT * (j - NTP) + kk;
-                    const uint16_t* src = p.k_new + ((size_t)(cu0 + min(n, T - 1)) * p.Hkv + kvh) * D + HALF * hf;
-#pragma unroll
-                    for (int c = 0; c < HALF / 8; ++c) {
-                        uint4 o = make_uint4(0, 0, 0, 0);
-                        if (n < T) {
-                            const uint4 w = *reinterpret_cast<const uint4*>(src + 8 * c);
-                            o = make_uint4(bf16x2_to_h2(w.x), bf16x2_to_h2(w.y), bf16x2_to_h2(w.z), bf16x2_to_h2(w.w));
-                        }
-                        const int d0 = HALF * hf + 8 * c;
-                        *reinterpret_cast<uint4*>(ksm + (d0 >> 6) * 8192 + sw_off(kk, (d0 & 63) >> 3)) = o;
-                    }
-#pragma unroll
-                    for (int gq = 0; gq < NA / 2; ++gq) sg[kk * 4 + (NA / 2) * hf + gq] = 1.0f;
-                }
-            }
-            // ---- V^T tile: warp -> 64 dims (one scale group), lane -> keys 2l, 2l+1 ----
-            {
-                const int wv = pt >> 5;                // 0..3
-                for (int dblk = wv; dblk < D / 64; dblk += 4) {
-                    uint32_t hv[2][32];                 // [key][dim pair] half2 of (dim 2m, 2m+1)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int kk = 2 * lane + e;
-                        if (prefix) {
-                            const int pos = kXT * j + kk;
-                            int page = -1;
-                            if (pos < L0) {
-                                page = ptrow[pos >> 4];
-                                if (page < 0 || page >= p.num_pages) page = -1;
-                            }
-                            const long long row = ((long long)max(page, 0) * p.Hkv + kvh) * kPage + (pos & 15);
-                            uint32_t sv2 = 0;
-                            if (page >= 0) {
-                                const uint32_t sb = reinterpret_cast<const uint16_t*>(p.vs + row * (D / 32))[dblk];
-                                sv2 = sb | (sb << 16);
-                            }
-                            const uint8_t* src = p.vc + row * D + 64 * dblk;
-#pragma unroll
-                            for (int c = 0; c < 4; ++c) {
-                                uint4 w = make_uint4(0, 0, 0, 0);
-                                if (page >= 0) w = *reinterpret_cast<const uint4*>(src + 16 * c);
-                                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                                for (int u = 0; u < 4; ++u) {
-                                    const uint32_t x = ws[u] ^ 0x80808080u;
-                                    const uint32_t c01 = hsub2_u32(prmt(x, 0x64646464u, 0x4140u), 0x64806480u);
-                                    const uint32_t c23 = hsub2_u32(prmt(x, 0x64646464u, 0x4342u), 0x64806480u);
-                                    // fp16(code * scale): one correctly rounded fp16 product
-                                    hv[e][8 * c + 2 * u] = hfma2_u32(c01, sv2, 0u);
-                                    hv[e][8 * c + 2 * u + 1] = hfma2_u32(c23, sv2, 0u);
-                                }
-                            }
-                        } else {
-                            const int n = kXT * (j - NTP) + kk;
-                            const uint16_t* src = p.v_new + ((size_t)(cu0 + min(n, T - 1)) * p.Hkv + kvh) * D + 64 * dblk;
-#pragma unroll
-                            for (int c = 0; c < 8; ++c) {
-                                uint4 w = make_uint4(0, 0, 0, 0);
-                                if (n < T) w = *reinterpret_cast<const uint4*>(src + 8 * c);
-                                hv[e][4 * c + 0] = bf16x2_to_h2(w.x);
-                                hv[e][4 * c + 1] = bf16x2_to_h2(w.y);
-                                hv[e][4 * c + 2] = bf16x2_to_h2(w.z);
-                                hv[e][4 * c + 3] = bf16x2_to_h2(w.w);
-                            }
-                        }
-                    }
-                    // V^T row d = 64 dblk + dd holds keys along K: (key 2l, key 2l + 1) -> 4 bytes
-                    const int kc = (2 * lane) >> 3, kb = ((2 * lane) & 7) * 2;
-#pragma unroll
-                    for (int m = 0; m < 32; ++m) {
-                        const int d = 64 * dblk + 2 * m;
-                        const uint32_t lo = prmt(hv[0][m], hv[1][m], 0x5410u);   // dim 2m of both keys
-                        const uint32_t hi = prmt(hv[0][m], hv[1][m], 0x7632u);   // dim 2m + 1
-                        *reinterpret_cast<uint32_t*>(vsm + sw_off(d, kc) + kb) = lo;
-                        *reinterpret_cast<uint32_t*>(vsm + sw_off(d + 1, kc) + kb) = hi;
-                    }
-                }
-            }
-            fence_proxy_async();
-            mbar_arrive(&bars[B_KVF0 + buf]);
-        }
-    } else if (warp == 8) {
+        __syncwarp();
+    } else if (warp == kXMma) {
         // =========================== MMA issue ===========================
-        if (lane == 0) {
+        if ((tid & 31) == 0) {
             const uint32_t qs = smem_addr(sm + X::OFF_Q);
             constexpr uint32_t IDQK = idesc_f16(128, 64), IDPV = idesc_f16(128, D);
             auto issue_qk = [&](int j) {
@@ -304,77 +305,85 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(const ExtendParams
         __syncwarp();
     } else {
         // =========================== softmax ===========================
-        const int r = tid;   // TMEM lane and tile row
+        const int half = warp >> 2;                    // keys [32 half, 32 half + 32) of every tile
+        const int r = 32 * (warp & 3) + (tid & 31);    // TMEM lane and tile row
         const int tok = tok0 + r / G, hq = hq0 + r % G;
         const bool rvalid = tok < T;
         const int tokc = min(tok, T - 1);
-        const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
-        // 1152 * sum of the fp16 query over each 64-dim group removes the K code offset
-        float bias[NA];
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        float* red = reinterpret_cast<float*>(sm + X::OFF_RED);   // [2][128]
         {
+            // Q tile row r = (token r / G, head r % G), bf16 -> fp16; this thread: half the dims
             const uint16_t* qrow = p.q + ((size_t)(cu0 + tokc) * p.Hq + hq) * D;
-#pragma unroll
-            for (int g = 0; g < NA; ++g) {
-                float s = 0.0f;
+            uint8_t* qs = sm + X::OFF_Q;
 #pragma unroll 4
-                for (int c = 0; c < 8; ++c) {
-                    const uint4 w = *reinterpret_cast<const uint4*>(qrow + 64 * g + 8 * c);
-                    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const float2 f = h2_to_f32x2(bf16x2_to_h2(ws[u]));
-                        s += f.x + f.y;
-                    }
+            for (int c = half * (D / 16); c < (half + 1) * (D / 16); ++c) {
+                uint4 o = make_uint4(0, 0, 0, 0);
+                if (rvalid) {
+                    const uint4 w = *reinterpret_cast<const uint4*>(qrow + 8 * c);
+                    o = make_uint4(bf16x2_to_h2(w.x), bf16x2_to_h2(w.y), bf16x2_to_h2(w.z), bf16x2_to_h2(w.w));
                 }
-                bias[g] = 1152.0f * s;
+                *reinterpret_cast<uint4*>(qs + (c >> 3) * 16384 + sw_off(r, c & 7)) = o;
             }
+            fence_proxy_async();
+            mbar_arrive(&bars[B_Q]);
         }
         float m_used = -INFINITY, l = 0.0f;
         uint8_t* psm = sm + X::OFF_P;
         for (int j = 0; j < NT && ok; ++j) {
             const int buf = j & 1;
-            const bool prefix = j < NTP;
-            const float* sg = sig + buf * 64 * 4;
-            wait(B_KVF0 + buf, (j >> 1) & 1);   // the producers' key scales of this tile
+            const float* ksc = reinterpret_cast<const float*>(sm + X::OFF_KS + buf * X::KS_BYTES);   // [64][NA]
+            wait(B_KVF0 + buf, (j >> 1) & 1);   // this tile's key scales
             wait(B_SFULL, j & 1);
             tc_fence_after();
-            float s[kXT];
+            // ---- my 32 keys: s = sum_g (K scale x softmax scale)_g * S_g, base 2 ----
+            float s[kXT / 2];
 #pragma unroll
-            for (int c = 0; c < kXT / 16; ++c) {
-                float acc[16];
+            for (int cc = 0; cc < 2; ++cc) {
+                const int k0 = 32 * half + 16 * cc;
+                uint32_t raw[64];
+                const uint32_t a0 = tmem_S + lane_base + k0;
+                if constexpr (NA == 4) tmem_ld16x4(a0, a0 + 64, a0 + 128, a0 + 192, raw);
+                else tmem_ld16x4(a0, a0 + 64, a0, a0 + 64, raw);
 #pragma unroll
-                for (int e = 0; e < 16; ++e) acc[e] = 0.0f;
-#pragma unroll
-                for (int g = 0; g < NA; ++g) {
-                    float v[16];
-                    tmem_ld16(tmem_S + lane_base + 64 * g + 16 * c, v);
-                    const float bg = prefix ? bias[g] : 0.0f;
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) acc[e] += sg[(16 * c + e) * 4 + g] * (v[e] - bg);
+                for (int e = 0; e < 16; ++e) {
+                    float acc;
+                    if constexpr (NA == 4) {
+                        const float4 w = reinterpret_cast<const float4*>(ksc)[k0 + e];
+                        acc = w.x * __uint_as_float(raw[e]);
+                        acc = fmaf(w.y, __uint_as_float(raw[16 + e]), acc);
+                        acc = fmaf(w.z, __uint_as_float(raw[32 + e]), acc);
+                        acc = fmaf(w.w, __uint_as_float(raw[48 + e]), acc);
+                    } else {
+                        const float2 w = reinterpret_cast<const float2*>(ksc)[k0 + e];
+                        acc = fmaf(w.y, __uint_as_float(raw[16 + e]), w.x * __uint_as_float(raw[e]));
+                    }
+                    s[16 * cc + e] = acc;
                 }
-#pragma unroll
-                for (int e = 0; e < 16; ++e) s[16 * c + e] = acc[e] * p.scale_log2;
             }
             tc_fence_before();
             mbar_arrive(&bars[B_SFREE]);   // S(j) is in registers: QK(j + 1) may overwrite it
-            float rmax = -INFINITY;
+            // ---- masking (only tiles that reach past the prefix, the chunk or the causal edge) ----
+            const int kbase = j < NTP ? kXT * j : kXT * (j - NTP);
+            const int klim = j < NTP ? L0 : (p.causal ? min(T, tokc + 1) : T);   // keys < klim are visible
+            if (kbase + 32 * half + 32 > klim) {
 #pragma unroll
-            for (int kk = 0; kk < kXT; ++kk) {
-                bool vis;
-                if (prefix) vis = (kXT * j + kk) < L0;
-                else {
-                    const int n = kXT * (j - NTP) + kk;
-                    vis = n < T && (!p.causal || n <= tokc);
-                }
-                if (!vis) s[kk] = -INFINITY;
-                rmax = fmaxf(rmax, s[kk]);
+                for (int e = 0; e < kXT / 2; ++e)
+                    if (kbase + 32 * half + e >= klim) s[e] = -INFINITY;
             }
+            float rmax = s[0];
+#pragma unroll
+            for (int e = 1; e < kXT / 2; ++e) rmax = fmaxf(rmax, s[e]);
+            // ---- the row max over both halves (an mbarrier, so that every wait is bounded) ----
+            red[(buf * 2 + half) * 128 + r] = rmax;
+            mbar_arrive(&bars[B_RMX + buf]);
+            wait(B_RMX + buf, (j >> 1) & 1);
+            rmax = fmaxf(red[(buf * 2) * 128 + r], red[(buf * 2 + 1) * 128 + r]);
             // PV(j - 1) must be done before P is overwritten and before O is rescaled
             if (j >= 1) wait(B_PVDONE, (j - 1) & 1);
             tc_fence_after();
-            // frame update per row; the TMEM rescale of O is a whole-warp operation
-            // (tcgen05.ld/st are .sync.aligned), so it runs warp-uniformly with
-            // factor 1 for rows whose frame did not move
+            // frame update per row (both halves decide alike); the TMEM rescale of O is a
+            // whole-warp operation, run warp-uniformly with factor 1 for rows that keep their frame
             const bool move = rmax > m_used + 8.0f;
             float alpha = 1.0f;
             if (move) {
@@ -384,7 +393,7 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(const ExtendParams
             }
             if (j >= 1 && __any_sync(0xffffffffu, move)) {
 #pragma unroll 1
-                for (int c = 0; c < D / 16; ++c) {
+                for (int c = half * (D / 32); c < (half + 1) * (D / 32); ++c) {
                     float v[16];
                     tmem_ld16(tmem_O + lane_base + 16 * c, v);
 #pragma unroll
@@ -394,7 +403,7 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(const ExtendParams
             }
             const float mref = (m_used == -INFINITY) ? 0.0f : m_used;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
+            for (int c = 0; c < 4; ++c) {
                 uint32_t h[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
@@ -403,7 +412,7 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(const ExtendParams
                     const float2 f = h2_to_f32x2(h[u]);
                     l += f.x + f.y;
                 }
-                *reinterpret_cast<uint4*>(psm + sw_off(r, c)) = make_uint4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<uint4*>(psm + sw_off(r, 4 * half + c)) = make_uint4(h[0], h[1], h[2], h[3]);
             }
             fence_proxy_async();
             tc_fence_before();
@@ -411,38 +420,54 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(const ExtendParams
         }
         if (NT > 0) wait(B_PVDONE, (NT - 1) & 1);
         tc_fence_after();
-        const float inv = (l > 0.0f) ? 1.0f / l : 0.0f;
+        // ---- row sum over both halves, then this thread's half of the O row ----
+        const int eb = (NT & 1) * 2;   // the exchange buffer the last tile did not use
+        red[(eb + half) * 128 + r] = l;
+        mbar_arrive(&bars[B_RSUM]);
+        wait(B_RSUM, 0);
+        const float lt = red[eb * 128 + r] + red[(eb + 1) * 128 + r];
+        const float inv = (lt > 0.0f) ? 1.0f / lt : 0.0f;
         const size_t obase = ((size_t)(cu0 + tokc) * p.Hq + hq) * D;
 #pragma unroll 1
-        for (int c = 0; c < D / 16; ++c) {
-            float v[16];
-            tmem_ld16(tmem_O + lane_base + 16 * c, v);
-            if (rvalid) {
-                if (p.out_f32) {
-                    float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + obase + 16 * c);
+        for (int c4 = half * (D / 128); c4 < (half + 1) * (D / 128); ++c4) {
+            uint32_t raw[64];
+            const uint32_t a0 = tmem_O + lane_base + 64 * c4;
+            tmem_ld16x4(a0, a0 + 16, a0 + 32, a0 + 48, raw);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) o[e] = make_float4(v[4 * e] * inv, v[4 * e + 1] * inv, v[4 * e + 2] * inv, v[4 * e + 3] * inv);
-                } else {
-                    uint32_t h[8];
+            for (int cc = 0; cc < 4; ++cc) {
+                const int c = 4 * c4 + cc;
+                float v[16];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        __nv_bfloat162 bb = __floats2bfloat162_rn(v[2 * e] * inv, v[2 * e + 1] * inv);
-                        h[e] = *reinterpret_cast<uint32_t*>(&bb);
+                for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(raw[16 * cc + e]);
+                if (rvalid) {
+                    if (p.out_f32) {
+                        float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + obase + 16 * c);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            o[e] = make_float4(v[4 * e] * inv, v[4 * e + 1] * inv, v[4 * e + 2] * inv, v[4 * e + 3] * inv);
+                    } else {
+                        uint32_t hb[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            __nv_bfloat162 bb = __floats2bfloat162_rn(v[2 * e] * inv, v[2 * e + 1] * inv);
+                            hb[e] = *reinterpret_cast<uint32_t*>(&bb);
+                        }
+                        uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + obase + 16 * c);
+                        o[0] = make_uint4(hb[0], hb[1], hb[2], hb[3]);
+                        o[1] = make_uint4(hb[4], hb[5], hb[6], hb[7]);
                     }
-                    uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + obase + 16 * c);
-                    o[0] = make_uint4(h[0], h[1], h[2], h[3]);
-                    o[1] = make_uint4(h[4], h[5], h[6], h[7]);
                 }
             }
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 8) {
+    if (warp == kXMma) {
         tc_fence_after();
         tmem_dealloc(tmem, X::TMEM_COLS);
     }
 }
+
 
 // ---------------------------------------------------------------------------
 // host side
@@ -455,7 +480,8 @@ cudaError_t extend_read_error(unsigned* out, bool clear) {
 }
 
 template <int D, int G>
-static cudaError_t xlaunch(dim3 grid, const ExtendParams& p, cudaStream_t st) {
+static cudaError_t xlaunch(dim3 grid, const CUtensorMap& tk, const CUtensorMap& tv, const ExtendParams& p,
+                           cudaStream_t st) {
     auto fn = extend_kernel<D, G>;
     constexpr int smem = XGeo<D>::SMEM + 1024;
     static bool configured = false;
@@ -464,28 +490,36 @@ static cudaError_t xlaunch(dim3 grid, const ExtendParams& p, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    fn<<<grid, kXThreads, smem, st>>>(p);
+    fn<<<grid, kXThreads, smem, st>>>(tk, tv, p);
     return cudaGetLastError();
 }
 
-// int8 pools; returns cudaErrorInvalidValue for shapes this kernel does not cover
-cudaError_t extend_launch(int fmt, int D, int G, int max_q_len, int NH, int B, const ExtendParams& p, cudaStream_t st) {
-    if (fmt != 0) return cudaErrorInvalidValue;
+// int8 pools; returns cudaErrorInvalidValue for shapes this kernel does not cover.
+// Two launches: the prep kernel (one block per 64-key tile of every sequence and
+// KV head) writes the workspace planes, the attention kernel reads them.
+cudaError_t extend_launch(int fmt, int D, int G, int max_q_len, int NH, int B, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const ExtendParams& p, cudaStream_t st) {
+    if (fmt != 0 || (D != 128 && D != 256) || !(G == 1 || G == 2 || G == 4 || G == 8)) return cudaErrorInvalidValue;
+    const dim3 pgrid((unsigned)(p.Lmax / kXT), (unsigned)p.Hkv, (unsigned)B);
+    if (D == 256) extend_prep_kernel<256><<<pgrid, 256, 0, st>>>(p);
+    else extend_prep_kernel<128><<<pgrid, 256, 0, st>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
     const int tpt = 128 / G;
     dim3 grid((unsigned)((max_q_len + tpt - 1) / tpt), (unsigned)NH, (unsigned)B);
     if (D == 256) {
         switch (G) {
-            case 1: return xlaunch<256, 1>(grid, p, st);
-            case 2: return xlaunch<256, 2>(grid, p, st);
-            case 4: return xlaunch<256, 4>(grid, p, st);
-            case 8: return xlaunch<256, 8>(grid, p, st);
+            case 1: return xlaunch<256, 1>(grid, tk, tv, p, st);
+            case 2: return xlaunch<256, 2>(grid, tk, tv, p, st);
+            case 4: return xlaunch<256, 4>(grid, tk, tv, p, st);
+            case 8: return xlaunch<256, 8>(grid, tk, tv, p, st);
         }
-    } else if (D == 128) {
+    } else {
         switch (G) {
-            case 1: return xlaunch<128, 1>(grid, p, st);
-            case 2: return xlaunch<128, 2>(grid, p, st);
-            case 4: return xlaunch<128, 4>(grid, p, st);
-            case 8: return xlaunch<128, 8>(grid, p, st);
+            case 1: return xlaunch<128, 1>(grid, tk, tv, p, st);
+            case 2: return xlaunch<128, 2>(grid, tk, tv, p, st);
+            case 4: return xlaunch<128, 4>(grid, tk, tv, p, st);
+            case 8: return xlaunch<128, 8>(grid, tk, tv, p, st);
         }
     }
     return cudaErrorInvalidValue;

@@ -65,6 +65,10 @@ struct ExtendParams {
     int causal;
     void* out;
     int out_f32;
+    int Lmax;            // keys per (sequence, KV head) in the workspace planes (multiple of 64)
+    uint16_t* xk;        // workspace: fp16 K' [B * Hkv][Lmax][D]
+    uint16_t* xv;        // workspace: fp16 V^T [B * Hkv][D][Lmax]
+    float* xs;           // workspace: fp32 key scales x softmax scale [B * Hkv][Lmax][D / 64]
 };
 
 cudaError_t append_upload_levels(const float* lv3, const float* lv4);
@@ -82,7 +86,8 @@ cudaError_t decode_tc_launch(int D, int G, int grid, const CUtensorMap& tk, cons
 cudaError_t decode_tc_read_error(unsigned* out, bool clear);
 
 cudaError_t extend_read_error(unsigned* out, bool clear);
-cudaError_t extend_launch(int fmt, int D, int G, int max_q_len, int NH, int B, const ExtendParams& p, cudaStream_t st);
+cudaError_t extend_launch(int fmt, int D, int G, int max_q_len, int NH, int B, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const ExtendParams& p, cudaStream_t st);
 int decode_max_batch();
 
 }  // namespace qkv
