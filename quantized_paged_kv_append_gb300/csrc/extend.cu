@@ -18,15 +18,17 @@
 // exactly the UMMA operand layouts): one CTA per tile of 128 (token, query
 // head) rows of one KV-head group (GQA packing: 128/G tokens x G heads share
 // every K/V tile), 6 warps:
-//   * warps 0-7 (softmax): row r = TMEM lane r is shared by two threads, one
-//     per half of the 64 keys (warps w and w + 4). Each combines its keys'
-//     per-group partial scores (4 FMAs a key), the two exchange their row
-//     maxima once per tile, and both apply the same online-softmax frame (lazy
+//   * warps 0-15 (softmax): row r = TMEM lane r is shared by four threads, one
+//     per 16 of the 64 keys (warps w, w + 4, w + 8, w + 12). Each combines its
+//     keys' per-group partial scores (4 FMAs a key), the four exchange their row
+//     maxima once per tile, and all apply the same online-softmax frame (lazy
 //     rescale: the running max only moves when it grows by more than 2^8);
-//     each writes its half of P (fp16) and rescales its half of the O row.
-//   * warp 8 (producer, one thread): TMA of the K', V^T and key-scale tiles,
-//     double-buffered.
-//   * warp 9 (MMA): owns the 512 TMEM columns and issues tcgen05.mma:
+//     each writes its part of P (fp16) and rescales its part of the O row.
+//   * warps 16 and 17 (producers, one thread each): TMA of the K' + key-scale
+//     tiles and of the V^T tiles, double-buffered on separate barriers (a K slot
+//     is free once the softmax threads hold the tile's scores and key scales,
+//     long before PV of the tile).
+//   * warp 18 (MMA): owns the 512 TMEM columns and issues tcgen05.mma:
 //     S_g = Q_g K_g^T per 64-dim group g into 4 x 64 TMEM columns (so the
 //     per-(key, group) K scales stay exact and are applied in fp32 by the
 //     softmax threads), and O += P V^T into 256 columns.
@@ -41,9 +43,10 @@ namespace qkv {
 __device__ unsigned int g_err_extend;
 
 constexpr int kXT = 64;          // keys per KV tile
-constexpr int kXSoft = 256;      // 8 softmax warps: row r = lane + 32 (w % 4), key half w / 4
-constexpr int kXThreads = 320;   // + 1 producer warp + 1 MMA warp
-constexpr int kXProd = 8, kXMma = 9;
+constexpr int kXSplit = 4;                 // threads per row: each takes 64 / kXSplit keys of a tile
+constexpr int kXSoft = 128 * kXSplit;      // softmax warps: row r = lane + 32 (w % 4), key part w / 4
+constexpr int kXThreads = kXSoft + 96;     // + 2 producer warps (K, V) + 1 MMA warp
+constexpr int kXProd = kXSoft / 32, kXMma = kXProd + 2;
 
 // shared-memory map (bytes from a 1 KB aligned base)
 template <int D>
@@ -58,8 +61,8 @@ struct XGeo {
     static constexpr int OFF_P = OFF_V + 2 * V_BYTES;    // 128 rows x 128 B
     static constexpr int KS_BYTES = kXT * NA * 4;        // fp32 K scales x softmax scale of a tile [64][NA]
     static constexpr int OFF_KS = OFF_P + 128 * 128;     // 2 buffers
-    static constexpr int OFF_RED = OFF_KS + 2 * KS_BYTES;   // [2 tiles][2 halves][128 rows] row-max / row-sum exchange
-    static constexpr int OFF_BAR = OFF_RED + 4 * 128 * 4;
+    static constexpr int OFF_RED = OFF_KS + 2 * KS_BYTES;   // [2 tiles][kXSplit parts][128 rows] row-max / row-sum exchange
+    static constexpr int OFF_BAR = OFF_RED + 2 * kXSplit * 128 * 4;
     static constexpr int OFF_TMEM = OFF_BAR + 16 * 8;
     static constexpr int SMEM = OFF_TMEM + 16;
     static constexpr int S_COLS = NA * 64;               // TMEM columns of the group scores
@@ -69,9 +72,15 @@ struct XGeo {
 };
 
 enum {
-    B_Q = 0, B_KVF0 = 1, B_KVF1 = 2, B_KVE0 = 3, B_KVE1 = 4, B_SFULL = 5, B_SFREE = 6, B_PFULL = 7, B_PVDONE = 8,
-    B_RMX = 9,    // [2] row maxima of both key halves written (256 softmax threads)
-    B_RSUM = 11   // row sums of both halves written (256)
+    B_Q = 0,
+    B_KF = 1,     // [2] K' tile + key scales landed (1 + tx)
+    B_VF = 3,     // [2] V^T tile landed (1 + tx)
+    B_KE = 5,     // [2] K slot free: every softmax thread has the tile's scores and key scales
+                  //     (after SFULL, so Q K^T of the tile has completed too)
+    B_VE = 7,     // [2] PV of the tile complete: V slot free (commit)
+    B_SFULL = 9, B_SFREE = 10, B_PFULL = 11, B_PVDONE = 12,
+    B_RMX = 13,   // [2] row maxima of every key part written (all softmax threads)
+    B_RSUM = 15   // row sums of every part written
 };
 
 __device__ __forceinline__ uint32_t bf16x2_to_h2(uint32_t w) {
@@ -221,10 +230,12 @@ __global__ void __launch_bounds__(kXThreads, 1)
     if (warp == kXMma) tmem_alloc(tmem_slot, X::TMEM_COLS);
     if (tid == 0) {
         mbar_init(&bars[B_Q], kXSoft);
-        mbar_init(&bars[B_KVF0], 1);
-        mbar_init(&bars[B_KVF1], 1);
-        mbar_init(&bars[B_KVE0], 1);
-        mbar_init(&bars[B_KVE1], 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars[B_KF + i], 1);
+            mbar_init(&bars[B_VF + i], 1);
+            mbar_init(&bars[B_KE + i], kXSoft);
+            mbar_init(&bars[B_VE + i], 1);
+        }
         mbar_init(&bars[B_SFULL], 1);
         mbar_init(&bars[B_SFREE], kXSoft);
         mbar_init(&bars[B_PFULL], kXSoft);
@@ -247,25 +258,33 @@ __global__ void __launch_bounds__(kXThreads, 1)
         }
     };
 
-    if (warp == kXProd) {
-        // =========================== producer ===========================
+    if (warp == kXProd || warp == kXProd + 1) {
+        // ================= producers: K' + key scales (warp kXProd), V^T (warp kXProd + 1) =================
+        // A K slot is refilled as soon as Q K^T of its tile completes, well before PV of the
+        // same tile, so the K stream runs about a tile further ahead than the V stream.
         if ((tid & 31) == 0) {
+            const bool isk = warp == kXProd;
             const int hrow = b * p.Hkv + kvh;
+            const int full0 = isk ? B_KF : B_VF, empty0 = isk ? B_KE : B_VE;
             int j = 0;
             for (; j < NT && ok; ++j) {
                 const int buf = j & 1;
-                if (j >= 2) wait(B_KVE0 + buf, ((j - 2) >> 1) & 1);
-                uint64_t* bar = &bars[B_KVF0 + buf];
-                mbar_arrive_expect_tx(bar, X::K_BYTES + X::V_BYTES + X::KS_BYTES);
+                if (j >= 2) wait(empty0 + buf, ((j - 2) >> 1) & 1);
+                uint64_t* bar = &bars[full0 + buf];
                 const int krow0 = hrow * p.Lmax + kXT * j;
+                if (isk) {
+                    mbar_arrive_expect_tx(bar, X::K_BYTES + X::KS_BYTES);
 #pragma unroll
-                for (int g = 0; g < NA; ++g)
-                    tma_load_2d(sm + X::OFF_K + buf * X::K_BYTES + g * 8192, &tmK, bar, 64 * g, krow0);
-                tma_load_2d(sm + X::OFF_V + buf * X::V_BYTES, &tmV, bar, kXT * j, hrow * D);
-                bulk_load(sm + X::OFF_KS + buf * X::KS_BYTES, p.xs + (size_t)krow0 * NA, X::KS_BYTES, bar);
+                    for (int g = 0; g < NA; ++g)
+                        tma_load_2d(sm + X::OFF_K + buf * X::K_BYTES + g * 8192, &tmK, bar, 64 * g, krow0);
+                    bulk_load(sm + X::OFF_KS + buf * X::KS_BYTES, p.xs + (size_t)krow0 * NA, X::KS_BYTES, bar);
+                } else {
+                    mbar_arrive_expect_tx(bar, X::V_BYTES);
+                    tma_load_2d(sm + X::OFF_V + buf * X::V_BYTES, &tmV, bar, kXT * j, hrow * D);
+                }
             }
             // every copy issued above has landed before the CTA exits
-            for (int t = (j >= 2 ? j - 2 : 0); t < j; ++t) wait(B_KVF0 + (t & 1), (t >> 1) & 1);
+            for (int t = (j >= 2 ? j - 2 : 0); t < j; ++t) wait(full0 + (t & 1), (t >> 1) & 1);
         }
         __syncwarp();
     } else if (warp == kXMma) {
@@ -275,7 +294,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
             constexpr uint32_t IDQK = idesc_f16(128, 64), IDPV = idesc_f16(128, D);
             auto issue_qk = [&](int j) {
                 const int buf = j & 1;
-                wait(B_KVF0 + buf, (j >> 1) & 1);
+                wait(B_KF + buf, (j >> 1) & 1);
                 if (j >= 1) wait(B_SFREE, (j - 1) & 1);
                 tc_fence_after();
                 const uint32_t ks = smem_addr(sm + X::OFF_K + buf * X::K_BYTES);
@@ -292,20 +311,22 @@ __global__ void __launch_bounds__(kXThreads, 1)
             for (int j = 0; j < NT && ok; ++j) {
                 if (j + 1 < NT) issue_qk(j + 1);
                 wait(B_PFULL, j & 1);
+                wait(B_VF + (j & 1), (j >> 1) & 1);
                 tc_fence_after();
                 const uint32_t ps = smem_addr(sm + X::OFF_P);
                 const uint32_t vs = smem_addr(sm + X::OFF_V + (j & 1) * X::V_BYTES);
 #pragma unroll
                 for (int u = 0; u < kXT / 16; ++u)
                     umma_f16(tmem_O, sw128_desc(ps + 32 * u), sw128_desc(vs + 32 * u), IDPV, (j > 0 || u > 0));
-                umma_commit(&bars[B_KVE0 + (j & 1)]);
+                umma_commit(&bars[B_VE + (j & 1)]);
                 umma_commit(&bars[B_PVDONE]);
             }
         }
         __syncwarp();
     } else {
         // =========================== softmax ===========================
-        const int half = warp >> 2;                    // keys [32 half, 32 half + 32) of every tile
+        constexpr int KP = kXT / kXSplit;              // keys per thread and tile
+        const int part = warp >> 2;                    // keys [KP part, KP part + KP) of every tile
         const int r = 32 * (warp & 3) + (tid & 31);    // TMEM lane and tile row
         const int tok = tok0 + r / G, hq = hq0 + r % G;
         const bool rvalid = tok < T;
@@ -313,11 +334,11 @@ __global__ void __launch_bounds__(kXThreads, 1)
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         float* red = reinterpret_cast<float*>(sm + X::OFF_RED);   // [2][128]
         {
-            // Q tile row r = (token r / G, head r % G), bf16 -> fp16; this thread: half the dims
+            // Q tile row r = (token r / G, head r % G), bf16 -> fp16; this thread: a part of the dims
             const uint16_t* qrow = p.q + ((size_t)(cu0 + tokc) * p.Hq + hq) * D;
             uint8_t* qs = sm + X::OFF_Q;
 #pragma unroll 4
-            for (int c = half * (D / 16); c < (half + 1) * (D / 16); ++c) {
+            for (int c = part * (D / 8 / kXSplit); c < (part + 1) * (D / 8 / kXSplit); ++c) {
                 uint4 o = make_uint4(0, 0, 0, 0);
                 if (rvalid) {
                     const uint4 w = *reinterpret_cast<const uint4*>(qrow + 8 * c);
@@ -333,14 +354,14 @@ __global__ void __launch_bounds__(kXThreads, 1)
         for (int j = 0; j < NT && ok; ++j) {
             const int buf = j & 1;
             const float* ksc = reinterpret_cast<const float*>(sm + X::OFF_KS + buf * X::KS_BYTES);   // [64][NA]
-            wait(B_KVF0 + buf, (j >> 1) & 1);   // this tile's key scales
+            wait(B_KF + buf, (j >> 1) & 1);   // this tile's key scales
             wait(B_SFULL, j & 1);
             tc_fence_after();
-            // ---- my 32 keys: s = sum_g (K scale x softmax scale)_g * S_g, base 2 ----
-            float s[kXT / 2];
+            // ---- my KP keys: s = sum_g (K scale x softmax scale)_g * S_g, base 2 ----
+            float s[KP];
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                const int k0 = 32 * half + 16 * cc;
+            for (int cc = 0; cc < KP / 16; ++cc) {
+                const int k0 = KP * part + 16 * cc;
                 uint32_t raw[64];
                 const uint32_t a0 = tmem_S + lane_base + k0;
                 if constexpr (NA == 4) tmem_ld16x4(a0, a0 + 64, a0 + 128, a0 + 192, raw);
@@ -363,22 +384,24 @@ __global__ void __launch_bounds__(kXThreads, 1)
             }
             tc_fence_before();
             mbar_arrive(&bars[B_SFREE]);   // S(j) is in registers: QK(j + 1) may overwrite it
+            mbar_arrive(&bars[B_KE + buf]);   // and the key scales are read: K(j + 2) may land
             // ---- masking (only tiles that reach past the prefix, the chunk or the causal edge) ----
             const int kbase = j < NTP ? kXT * j : kXT * (j - NTP);
             const int klim = j < NTP ? L0 : (p.causal ? min(T, tokc + 1) : T);   // keys < klim are visible
-            if (kbase + 32 * half + 32 > klim) {
+            if (kbase + KP * part + KP > klim) {
 #pragma unroll
-                for (int e = 0; e < kXT / 2; ++e)
-                    if (kbase + 32 * half + e >= klim) s[e] = -INFINITY;
+                for (int e = 0; e < KP; ++e)
+                    if (kbase + KP * part + e >= klim) s[e] = -INFINITY;
             }
             float rmax = s[0];
 #pragma unroll
-            for (int e = 1; e < kXT / 2; ++e) rmax = fmaxf(rmax, s[e]);
-            // ---- the row max over both halves (an mbarrier, so that every wait is bounded) ----
-            red[(buf * 2 + half) * 128 + r] = rmax;
+            for (int e = 1; e < KP; ++e) rmax = fmaxf(rmax, s[e]);
+            // ---- the row max over all parts (an mbarrier, so that every wait is bounded) ----
+            red[(buf * kXSplit + part) * 128 + r] = rmax;
             mbar_arrive(&bars[B_RMX + buf]);
             wait(B_RMX + buf, (j >> 1) & 1);
-            rmax = fmaxf(red[(buf * 2) * 128 + r], red[(buf * 2 + 1) * 128 + r]);
+#pragma unroll
+            for (int q = 0; q < kXSplit; ++q) rmax = fmaxf(rmax, red[(buf * kXSplit + q) * 128 + r]);
             // PV(j - 1) must be done before P is overwritten and before O is rescaled
             if (j >= 1) wait(B_PVDONE, (j - 1) & 1);
             tc_fence_after();
@@ -393,7 +416,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
             }
             if (j >= 1 && __any_sync(0xffffffffu, move)) {
 #pragma unroll 1
-                for (int c = half * (D / 32); c < (half + 1) * (D / 32); ++c) {
+                for (int c = part * (D / 16 / kXSplit); c < (part + 1) * (D / 16 / kXSplit); ++c) {
                     float v[16];
                     tmem_ld16(tmem_O + lane_base + 16 * c, v);
 #pragma unroll
@@ -403,7 +426,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
             }
             const float mref = (m_used == -INFINITY) ? 0.0f : m_used;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < KP / 8; ++c) {
                 uint32_t h[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
@@ -412,7 +435,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
                     const float2 f = h2_to_f32x2(h[u]);
                     l += f.x + f.y;
                 }
-                *reinterpret_cast<uint4*>(psm + sw_off(r, 4 * half + c)) = make_uint4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<uint4*>(psm + sw_off(r, (KP / 8) * part + c)) = make_uint4(h[0], h[1], h[2], h[3]);
             }
             fence_proxy_async();
             tc_fence_before();
@@ -420,22 +443,25 @@ __global__ void __launch_bounds__(kXThreads, 1)
         }
         if (NT > 0) wait(B_PVDONE, (NT - 1) & 1);
         tc_fence_after();
-        // ---- row sum over both halves, then this thread's half of the O row ----
-        const int eb = (NT & 1) * 2;   // the exchange buffer the last tile did not use
-        red[(eb + half) * 128 + r] = l;
+        // ---- row sum over all parts, then this thread's part of the O row ----
+        const int eb = (NT & 1) * kXSplit;   // the exchange buffer the last tile did not use
+        red[(eb + part) * 128 + r] = l;
         mbar_arrive(&bars[B_RSUM]);
         wait(B_RSUM, 0);
-        const float lt = red[eb * 128 + r] + red[(eb + 1) * 128 + r];
+        float lt = 0.0f;
+#pragma unroll
+        for (int q = 0; q < kXSplit; ++q) lt += red[(eb + q) * 128 + r];
         const float inv = (lt > 0.0f) ? 1.0f / lt : 0.0f;
         const size_t obase = ((size_t)(cu0 + tokc) * p.Hq + hq) * D;
-#pragma unroll 1
-        for (int c4 = half * (D / 128); c4 < (half + 1) * (D / 128); ++c4) {
+        constexpr int OC = D / 16 / kXSplit;   // 16-column chunks of O per thread (4 at D = 256, 2 at 128)
+        {
             uint32_t raw[64];
-            const uint32_t a0 = tmem_O + lane_base + 64 * c4;
-            tmem_ld16x4(a0, a0 + 16, a0 + 32, a0 + 48, raw);
+            const uint32_t a0 = tmem_O + lane_base + 16 * OC * part;
+            if constexpr (OC == 4) tmem_ld16x4(a0, a0 + 16, a0 + 32, a0 + 48, raw);
+            else tmem_ld16x4(a0, a0 + 16, a0, a0 + 16, raw);
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                const int c = 4 * c4 + cc;
+            for (int cc = 0; cc < OC; ++cc) {
+                const int c = OC * part + cc;
                 float v[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(raw[16 * cc + e]);
