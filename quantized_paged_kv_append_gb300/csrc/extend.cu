@@ -358,14 +358,16 @@ __global__ void __launch_bounds__(kXThreads, 1)
             wait(B_SFULL, j & 1);
             tc_fence_after();
             // ---- my KP keys: s = sum_g (K scale x softmax scale)_g * S_g, base 2 ----
+            static_assert(KP == 16, "one TMEM load of 16 keys x 4 groups per thread and tile");
             float s[KP];
-#pragma unroll
-            for (int cc = 0; cc < KP / 16; ++cc) {
-                const int k0 = KP * part + 16 * cc;
+            {
+                const int k0 = KP * part;
                 uint32_t raw[64];
                 const uint32_t a0 = tmem_S + lane_base + k0;
                 if constexpr (NA == 4) tmem_ld16x4(a0, a0 + 64, a0 + 128, a0 + 192, raw);
                 else tmem_ld16x4(a0, a0 + 64, a0, a0 + 64, raw);
+                tc_fence_before();
+                mbar_arrive(&bars[B_SFREE]);   // S(j) is in registers: QK(j + 1) may overwrite it
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     float acc;
@@ -379,12 +381,10 @@ __global__ void __launch_bounds__(kXThreads, 1)
                         const float2 w = reinterpret_cast<const float2*>(ksc)[k0 + e];
                         acc = fmaf(w.y, __uint_as_float(raw[16 + e]), w.x * __uint_as_float(raw[e]));
                     }
-                    s[16 * cc + e] = acc;
+                    s[e] = acc;
                 }
             }
-            tc_fence_before();
-            mbar_arrive(&bars[B_SFREE]);   // S(j) is in registers: QK(j + 1) may overwrite it
-            mbar_arrive(&bars[B_KE + buf]);   // and the key scales are read: K(j + 2) may land
+            mbar_arrive(&bars[B_KE + buf]);   // the key scales are read: K(j + 2) may land
             // ---- masking (only tiles that reach past the prefix, the chunk or the causal edge) ----
             const int kbase = j < NTP ? kXT * j : kXT * (j - NTP);
             const int klim = j < NTP ? L0 : (p.causal ? min(T, tokc + 1) : T);   // keys < klim are visible
