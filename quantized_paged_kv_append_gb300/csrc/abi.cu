@@ -383,8 +383,10 @@ int kv_decode_attn(const qkv_cache_desc* cache, const void* q, const void* k_new
     p.slot_floats = L.slot_floats;
     p.k_new = (const uint16_t*)k_new;
     p.v_new = (const uint16_t*)v_new;
-    cudaError_t e = cache->format == QKV_INT8 ? decode_tc_launch(D, L.G, grid, tk, tv, p, (cudaStream_t)stream)
-                                              : decode_launch(cache->format, D, L.G, grid, tk, tv, p, (cudaStream_t)stream);
+    // int8 and k8v4: the tcgen05 kernel; ISO3 / ISO4: the warp-level mma kernel
+    const bool tc = cache->format == QKV_INT8 || cache->format == QKV_K8V4;
+    cudaError_t e = tc ? decode_tc_launch(D, L.G, grid, cache->format == QKV_K8V4, tk, tv, p, (cudaStream_t)stream)
+                       : decode_launch(cache->format, D, L.G, grid, tk, tv, p, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e);
     return QKV_OK;
 }

@@ -52,20 +52,26 @@ constexpr int kWMma = kWProd + 1;           // MMA warp
 constexpr int kWProdV = kWMma + 1;          // producer warp of the V planes
 constexpr int kThr = (kWProdV + 1) * 32;    // 480 threads
 
-template <int D>
+// VQ: V planes hold q4_0 codes of the FWHT-rotated vector (k8v4), else int8.
+template <int D, bool VQ>
 struct TG {
-    static constexpr int NA = D / 64;             // 64-dim atoms = int8 scale groups
-    static constexpr int NHf = D / 128;           // PV halves of 128 dims
-    static constexpr int PAGE_B = D * kPage;      // staged codes of one page: D / 128 boxes of 2048 B
-    static constexpr int SC_B = kPage * 2 * NA;   // staged scales of one page
+    static constexpr int NA = D / 64;             // 64-dim atoms = int8 K scale groups
+    static constexpr int VG = VQ ? D / 32 : D / 64;   // V scale groups
+    static constexpr int PG = VQ ? VG : 4;        // P' column groups of 16 (8 heads hi + lo); int8 pads to 4
+    static constexpr int PM = 16 * PG;            // M of the PV MMA: 64 (int8) or 128 (q4)
+    static constexpr int PAGE_B = D * kPage;      // staged K codes of one page: D / 128 boxes of 2048 B
+    static constexpr int VPAGE_B = (VQ ? D / 2 : D) * kPage;   // staged V codes of one page
+    static constexpr int VBOX = VPAGE_B / 2048;   // 128-byte TMA boxes per V page
+    static constexpr int SC_B = kPage * 2 * NA;   // staged K scales of one page
+    static constexpr int VSC_B = kPage * 2 * VG;  // staged V scales of one page
     static constexpr int OFF_KST = 0;                               // [2][8][PAGE_B]
-    static constexpr int OFF_VST = OFF_KST + 2 * kTP * PAGE_B;      // [2][8][PAGE_B]
-    static constexpr int OFF_VP = OFF_VST + 2 * kTP * PAGE_B;       // V' [NA][128 rows][128 B]
-    static constexpr int OFF_PP = OFF_VP + NA * 16384;              // P' [128 rows][128 B]
-    static constexpr int OFF_Q = OFF_PP + 16384;                    // Q [NA][16 rows][128 B]
+    static constexpr int OFF_VST = OFF_KST + 2 * kTP * PAGE_B;      // [2][8][VPAGE_B]
+    static constexpr int OFF_VP = OFF_VST + 2 * kTP * VPAGE_B;      // V' [NA][128 rows][128 B]
+    static constexpr int OFF_PP = OFF_VP + NA * 16384;              // P' [PM / 64][128 rows][128 B]
+    static constexpr int OFF_Q = OFF_PP + (PM / 64) * 16384;        // Q [NA][16 rows][128 B]
     static constexpr int OFF_KSC = OFF_Q + NA * 2048;               // [2][8][SC_B]
-    static constexpr int OFF_VSC = OFF_KSC + 2 * kTP * SC_B;        // [2][8][SC_B]
-    static constexpr int OFF_BIAS = OFF_VSC + 2 * kTP * SC_B;       // float [NA][8]
+    static constexpr int OFF_VSC = OFF_KSC + 2 * kTP * SC_B;        // [2][8][VSC_B]
+    static constexpr int OFF_BIAS = OFF_VSC + 2 * kTP * VSC_B;      // float [NA][8]
     static constexpr int OFF_RED = OFF_BIAS + 256;                  // softmax-warp reductions
     static constexpr int OFF_ROW = OFF_RED + 512;                   // quantize-on-write rows [2][512]
     static constexpr int OFF_BAR = OFF_ROW + 1024;
@@ -77,7 +83,8 @@ struct TG {
     static constexpr int TCOLS = (OCOL + D) <= 256 ? 256 : 512;
     static_assert(OCOL + D <= 512, "TMEM budget");
     static_assert(SMEM + 1024 <= 232448 - 1024, "shared memory budget");
-    static_assert(2 * kTP * SC_B <= 4096, "scale staging");
+    static_assert(2 * kTP * SC_B <= 4096 && 2 * kTP * VSC_B <= 4096, "scale staging");
+    static_assert(!VQ || D == 256, "q4 V is FWHT-256 rotated");
 };
 
 enum {
@@ -188,11 +195,11 @@ __device__ void write_out(const DecodeParams& p, int b, int hq0, int i, float v)
 
 }  // namespace
 
-template <int D, int G>
+template <int D, int G, bool VQ>
 __global__ void __launch_bounds__(kThr, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const DecodeParams p) {
-    using X = TG<D>;
+    using X = TG<D, VQ>;
     constexpr int NA = X::NA;
     extern __shared__ __align__(1024) uint8_t dsm_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~uintptr_t(1023));
@@ -300,6 +307,9 @@ __global__ void __launch_bounds__(kThr, 1)
         const CUtensorMap* tm = kind ? &tmV : &tmK;
         const uint8_t* scl = kind ? p.vs : p.ks;
         const uint16_t* newsrc = kind ? p.v_new : p.k_new;
+        // per-plane geometry: V pages of q4 codes are half as wide and carry twice the scales
+        const int pageb = kind ? X::VPAGE_B : X::PAGE_B, scb = kind ? X::VSC_B : X::SC_B;
+        const int nbox = kind ? X::VBOX : D / 128, scrow = kind ? 2 * X::VG : 2 * NA;
         uint32_t T = 0, pat_phase = 0;
         Piece pc;
         while (walker.next(p, pc)) {
@@ -328,19 +338,18 @@ __global__ void __launch_bounds__(kThr, 1)
                 const int pid_patch = __shfl_sync(0xffffffffu, pid, jp < 0 ? 0 : jp);
                 if (T >= 2) wait_or_flag(emptyb + buf, ((T >> 1) - 1) & 1);
                 uint64_t* full = fullb + buf;
-                uint8_t* st = sm + (kind ? X::OFF_VST : X::OFF_KST) + buf * kTP * X::PAGE_B;
-                uint8_t* ss = sm + (kind ? X::OFF_VSC : X::OFF_KSC) + buf * kTP * X::SC_B;
+                uint8_t* st = sm + (kind ? X::OFF_VST : X::OFF_KST) + buf * kTP * pageb;
+                uint8_t* ss = sm + (kind ? X::OFF_VSC : X::OFF_KSC) + buf * kTP * scb;
                 const int nload = npg - (jp >= 0 ? 1 : 0);
-                if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)nload * (X::PAGE_B + X::SC_B));
+                if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)nload * (pageb + scb));
                 __syncwarp();
                 if (lane < npg && lane != jp) {
                     // pages are read once per launch: evict-first in L2
                     const int row = (pid * p.Hkv + kvh) * kPage;
                     const uint64_t pol = l2_evict_first_policy();
-#pragma unroll
-                    for (int bx = 0; bx < D / 128; ++bx)
-                        tma_load_2d_hint(st + lane * X::PAGE_B + bx * 2048, tm, full, bx * 128, row, pol);
-                    bulk_load_hint(ss + lane * X::SC_B, scl + (size_t)row * 2 * NA, X::SC_B, full, pol);
+                    for (int bx = 0; bx < nbox; ++bx)
+                        tma_load_2d_hint(st + lane * pageb + bx * 2048, tm, full, bx * 128, row, pol);
+                    bulk_load_hint(ss + lane * scb, scl + (size_t)row * scrow, scb, full, pol);
                 }
                 if (jp >= 0) {
                     // the sequence's newest token: load its page, quantize the new row into the
@@ -348,32 +357,33 @@ __global__ void __launch_bounds__(kThr, 1)
                     const int row = (pid_patch * p.Hkv + kvh) * kPage;
                     uint64_t* pb = &bars[B_PAT + kind];
                     if (lane == 0) {
-                        mbar_arrive_expect_tx(pb, X::PAGE_B + X::SC_B);
-#pragma unroll
-                        for (int bx = 0; bx < D / 128; ++bx)
-                            tma_load_2d(st + jp * X::PAGE_B + bx * 2048, tm, pb, bx * 128, row);
-                        bulk_load(ss + jp * X::SC_B, scl + (size_t)row * 2 * NA, X::SC_B, pb);
+                        mbar_arrive_expect_tx(pb, pageb + scb);
+                        for (int bx = 0; bx < nbox; ++bx)
+                            tma_load_2d(st + jp * pageb + bx * 2048, tm, pb, bx * 128, row);
+                        bulk_load(ss + jp * scb, scl + (size_t)row * scrow, scb, pb);
                     }
                     wait_or_flag(pb, pat_phase);
                     pat_phase ^= 1;
                     uint8_t* rowbuf = sm + X::OFF_ROW + kind * 512;
                     const uint16_t* src = newsrc + ((size_t)pc.b * p.Hkv + kvh) * D;
-                    quantize_row<ENC_INT8, D>(src, rowbuf, rowbuf + 256, lane, nullptr, nullptr, nullptr);
+                    if (VQ && kind) quantize_row<ENC_Q4, D>(src, rowbuf, rowbuf + 256, lane, nullptr, nullptr, nullptr);
+                    else quantize_row<ENC_INT8, D>(src, rowbuf, rowbuf + 256, lane, nullptr, nullptr, nullptr);
                     __syncwarp();
                     const int rr = (pc.L - 1) % kPage;
                     const long long grow = (long long)row + rr;
-                    uint8_t* gcode = const_cast<uint8_t*>(kind ? p.vc : p.kc) + grow * D;
-                    uint8_t* gscale = const_cast<uint8_t*>(scl) + grow * 2 * NA;
-                    uint8_t* scode = st + jp * X::PAGE_B;
-                    if (lane < D / 16) {
+                    const int rowb = pageb / kPage;   // code bytes of one row
+                    uint8_t* gcode = const_cast<uint8_t*>(kind ? p.vc : p.kc) + grow * rowb;
+                    uint8_t* gscale = const_cast<uint8_t*>(scl) + grow * scrow;
+                    uint8_t* scode = st + jp * pageb;
+                    if (lane < rowb / 16) {
                         const uint4 v = *reinterpret_cast<const uint4*>(rowbuf + 16 * lane);
                         *reinterpret_cast<uint4*>(gcode + 16 * lane) = v;
                         *reinterpret_cast<uint4*>(scode + (lane >> 3) * 2048 + sw_off(rr, lane & 7)) = v;
                     }
-                    if (lane < NA) {
+                    if (lane < scrow / 2) {
                         const uint16_t v = reinterpret_cast<const uint16_t*>(rowbuf + 256)[lane];
                         reinterpret_cast<uint16_t*>(gscale)[lane] = v;
-                        reinterpret_cast<uint16_t*>(ss + jp * X::SC_B + rr * 2 * NA)[lane] = v;
+                        reinterpret_cast<uint16_t*>(ss + jp * scb + rr * scrow)[lane] = v;
                     }
                     fence_proxy_async();   // before later TMA refills of these bytes
                     __syncwarp();
@@ -387,7 +397,7 @@ __global__ void __launch_bounds__(kThr, 1)
         // =============================== MMA issue ===============================
         if (lane == 0) {
             constexpr uint32_t IDQK = idesc_f16(128, 16);
-            constexpr uint32_t IDPV = idesc_f16(64, D, 1, 1);
+            constexpr uint32_t IDPV = idesc_f16(X::PM, D, 1, 1);
             // base descriptors; every MMA adds a compile-time offset (16-byte units) to them
             const uint64_t qd0 = sw128_desc(smem_addr(sm + X::OFF_Q));
             const uint64_t vd0 = sw128_desc_lbo(smem_addr(sm + X::OFF_VP), 16384, 1024);
@@ -475,8 +485,33 @@ __global__ void __launch_bounds__(kThr, 1)
             wait_or_flag(&bars[B_VF + buf], (Tc >> 1) & 1);
             // V' is free once PV of the tile before read it
             if (Tc >= 1) wait_or_flag(&bars[B_PVD + ((Tc - 1) & 1)], ((Tc - 1) >> 1) & 1);
-            const uint8_t* slot = sm + X::OFF_VST + (buf * kTP + jpage) * X::PAGE_B;
+            const uint8_t* slot = sm + X::OFF_VST + (buf * kTP + jpage) * X::VPAGE_B;
             uint8_t* vp = sm + X::OFF_VP;
+            if constexpr (VQ) {
+                // q4_0 block b (32 dims: 16 code bytes, byte j = element j low, j + 16 high nibble)
+                // -> exact fp16 (q - 8). Pairs come out as (4w, 4w + 2), (4w + 1, 4w + 3): the same
+                // position <-> dimension permutation (perm4) as the int8 path.
+#pragma unroll
+                for (int bi = 0; bi < D / 64; ++bi) {
+                    const int blk = (D / 64) * hf + bi;
+                    const uint4 x = *reinterpret_cast<const uint4*>(slot + sw_off(rr, blk));
+                    const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+                    uint32_t lo[8], hi[8];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        lo[2 * k] = hsub2_u32((xs[k] & 0x000f000fu) | 0x64006400u, 0x64086408u);
+                        lo[2 * k + 1] = hsub2_u32(((xs[k] >> 8) & 0x000f000fu) | 0x64006400u, 0x64086408u);
+                        hi[2 * k] = hsub2_u32(((xs[k] >> 4) & 0x000f000fu) | 0x64006400u, 0x64086408u);
+                        hi[2 * k + 1] = hsub2_u32(((xs[k] >> 12) & 0x000f000fu) | 0x64006400u, 0x64086408u);
+                    }
+                    uint8_t* atom = vp + (blk >> 1) * 16384;
+                    const int ch = 4 * (blk & 1);
+                    *reinterpret_cast<uint4*>(atom + sw_off(r, ch)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    *reinterpret_cast<uint4*>(atom + sw_off(r, ch + 1)) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+                    *reinterpret_cast<uint4*>(atom + sw_off(r, ch + 2)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4*>(atom + sw_off(r, ch + 3)) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+                }
+            } else
 #pragma unroll
             for (int i = 0; i < NCH; ++i) {
                 const int gc = hf * NCH + i;
@@ -641,12 +676,12 @@ __global__ void __launch_bounds__(kThr, 1)
                 for (int h = 0; h < G; ++h) s[h] = valid ? s[h] * p.scale_log2 : -INFINITY;
                 // ---- V scales ----
                 wait_or_flag(&bars[B_VF + buf], ph);
-                float vsf[NA];
+                float vsf[X::VG];
                 int e_row = 0;
                 {
-                    const uint8_t* vsr = sm + X::OFF_VSC + (buf * kTP + jpage) * X::SC_B + (r & 15) * 2 * NA;
+                    const uint8_t* vsr = sm + X::OFF_VSC + (buf * kTP + jpage) * X::VSC_B + (r & 15) * 2 * X::VG;
 #pragma unroll
-                    for (int g = 0; g < NA; ++g) {
+                    for (int g = 0; g < X::VG; ++g) {
                         const uint32_t hb = reinterpret_cast<const uint16_t*>(vsr)[g];
                         vsf[g] = f16_bits_to_f32(hb);
                         e_row = max(e_row, (int)((hb & 0x7fffu) >> 10));
@@ -724,10 +759,10 @@ __global__ void __launch_bounds__(kThr, 1)
                     const float e2 = (E == 1000) ? 1.0f : exp2i(E);
                     uint8_t* pp = sm + X::OFF_PP;
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) {
+                    for (int g = 0; g < X::PG; ++g) {
                         uint32_t hw[4] = {0u, 0u, 0u, 0u}, lw[4] = {0u, 0u, 0u, 0u};
-                        if (g < NA && valid) {
-                            const float sc = vsf[g < NA ? g : 0] * e2;
+                        if (g < X::VG && valid) {
+                            const float sc = vsf[g < X::VG ? g : 0] * e2;
                             float P[8];
 #pragma unroll
                             for (int h = 0; h < 8; ++h) P[h] = h < G ? pr[h < G ? h : 0] * sc : 0.0f;
@@ -738,8 +773,9 @@ __global__ void __launch_bounds__(kThr, 1)
                                 lw[k] = f32x2_to_h2(P[2 * k] - f.x, P[2 * k + 1] - f.y);
                             }
                         }
-                        *reinterpret_cast<uint4*>(pp + sw_off(r, 2 * g)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                        *reinterpret_cast<uint4*>(pp + sw_off(r, 2 * g + 1)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                        uint8_t* pa = pp + (g >> 2) * 16384;   // 64 P' columns (4 groups) per atom
+                        *reinterpret_cast<uint4*>(pa + sw_off(r, 2 * (g & 3))) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                        *reinterpret_cast<uint4*>(pa + sw_off(r, 2 * (g & 3) + 1)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
                     }
                 }
                 fence_proxy_async();
@@ -771,7 +807,77 @@ __global__ void __launch_bounds__(kThr, 1)
             const int npieces = (int)(chi - clo + 1);
             const long long seg = (long long)pc.b * p.NH + pc.hg;
             float* mine = p.part1 + (size_t)(c + seg) * p.slot_floats;
-            if (warp < NA) {
+            if constexpr (VQ) {
+                // q4 V (M = 128, lane = O row 16 g + j): warp w holds groups 2w (lanes 0-15) and
+                // 2w + 1 (lanes 16-31). The rotated output goes per head to shared memory (the P'
+                // area is free), the inverse rotation (FWHT-256 x 1/16, its own inverse) runs there,
+                // then the output or the partial slot is written. The rotation is linear, so the
+                // merge of partial slots commutes with it.
+                float* ox = reinterpret_cast<float*>(sm + X::OFF_PP);   // [8 heads][D]
+                {
+                    const int h = lane & 7, grp = lane >> 4;
+                    const float e_inv = (E == 1000) ? 0.0f : exp2i(-E);
+                    const float Lh = h < G ? sML[8 + (h < G ? h : 0)] : 0.0f;
+                    const float inv = npieces == 1 ? (Lh > 0.0f ? e_inv / Lh : 0.0f) : e_inv;
+#pragma unroll 1
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        float v[16];
+                        tmem_ld16(tmem + lb + X::OCOL + 64 * warp + 16 * c4, v);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) v[j] += __shfl_xor_sync(0xffffffffu, v[j], 8);
+                        if ((lane & 8) == 0 && (c4 >> 1) == grp && h < G) {
+                            const int d0 = 64 * warp + 16 * c4;
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) ox[h * D + d0 + perm4(j)] = v[j] * inv;
+                        }
+                    }
+                }
+                soft_sync();
+                const int hh = r >> 4, q = r & 15;   // thread (head, 16-dim slice)
+                if (hh < G) {
+                    // strides 16 .. 128: the dims q + 16 k
+                    float x[16];
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) x[k] = ox[hh * D + q + 16 * k];
+#pragma unroll
+                    for (int st = 1; st < 16; st <<= 1)
+#pragma unroll
+                        for (int k = 0; k < 16; ++k)
+                            if ((k & st) == 0) {
+                                const float a0 = x[k], a1 = x[k + st];
+                                x[k] = a0 + a1;
+                                x[k + st] = a0 - a1;
+                            }
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) ox[hh * D + q + 16 * k] = x[k];
+                }
+                soft_sync();
+                if (hh < G) {
+                    // strides 1 .. 8: the dims 16 q + i
+                    float y[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) y[i] = ox[hh * D + 16 * q + i];
+#pragma unroll
+                    for (int st = 1; st < 16; st <<= 1)
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            if ((i & st) == 0) {
+                                const float a0 = y[i], a1 = y[i + st];
+                                y[i] = a0 + a1;
+                                y[i + st] = a0 - a1;
+                            }
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) y[i] *= 0.0625f;
+                    if (npieces == 1) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) write_out<D, G>(p, pc.b, hq0, hh * D + 16 * q + i, y[i]);
+                    } else {
+                        float4* dst = reinterpret_cast<float4*>(mine + 16 + hh * D + 16 * q);
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) dst[q4] = make_float4(y[4 * q4], y[4 * q4 + 1], y[4 * q4 + 2], y[4 * q4 + 3]);
+                    }
+                }
+            } else if (warp < NA) {
                 // warp g: lanes h and 8 + h hold the hi and lo rows of head h over the dims of group g
                 const float e_inv = (E == 1000) ? 0.0f : exp2i(-E);
                 const float Lh = lane < G ? sML[8 + lane] : 0.0f;
@@ -931,13 +1037,13 @@ cudaError_t decode_tc_read_error(unsigned* out, bool clear) {
 // Both kernels are launched with programmatic stream serialization: each may
 // start while its predecessor in the stream drains, and waits for it
 // (griddepcontrol.wait) before touching memory.
-template <int D, int G>
+template <int D, int G, bool VQ>
 static cudaError_t launch_tc(int grid, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p_in,
                              cudaStream_t st) {
     DecodeParams p = p_in;
     p.rec_by_seg = (long long)p.B * p.NH <= grid;
-    using X = TG<D>;
-    auto fn = decode_tc_kernel<D, G>;
+    using X = TG<D, VQ>;
+    auto fn = decode_tc_kernel<D, G, VQ>;
     static bool configured = false;   // per instantiation; the attribute is per device context
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, X::SMEM + 1024);
@@ -962,23 +1068,26 @@ static cudaError_t launch_tc(int grid, const CUtensorMap& tk, const CUtensorMap&
     return cudaLaunchKernelEx(&cfg, decode_tc_combine<D, G>, p);
 }
 
-template <int D>
+template <int D, bool VQ>
 static cudaError_t launch_tc_g(int G, int grid, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                                cudaStream_t st) {
     switch (G) {
-        case 1: return launch_tc<D, 1>(grid, tk, tv, p, st);
-        case 2: return launch_tc<D, 2>(grid, tk, tv, p, st);
-        case 4: return launch_tc<D, 4>(grid, tk, tv, p, st);
-        case 8: return launch_tc<D, 8>(grid, tk, tv, p, st);
+        case 1: return launch_tc<D, 1, VQ>(grid, tk, tv, p, st);
+        case 2: return launch_tc<D, 2, VQ>(grid, tk, tv, p, st);
+        case 4: return launch_tc<D, 4, VQ>(grid, tk, tv, p, st);
+        case 8: return launch_tc<D, 8, VQ>(grid, tk, tv, p, st);
     }
     return cudaErrorInvalidValue;
 }
 
-cudaError_t decode_tc_launch(int D, int G, int grid, const CUtensorMap& tk, const CUtensorMap& tv,
+// int8 K and V (v_q4 = false, head_dim 128 or 256) or int8 K with FWHT-rotated q4_0 V
+// (k8v4, v_q4 = true, head_dim 256)
+cudaError_t decode_tc_launch(int D, int G, int grid, bool v_q4, const CUtensorMap& tk, const CUtensorMap& tv,
                              const DecodeParams& p, cudaStream_t st) {
     grid = grid < kMaxGrid ? grid : kMaxGrid;
-    if (D == 256) return launch_tc_g<256>(G, grid, tk, tv, p, st);
-    if (D == 128) return launch_tc_g<128>(G, grid, tk, tv, p, st);
+    if (v_q4) return D == 256 ? launch_tc_g<256, true>(G, grid, tk, tv, p, st) : cudaErrorInvalidValue;
+    if (D == 256) return launch_tc_g<256, false>(G, grid, tk, tv, p, st);
+    if (D == 128) return launch_tc_g<128, false>(G, grid, tk, tv, p, st);
     return cudaErrorInvalidValue;
 }
 
