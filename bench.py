@@ -501,7 +501,8 @@ def run_decode_config(args, name):
     peak, peak_kind = peaks()
     value = step_bytes / (per_ms / 1e3) / 1e9
     achieved = step_bytes / (one_ms / 1e3) / 1e9
-    kernel = "decode_tc_kernel + decode_tc_combine" if fmt == "int8" else f"decode_kernel<{fmt}> (warp-level mma)"
+    kernel = ("decode_tc_kernel + decode_tc_combine" if fmt in ("int8", "k8v4")
+              else f"decode_kernel<{fmt}> (warp-level mma)")
     res = {"metric": f"decode-attn packed-KV HBM GB/s, {name}", "value": round(value, 1), "unit": "GB/s",
            "n_gpus": 1, "steps": args.steps * max(3, args.reps), "warmup": max(3, args.warmup),
            "ms_per_step": round(per_ms, 5), "us_per_step": round(per_ms * 1e3, 2), "higher_is_better": True,
