@@ -116,6 +116,7 @@ int device_setup(int* dev_out) {
         const Levels& L = levels();
         if ((e = append_upload_levels(L.l3, L.l4)) != cudaSuccess) return cuda_fail(e);
         if ((e = decode_upload_levels(L.l3, L.l4)) != cudaSuccess) return cuda_fail(e);
+        if ((e = decode_tc_upload_levels(L.l3, L.l4)) != cudaSuccess) return cuda_fail(e);
         int sms = 0;
         if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return cuda_fail(e);
         g_dev_sms[dev] = sms;
@@ -383,10 +384,7 @@ int kv_decode_attn(const qkv_cache_desc* cache, const void* q, const void* k_new
     p.slot_floats = L.slot_floats;
     p.k_new = (const uint16_t*)k_new;
     p.v_new = (const uint16_t*)v_new;
-    // int8 and k8v4: the tcgen05 kernel; ISO3 / ISO4: the warp-level mma kernel
-    const bool tc = cache->format == QKV_INT8 || cache->format == QKV_K8V4;
-    cudaError_t e = tc ? decode_tc_launch(D, L.G, grid, cache->format == QKV_K8V4, tk, tv, p, (cudaStream_t)stream)
-                       : decode_launch(cache->format, D, L.G, grid, tk, tv, p, (cudaStream_t)stream);
+    cudaError_t e = decode_tc_launch(D, L.G, grid, cache->format, tk, tv, p, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e);
     return QKV_OK;
 }

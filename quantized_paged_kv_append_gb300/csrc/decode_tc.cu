@@ -41,6 +41,9 @@
 namespace qkv {
 
 __device__ unsigned int g_err_dtc;
+// Lloyd-Max levels and decision midpoints: [0] ISO3 (8 levels), [1] ISO4 (16 levels)
+__constant__ float c_tc_levels[2][16];
+__constant__ float c_tc_mids[2][16];
 
 namespace {
 
@@ -52,24 +55,37 @@ constexpr int kWMma = kWProd + 1;           // MMA warp
 constexpr int kWProdV = kWMma + 1;          // producer warp of the V planes
 constexpr int kThr = (kWProdV + 1) * 32;    // 480 threads
 
-// VQ: V planes hold q4_0 codes of the FWHT-rotated vector (k8v4), else int8.
-template <int D, bool VQ>
+// Formats (the ABI's qkv_format): 0 int8 K and V; 1 k8v4 (int8 K, q4_0 codes of the
+// FWHT-rotated V); 2 / 3 ISO3 / ISO4 (K and V: Lloyd-Max codes of the rotated unit
+// vector per 128 values, one fp16 norm scale per block).
+template <int D, int FMT>
 struct TG {
-    static constexpr int NA = D / 64;             // 64-dim atoms = int8 K scale groups
-    static constexpr int VG = VQ ? D / 32 : D / 64;   // V scale groups
-    static constexpr int PG = VQ ? VG : 4;        // P' column groups of 16 (8 heads hi + lo); int8 pads to 4
-    static constexpr int PM = 16 * PG;            // M of the PV MMA: 64 (int8) or 128 (q4)
-    static constexpr int PAGE_B = D * kPage;      // staged K codes of one page: D / 128 boxes of 2048 B
-    static constexpr int VPAGE_B = (VQ ? D / 2 : D) * kPage;   // staged V codes of one page
-    static constexpr int VBOX = VPAGE_B / 2048;   // 128-byte TMA boxes per V page
-    static constexpr int SC_B = kPage * 2 * NA;   // staged K scales of one page
-    static constexpr int VSC_B = kPage * 2 * VG;  // staged V scales of one page
+    static constexpr bool VQ = FMT == 1, ISO = FMT >= 2;
+    static constexpr int ISO_RB = FMT == 2 ? 48 : 64;             // ISO code bytes per 128 values
+    static constexpr int ISO_SB = FMT == 2 ? 2 : 4;               // ISO scale bytes per 128 values
+    static constexpr int NA = D / 64;             // 64-dim atoms (Q tile, K' and V' tiles)
+    static constexpr int NKG = ISO ? D / 128 : D / 64;            // K scale groups = score accumulators
+    static constexpr int KROW = ISO ? ISO_RB * D / 128 : D;       // K code bytes of one row
+    static constexpr int KSROW = ISO ? ISO_SB * D / 128 : 2 * NA; // K scale bytes of one row
+    static constexpr int VROW = ISO ? KROW : (VQ ? D / 2 : D);
+    static constexpr int VSROW = ISO ? KSROW : (VQ ? 2 * (D / 32) : 2 * NA);
+    static constexpr int VG = ISO ? D / 128 : (VQ ? D / 32 : D / 64);   // V scale groups
+    static constexpr int PG = VQ ? VG : 4;        // P' column groups of 16 (8 heads hi + lo); padded to 4
+    static constexpr int PM = 16 * PG;            // M of the PV MMA: 64, or 128 for q4 V
+    static constexpr int PAGE_B = KROW * kPage;   // staged K codes of one page
+    static constexpr int VPAGE_B = VROW * kPage;  // staged V codes of one page
+    static constexpr int VBOX = VPAGE_B / 2048;   // 128-byte TMA boxes per V page (int8, q4)
+    static constexpr int SC_B = kPage * KSROW;    // staged K scales of one page
+    static constexpr int VSC_B = kPage * VSROW;   // staged V scales of one page
+    static constexpr int QT = ISO ? 2 : 1;        // query tiles: the rotated query needs fp16 hi + lo
+    static constexpr int LUT_N = FMT == 2 ? 64 : FMT == 3 ? 256 : 0;   // code pair -> fp16 level pair
     static constexpr int OFF_KST = 0;                               // [2][8][PAGE_B]
     static constexpr int OFF_VST = OFF_KST + 2 * kTP * PAGE_B;      // [2][8][VPAGE_B]
     static constexpr int OFF_VP = OFF_VST + 2 * kTP * VPAGE_B;      // V' [NA][128 rows][128 B]
     static constexpr int OFF_PP = OFF_VP + NA * 16384;              // P' [PM / 64][128 rows][128 B]
-    static constexpr int OFF_Q = OFF_PP + (PM / 64) * 16384;        // Q [NA][16 rows][128 B]
-    static constexpr int OFF_KSC = OFF_Q + NA * 2048;               // [2][8][SC_B]
+    static constexpr int OFF_Q = OFF_PP + (PM / 64) * 16384;        // Q [QT][NA][16 rows][128 B]
+    static constexpr int OFF_LUT = OFF_Q + QT * NA * 2048;          // per-lane level pairs [LUT_N][32]
+    static constexpr int OFF_KSC = OFF_LUT + LUT_N * 32 * 4;        // [2][8][SC_B]
     static constexpr int OFF_VSC = OFF_KSC + 2 * kTP * SC_B;        // [2][8][VSC_B]
     static constexpr int OFF_BIAS = OFF_VSC + 2 * kTP * VSC_B;      // float [NA][8]
     static constexpr int OFF_RED = OFF_BIAS + 256;                  // softmax-warp reductions
@@ -78,13 +94,15 @@ struct TG {
     static constexpr int OFF_MISC = OFF_BAR + 32 * 8;
     static constexpr int SMEM = OFF_MISC + 64;
     static constexpr int KCOL = 0;                     // K' columns: D / 2 (fp16 pairs)
-    static constexpr int SCOL = D / 2;                 // two score buffers of NA x 16 columns
-    static constexpr int OCOL = SCOL + 2 * NA * 16;    // O (M = 64 rows in lanes 32 (r / 16) + r % 16, N = D)
+    static constexpr int SCOL = D / 2;                 // two score buffers of NKG x 16 columns
+    static constexpr int OCOL = SCOL + 2 * NKG * 16;   // O (M = 64 rows in lanes 32 (r / 16) + r % 16, N = D)
     static constexpr int TCOLS = (OCOL + D) <= 256 ? 256 : 512;
     static_assert(OCOL + D <= 512, "TMEM budget");
     static_assert(SMEM + 1024 <= 232448 - 1024, "shared memory budget");
     static_assert(2 * kTP * SC_B <= 4096 && 2 * kTP * VSC_B <= 4096, "scale staging");
     static_assert(!VQ || D == 256, "q4 V is FWHT-256 rotated");
+    static_assert(OFF_VP % 1024 == 0 && OFF_PP % 1024 == 0 && OFF_Q % 1024 == 0, "UMMA operand alignment");
+    static_assert(PAGE_B % 16 == 0 && VPAGE_B % 16 == 0 && SC_B % 16 == 0 && VSC_B % 16 == 0, "bulk copies");
 };
 
 enum {
@@ -195,12 +213,13 @@ __device__ void write_out(const DecodeParams& p, int b, int hq0, int i, float v)
 
 }  // namespace
 
-template <int D, int G, bool VQ>
+template <int D, int G, int FMT>
 __global__ void __launch_bounds__(kThr, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const DecodeParams p) {
-    using X = TG<D, VQ>;
+    using X = TG<D, FMT>;
     constexpr int NA = X::NA;
+    constexpr bool VQ = X::VQ;
     extern __shared__ __align__(1024) uint8_t dsm_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -231,6 +250,24 @@ __global__ void __launch_bounds__(kThr, 1)
         mbar_init(&bars[B_PAT + 1], 1);
         fence_mbar_init();
         *s_abort = 0;
+    }
+    if constexpr (X::ISO) {
+        // per-lane copies (no bank conflicts) of the fp16 level pair of every pair of codes:
+        // ISO4 pair index = c0 | c1 << 4; ISO3 pair index = low 2 bits of c0, c1 | their high bits << 4
+        uint32_t* lutw = reinterpret_cast<uint32_t*>(sm + X::OFF_LUT);
+        constexpr int TT = FMT == 3 ? 1 : 0;
+        for (int e = tid; e < X::LUT_N * 32; e += kThr) {
+            const int idx = e >> 5;
+            int c0, c1;
+            if constexpr (TT == 1) {
+                c0 = idx & 15;
+                c1 = idx >> 4;
+            } else {
+                c0 = (idx & 3) | (((idx >> 4) & 1) << 2);
+                c1 = ((idx >> 2) & 3) | (((idx >> 5) & 1) << 2);
+            }
+            lutw[e] = f32x2_to_h2(c_tc_levels[TT][c0], c_tc_levels[TT][c1]);
+        }
     }
     if (warp == kWMma) tmem_alloc(tslot, X::TCOLS);
     tc_fence_before();
@@ -307,9 +344,12 @@ __global__ void __launch_bounds__(kThr, 1)
         const CUtensorMap* tm = kind ? &tmV : &tmK;
         const uint8_t* scl = kind ? p.vs : p.ks;
         const uint16_t* newsrc = kind ? p.v_new : p.k_new;
-        // per-plane geometry: V pages of q4 codes are half as wide and carry twice the scales
+        // per-plane geometry: V pages of q4 codes are half as wide and carry twice the scales;
+        // ISO pages (48 or 64 code bytes per 128 values) are staged row-major by one bulk copy
         const int pageb = kind ? X::VPAGE_B : X::PAGE_B, scb = kind ? X::VSC_B : X::SC_B;
-        const int nbox = kind ? X::VBOX : D / 128, scrow = kind ? 2 * X::VG : 2 * NA;
+        const int nbox = kind ? X::VBOX : D / 128, scrow = kind ? X::VSROW : X::KSROW;
+        const int rowb = pageb / kPage;   // code bytes of one row
+        const uint8_t* codes = kind ? p.vc : p.kc;
         uint32_t T = 0, pat_phase = 0;
         Piece pc;
         while (walker.next(p, pc)) {
@@ -347,8 +387,12 @@ __global__ void __launch_bounds__(kThr, 1)
                     // pages are read once per launch: evict-first in L2
                     const int row = (pid * p.Hkv + kvh) * kPage;
                     const uint64_t pol = l2_evict_first_policy();
-                    for (int bx = 0; bx < nbox; ++bx)
-                        tma_load_2d_hint(st + lane * pageb + bx * 2048, tm, full, bx * 128, row, pol);
+                    if constexpr (X::ISO) {
+                        bulk_load_hint(st + lane * pageb, codes + (size_t)row * rowb, pageb, full, pol);
+                    } else {
+                        for (int bx = 0; bx < nbox; ++bx)
+                            tma_load_2d_hint(st + lane * pageb + bx * 2048, tm, full, bx * 128, row, pol);
+                    }
                     bulk_load_hint(ss + lane * scb, scl + (size_t)row * scrow, scb, full, pol);
                 }
                 if (jp >= 0) {
@@ -358,27 +402,38 @@ __global__ void __launch_bounds__(kThr, 1)
                     uint64_t* pb = &bars[B_PAT + kind];
                     if (lane == 0) {
                         mbar_arrive_expect_tx(pb, pageb + scb);
-                        for (int bx = 0; bx < nbox; ++bx)
-                            tma_load_2d(st + jp * pageb + bx * 2048, tm, pb, bx * 128, row);
+                        if constexpr (X::ISO) {
+                            bulk_load(st + jp * pageb, codes + (size_t)row * rowb, pageb, pb);
+                        } else {
+                            for (int bx = 0; bx < nbox; ++bx)
+                                tma_load_2d(st + jp * pageb + bx * 2048, tm, pb, bx * 128, row);
+                        }
                         bulk_load(ss + jp * scb, scl + (size_t)row * scrow, scb, pb);
                     }
                     wait_or_flag(pb, pat_phase);
                     pat_phase ^= 1;
                     uint8_t* rowbuf = sm + X::OFF_ROW + kind * 512;
                     const uint16_t* src = newsrc + ((size_t)pc.b * p.Hkv + kvh) * D;
-                    if (VQ && kind) quantize_row<ENC_Q4, D>(src, rowbuf, rowbuf + 256, lane, nullptr, nullptr, nullptr);
-                    else quantize_row<ENC_INT8, D>(src, rowbuf, rowbuf + 256, lane, nullptr, nullptr, nullptr);
+                    if constexpr (X::ISO) {
+                        constexpr int TT = FMT == 3 ? 1 : 0;
+                        quantize_row<FMT == 3 ? ENC_ISO4 : ENC_ISO3, D>(src, rowbuf, rowbuf + 256, lane, p.quat,
+                                                                        c_tc_levels[TT], c_tc_mids[TT]);
+                    } else if (VQ && kind) {
+                        quantize_row<ENC_Q4, D>(src, rowbuf, rowbuf + 256, lane, nullptr, nullptr, nullptr);
+                    } else {
+                        quantize_row<ENC_INT8, D>(src, rowbuf, rowbuf + 256, lane, nullptr, nullptr, nullptr);
+                    }
                     __syncwarp();
                     const int rr = (pc.L - 1) % kPage;
                     const long long grow = (long long)row + rr;
-                    const int rowb = pageb / kPage;   // code bytes of one row
-                    uint8_t* gcode = const_cast<uint8_t*>(kind ? p.vc : p.kc) + grow * rowb;
+                    uint8_t* gcode = const_cast<uint8_t*>(codes) + grow * rowb;
                     uint8_t* gscale = const_cast<uint8_t*>(scl) + grow * scrow;
                     uint8_t* scode = st + jp * pageb;
                     if (lane < rowb / 16) {
                         const uint4 v = *reinterpret_cast<const uint4*>(rowbuf + 16 * lane);
                         *reinterpret_cast<uint4*>(gcode + 16 * lane) = v;
-                        *reinterpret_cast<uint4*>(scode + (lane >> 3) * 2048 + sw_off(rr, lane & 7)) = v;
+                        if constexpr (X::ISO) *reinterpret_cast<uint4*>(scode + rr * rowb + 16 * lane) = v;
+                        else *reinterpret_cast<uint4*>(scode + (lane >> 3) * 2048 + sw_off(rr, lane & 7)) = v;
                     }
                     if (lane < scrow / 2) {
                         const uint16_t v = reinterpret_cast<const uint16_t*>(rowbuf + 256)[lane];
@@ -443,13 +498,27 @@ __global__ void __launch_bounds__(kThr, 1)
                     if (ready && first) ready = mbar_test_wait(&bars[B_QRD], pieceq & 1);
                     if (ready) {
                         tc_fence_after();
-                        const uint32_t sd = tmem + X::SCOL + (Tq & 1) * NA * 16;
+                        const uint32_t sd = tmem + X::SCOL + (Tq & 1) * X::NKG * 16;
+                        if constexpr (X::ISO) {
+                            // per 128-dim block: 8 k-steps with the rotated query's fp16 hi part,
+                            // then 8 with its lo part, into the block's one accumulator
 #pragma unroll
-                        for (int g = 0; g < NA; ++g)
+                            for (int gk = 0; gk < X::NKG; ++gk)
 #pragma unroll
-                            for (int u = 0; u < 4; ++u)
-                                umma_f16_ta(sd + 16 * g, tk + 8 * (4 * g + u), qd0 + (uint64_t)((g * 2048 + 32 * u) >> 4), IDQK,
-                                            u > 0);
+                                for (int pass = 0; pass < 2; ++pass)
+#pragma unroll
+                                    for (int u = 0; u < 8; ++u)
+                                        umma_f16_ta(sd + 16 * gk, tk + 8 * (8 * gk + u),
+                                                    qd0 + (uint64_t)((pass * NA * 2048 + (2 * gk + (u >> 2)) * 2048 + 32 * (u & 3)) >> 4),
+                                                    IDQK, pass > 0 || u > 0);
+                        } else {
+#pragma unroll
+                            for (int g = 0; g < NA; ++g)
+#pragma unroll
+                                for (int u = 0; u < 4; ++u)
+                                    umma_f16_ta(sd + 16 * g, tk + 8 * (4 * g + u), qd0 + (uint64_t)((g * 2048 + 32 * u) >> 4),
+                                                IDQK, u > 0);
+                        }
                         umma_commit(&bars[B_QKD + (Tq & 1)]);
                         ++Tq;
                         if (pq.p0 + kTP * (tq + 1) < pq.p1) {
@@ -480,6 +549,31 @@ __global__ void __launch_bounds__(kThr, 1)
         const int r = 32 * sub + lane, jpage = r >> 4, rr = r & 15;
         constexpr int NCH = D / 32;   // 16-code chunks per thread (half of the head dimension)
         const uint32_t lb = (uint32_t)(32 * sub) << 16;
+        // ISO: the fp16 level pairs of 16 consecutive code pairs p0 .. p0 + 15 (dims 2 p, 2 p + 1)
+        // of one staged token row, through the per-lane pair table
+        const uint32_t* lut = reinterpret_cast<const uint32_t*>(sm + X::OFF_LUT) + lane;
+        auto iso16 = [&](const uint8_t* crow, int p0, uint32_t (&w)[16]) {
+            const uint8_t* cb = crow + (p0 >> 6) * X::ISO_RB;   // 64 pairs per 128-value block
+            const int q0 = p0 & 63;
+            if constexpr (FMT == 3) {
+                const uint4 x = *reinterpret_cast<const uint4*>(cb + q0);   // byte q = codes 2q (low), 2q + 1
+                const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int i = 0; i < 16; ++i) w[i] = lut[((xs[i >> 2] >> (8 * (i & 3))) & 0xffu) * 32];
+            } else {
+                // byte l: low 2 bits of codes 4l .. 4l + 3; nibble l of the high-bit bytes: their bit 2
+                const int l0 = q0 >> 1;
+                const uint2 lo = *reinterpret_cast<const uint2*>(cb + l0);
+                const uint32_t hn = *reinterpret_cast<const uint32_t*>(cb + 32 + (l0 >> 1));
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int l = i >> 1, u = i & 1;
+                    const uint32_t lob = ((l < 4 ? lo.x : lo.y) >> (8 * (l & 3))) & 0xffu;
+                    const uint32_t hnn = (hn >> (4 * l)) & 0xfu;
+                    w[i] = lut[(((lob >> (4 * u)) & 0xfu) | (((hnn >> (2 * u)) & 3u) << 4)) * 32];
+                }
+            }
+        };
         auto convert_v = [&](uint32_t Tc) {
             const int buf = Tc & 1;
             wait_or_flag(&bars[B_VF + buf], (Tc >> 1) & 1);
@@ -487,7 +581,20 @@ __global__ void __launch_bounds__(kThr, 1)
             if (Tc >= 1) wait_or_flag(&bars[B_PVD + ((Tc - 1) & 1)], ((Tc - 1) >> 1) & 1);
             const uint8_t* slot = sm + X::OFF_VST + (buf * kTP + jpage) * X::VPAGE_B;
             uint8_t* vp = sm + X::OFF_VP;
-            if constexpr (VQ) {
+            if constexpr (X::ISO) {
+                // level pairs in natural dim order: pair p -> V' atom p / 32, 16-byte chunk (p % 32) / 4
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c) {
+                    const int p0 = (D / 4) * hf + 16 * c;
+                    uint32_t w[16];
+                    iso16(slot + rr * X::VROW, p0, w);
+                    uint8_t* atom = vp + (p0 >> 5) * 16384;
+                    const int ch = (p0 & 31) >> 2;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        *reinterpret_cast<uint4*>(atom + sw_off(r, ch + k)) = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+                }
+            } else if constexpr (VQ) {
                 // q4_0 block b (32 dims: 16 code bytes, byte j = element j low, j + 16 high nibble)
                 // -> exact fp16 (q - 8). Pairs come out as (4w, 4w + 2), (4w + 1, 4w + 3): the same
                 // position <-> dimension permutation (perm4) as the int8 path.
@@ -544,7 +651,25 @@ __global__ void __launch_bounds__(kThr, 1)
                 wait_or_flag(&bars[B_KF + buf], (T >> 1) & 1);
                 if (T >= 1) wait_or_flag(&bars[B_QKD + ((T - 1) & 1)], ((T - 1) >> 1) & 1);
                 tc_fence_after();
-                {
+                if constexpr (X::ISO) {
+                    // level pairs of dims 2 p, 2 p + 1 into TMEM column p, one token per lane
+                    const uint8_t* crow = sm + X::OFF_KST + (buf * kTP + jpage) * X::PAGE_B + rr * X::KROW;
+#pragma unroll
+                    for (int c = 0; c < D / 128; ++c) {
+                        uint32_t w[32];
+                        const int p0 = (D / 4) * hf + 32 * c;
+                        uint32_t w0[16], w1[16];
+                        iso16(crow, p0, w0);
+                        iso16(crow, p0 + 16, w1);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            w[i] = w0[i];
+                            w[16 + i] = w1[i];
+                        }
+                        tmem_st32_nowait(tmem + lb + X::KCOL + p0, w);
+                    }
+                    tmem_wait_st();
+                } else {
                     const uint8_t* slot = sm + X::OFF_KST + (buf * kTP + jpage) * X::PAGE_B;
 #pragma unroll
                     for (int i0 = 0; i0 < NCH; i0 += 4) {
@@ -601,13 +726,40 @@ __global__ void __launch_bounds__(kThr, 1)
                         const uint4 raw = *reinterpret_cast<const uint4*>(qrow);
                         const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
                         float v[8];
+                        if constexpr (X::ISO) {
+                            // natural dim order; each 4-D group rotated: <q, conj(R) c> = <R q, c>
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int d = perm4(e);
-                            v[e] = bf16_bits_to_f32((rw[d >> 1] >> (16 * (d & 1))) & 0xffffu);
+                            for (int e = 0; e < 8; ++e) v[e] = bf16_bits_to_f32((rw[e >> 1] >> (16 * (e & 1))) & 0xffffu);
+                            const float q0 = p.quat[0], q1 = p.quat[1], q2 = p.quat[2], q3 = p.quat[3];
+#pragma unroll
+                            for (int g4 = 0; g4 < 2; ++g4) {
+                                const float a0 = v[4 * g4], b0 = v[4 * g4 + 1], c0 = v[4 * g4 + 2], d0 = v[4 * g4 + 3];
+                                v[4 * g4] = q0 * a0 - q1 * b0 - q2 * c0 - q3 * d0;
+                                v[4 * g4 + 1] = q0 * b0 + q1 * a0 + q2 * d0 - q3 * c0;
+                                v[4 * g4 + 2] = q0 * c0 - q1 * d0 + q2 * a0 + q3 * b0;
+                                v[4 * g4 + 3] = q0 * d0 + q1 * c0 - q2 * b0 + q3 * a0;
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const int d = perm4(e);
+                                v[e] = bf16_bits_to_f32((rw[d >> 1] >> (16 * (d & 1))) & 0xffffu);
+                            }
                         }
 #pragma unroll
                         for (int k = 0; k < 4; ++k) w[k] = f32x2_to_h2(v[2 * k], v[2 * k + 1]);
+                        if constexpr (X::ISO) {
+                            // the fp16 remainder of the rotated query: a second (lo) tile
+                            uint32_t wl[4];
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const float2 f = h2_to_f32x2(w[k]);
+                                wl[k] = f32x2_to_h2(v[2 * k] - f.x, v[2 * k + 1] - f.y);
+                            }
+                            *reinterpret_cast<uint4*>(qsm + (NA + a) * 2048 + sw_off(n, cc)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+                        }
+                    } else if constexpr (X::ISO) {
+                        *reinterpret_cast<uint4*>(qsm + (NA + a) * 2048 + sw_off(n, cc)) = make_uint4(0u, 0u, 0u, 0u);
                     }
                     *reinterpret_cast<uint4*>(qsm + a * 2048 + sw_off(n, cc)) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
@@ -622,7 +774,7 @@ __global__ void __launch_bounds__(kThr, 1)
                 }
 #pragma unroll
                 for (int off = 1; off < TPG; off <<= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-                if (h < G && (r & 15) % TPG == 0) bias_s[(s0 / 64) * 8 + h] = 1152.0f * part;
+                if (h < G && (r & 15) % TPG == 0) bias_s[(s0 / 64) * 8 + h] = X::ISO ? 0.0f : 1152.0f * part;
             }
             fence_proxy_async();
             soft_sync();
@@ -649,11 +801,13 @@ __global__ void __launch_bounds__(kThr, 1)
                 const bool valid = jpage < npg && pos < pc.L;
                 // ---- scores ----
                 wait_or_flag(&bars[B_KF + buf], ph);
-                float ks[NA];
+                float ks[X::NKG];
                 {
-                    const uint8_t* ksr = sm + X::OFF_KSC + (buf * kTP + jpage) * X::SC_B + (r & 15) * 2 * NA;
+                    // one fp16 scale per group (ISO4 rows carry 2 reserved bytes after each)
+                    const uint16_t* ksr = reinterpret_cast<const uint16_t*>(sm + X::OFF_KSC + (buf * kTP + jpage) * X::SC_B +
+                                                                            (r & 15) * X::KSROW);
 #pragma unroll
-                    for (int g = 0; g < NA; ++g) ks[g] = f16_bits_to_f32(reinterpret_cast<const uint16_t*>(ksr)[g]);
+                    for (int g = 0; g < X::NKG; ++g) ks[g] = f16_bits_to_f32(ksr[g * (X::ISO ? X::ISO_SB / 2 : 1)]);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[B_KE + buf]);
@@ -663,11 +817,11 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll
                 for (int h = 0; h < G; ++h) s[h] = 0.0f;
 #pragma unroll
-                for (int g = 0; g < NA; ++g) {
+                for (int g = 0; g < X::NKG; ++g) {
                     float v[16];
-                    tmem_ld16(tmem + lb + X::SCOL + buf * NA * 16 + 16 * g, v);
+                    tmem_ld16(tmem + lb + X::SCOL + buf * X::NKG * 16 + 16 * g, v);
 #pragma unroll
-                    for (int h = 0; h < G; ++h) s[h] += ks[g] * (v[h] - bias[g][h]);
+                    for (int h = 0; h < G; ++h) s[h] += X::ISO ? ks[g] * v[h] : ks[g] * (v[h] - bias[g][h]);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -679,10 +833,10 @@ __global__ void __launch_bounds__(kThr, 1)
                 float vsf[X::VG];
                 int e_row = 0;
                 {
-                    const uint8_t* vsr = sm + X::OFF_VSC + (buf * kTP + jpage) * X::VSC_B + (r & 15) * 2 * X::VG;
+                    const uint8_t* vsr = sm + X::OFF_VSC + (buf * kTP + jpage) * X::VSC_B + (r & 15) * X::VSROW;
 #pragma unroll
                     for (int g = 0; g < X::VG; ++g) {
-                        const uint32_t hb = reinterpret_cast<const uint16_t*>(vsr)[g];
+                        const uint32_t hb = reinterpret_cast<const uint16_t*>(vsr)[g * (X::ISO ? X::ISO_SB / 2 : 1)];
                         vsf[g] = f16_bits_to_f32(hb);
                         e_row = max(e_row, (int)((hb & 0x7fffu) >> 10));
                     }
@@ -740,15 +894,17 @@ __global__ void __launch_bounds__(kThr, 1)
                 // ---- P' (and the rare rescale of O) once PV of the previous tile is done ----
                 if (T >= 1) wait_or_flag(&bars[B_PVD + ((T - 1) & 1)], ((T - 1) >> 1) & 1);
                 tc_fence_after();
-                if (rescale && warp < NA) {
-                    // O rows 16 g + j (lane j of warp g: head j % 8, hi / lo) over the dims of group g
+                // O rows 16 g + j (lane j of warp g: head j % 8, hi / lo) over the dims of group g;
+                // ISO V groups are 128 dims, so warp g < VG owns 128 columns
+                constexpr int OW = X::ISO ? X::VG : NA, OCW = X::ISO ? 128 : 64;
+                if (rescale && warp < OW) {
                     float f = fac[0];
 #pragma unroll
                     for (int h = 1; h < 8; ++h) f = ((lane & 7) == h) ? fac[h] : f;
 #pragma unroll 1
-                    for (int c4 = 0; c4 < 4; ++c4) {
+                    for (int c4 = 0; c4 < OCW / 16; ++c4) {
                         float v[16];
-                        const uint32_t ta = tmem + lb + X::OCOL + 64 * warp + 16 * c4;
+                        const uint32_t ta = tmem + lb + X::OCOL + OCW * warp + 16 * c4;
                         tmem_ld16(ta, v);
 #pragma unroll
                         for (int j = 0; j < 16; ++j) v[j] *= f;
@@ -877,26 +1033,41 @@ __global__ void __launch_bounds__(kThr, 1)
                         for (int q4 = 0; q4 < 4; ++q4) dst[q4] = make_float4(y[4 * q4], y[4 * q4 + 1], y[4 * q4 + 2], y[4 * q4 + 3]);
                     }
                 }
-            } else if (warp < NA) {
+            } else if (warp < (X::ISO ? X::VG : NA)) {
                 // warp g: lanes h and 8 + h hold the hi and lo rows of head h over the dims of group g
+                // (64 dims in converter order for int8; 128 dims in natural order for ISO, where each
+                // 4-D group is rotated back: conj(q) (x) o)
+                constexpr int OCW = X::ISO ? 128 : 64;
                 const float e_inv = (E == 1000) ? 0.0f : exp2i(-E);
                 const float Lh = lane < G ? sML[8 + lane] : 0.0f;
                 const float inv = npieces == 1 ? (Lh > 0.0f ? e_inv / Lh : 0.0f) : e_inv;
 #pragma unroll 1
-                for (int c4 = 0; c4 < 4; ++c4) {
+                for (int c4 = 0; c4 < OCW / 16; ++c4) {
                     float v[16];
-                    tmem_ld16(tmem + lb + X::OCOL + 64 * warp + 16 * c4, v);
+                    tmem_ld16(tmem + lb + X::OCOL + OCW * warp + 16 * c4, v);
 #pragma unroll
                     for (int j = 0; j < 16; ++j) v[j] += __shfl_xor_sync(0xffffffffu, v[j], 8);
                     if (lane < G) {
-                        const int d0 = 64 * warp + 16 * c4;
-                        if (npieces == 1) {
+                        const int d0 = OCW * warp + 16 * c4;
+                        float o[16];
+                        if constexpr (X::ISO) {
+                            const float q0 = p.quat[0], q1 = p.quat[1], q2 = p.quat[2], q3 = p.quat[3];
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) write_out<D, G>(p, pc.b, hq0, lane * D + d0 + perm4(j), v[j] * inv);
+                            for (int k = 0; k < 4; ++k) {
+                                const float a0 = v[4 * k], b0 = v[4 * k + 1], c0 = v[4 * k + 2], dd = v[4 * k + 3];
+                                o[4 * k] = (q0 * a0 + q1 * b0 + q2 * c0 + q3 * dd) * inv;
+                                o[4 * k + 1] = (q0 * b0 - q1 * a0 - q2 * dd + q3 * c0) * inv;
+                                o[4 * k + 2] = (q0 * c0 + q1 * dd - q2 * a0 - q3 * b0) * inv;
+                                o[4 * k + 3] = (q0 * dd - q1 * c0 + q2 * b0 - q3 * a0) * inv;
+                            }
                         } else {
-                            float o[16];
 #pragma unroll
                             for (int j = 0; j < 16; ++j) o[perm4(j)] = v[j] * inv;
+                        }
+                        if (npieces == 1) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) write_out<D, G>(p, pc.b, hq0, lane * D + d0 + j, o[j]);
+                        } else {
                             float4* dst = reinterpret_cast<float4*>(mine + 16 + lane * D + d0);
 #pragma unroll
                             for (int q4 = 0; q4 < 4; ++q4) dst[q4] = make_float4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
@@ -1027,6 +1198,17 @@ __global__ void __launch_bounds__(kCombThr) decode_tc_combine(const DecodeParams
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
+cudaError_t decode_tc_upload_levels(const float* lv3, const float* lv4) {
+    float lv[2][16] = {}, mid[2][16] = {};
+    for (int j = 0; j < 8; ++j) lv[0][j] = lv3[j];
+    for (int j = 0; j < 16; ++j) lv[1][j] = lv4[j];
+    for (int j = 0; j < 7; ++j) mid[0][j] = (lv3[j] + lv3[j + 1]) * 0.5f;
+    for (int j = 0; j < 15; ++j) mid[1][j] = (lv4[j] + lv4[j + 1]) * 0.5f;
+    cudaError_t e = cudaMemcpyToSymbol(c_tc_levels, lv, sizeof(lv));
+    if (e != cudaSuccess) return e;
+    return cudaMemcpyToSymbol(c_tc_mids, mid, sizeof(mid));
+}
+
 cudaError_t decode_tc_read_error(unsigned* out, bool clear) {
     cudaError_t e = cudaMemcpyFromSymbol(out, g_err_dtc, sizeof(unsigned));
     if (e != cudaSuccess || !clear) return e;
@@ -1037,13 +1219,13 @@ cudaError_t decode_tc_read_error(unsigned* out, bool clear) {
 // Both kernels are launched with programmatic stream serialization: each may
 // start while its predecessor in the stream drains, and waits for it
 // (griddepcontrol.wait) before touching memory.
-template <int D, int G, bool VQ>
+template <int D, int G, int FMT>
 static cudaError_t launch_tc(int grid, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p_in,
                              cudaStream_t st) {
     DecodeParams p = p_in;
     p.rec_by_seg = (long long)p.B * p.NH <= grid;
-    using X = TG<D, VQ>;
-    auto fn = decode_tc_kernel<D, G, VQ>;
+    using X = TG<D, FMT>;
+    auto fn = decode_tc_kernel<D, G, FMT>;
     static bool configured = false;   // per instantiation; the attribute is per device context
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, X::SMEM + 1024);
@@ -1068,26 +1250,30 @@ static cudaError_t launch_tc(int grid, const CUtensorMap& tk, const CUtensorMap&
     return cudaLaunchKernelEx(&cfg, decode_tc_combine<D, G>, p);
 }
 
-template <int D, bool VQ>
+template <int D, int FMT>
 static cudaError_t launch_tc_g(int G, int grid, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                                cudaStream_t st) {
     switch (G) {
-        case 1: return launch_tc<D, 1, VQ>(grid, tk, tv, p, st);
-        case 2: return launch_tc<D, 2, VQ>(grid, tk, tv, p, st);
-        case 4: return launch_tc<D, 4, VQ>(grid, tk, tv, p, st);
-        case 8: return launch_tc<D, 8, VQ>(grid, tk, tv, p, st);
+        case 1: return launch_tc<D, 1, FMT>(grid, tk, tv, p, st);
+        case 2: return launch_tc<D, 2, FMT>(grid, tk, tv, p, st);
+        case 4: return launch_tc<D, 4, FMT>(grid, tk, tv, p, st);
+        case 8: return launch_tc<D, 8, FMT>(grid, tk, tv, p, st);
     }
     return cudaErrorInvalidValue;
 }
 
-// int8 K and V (v_q4 = false, head_dim 128 or 256) or int8 K with FWHT-rotated q4_0 V
-// (k8v4, v_q4 = true, head_dim 256)
-cudaError_t decode_tc_launch(int D, int G, int grid, bool v_q4, const CUtensorMap& tk, const CUtensorMap& tv,
+// fmt: 0 int8 (head_dim 128 or 256), 1 k8v4 (256), 2 ISO3 and 3 ISO4 (128 or 256); the
+// tensor maps are used for int8 and q4 code planes only
+cudaError_t decode_tc_launch(int D, int G, int grid, int fmt, const CUtensorMap& tk, const CUtensorMap& tv,
                              const DecodeParams& p, cudaStream_t st) {
     grid = grid < kMaxGrid ? grid : kMaxGrid;
-    if (v_q4) return D == 256 ? launch_tc_g<256, true>(G, grid, tk, tv, p, st) : cudaErrorInvalidValue;
-    if (D == 256) return launch_tc_g<256, false>(G, grid, tk, tv, p, st);
-    if (D == 128) return launch_tc_g<128, false>(G, grid, tk, tv, p, st);
+    if (fmt == 1) return D == 256 ? launch_tc_g<256, 1>(G, grid, tk, tv, p, st) : cudaErrorInvalidValue;
+    if (D != 128 && D != 256) return cudaErrorInvalidValue;
+    switch (fmt) {
+        case 0: return D == 256 ? launch_tc_g<256, 0>(G, grid, tk, tv, p, st) : launch_tc_g<128, 0>(G, grid, tk, tv, p, st);
+        case 2: return D == 256 ? launch_tc_g<256, 2>(G, grid, tk, tv, p, st) : launch_tc_g<128, 2>(G, grid, tk, tv, p, st);
+        case 3: return D == 256 ? launch_tc_g<256, 3>(G, grid, tk, tv, p, st) : launch_tc_g<128, 3>(G, grid, tk, tv, p, st);
+    }
     return cudaErrorInvalidValue;
 }
 

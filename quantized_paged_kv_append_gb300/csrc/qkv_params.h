@@ -81,8 +81,9 @@ cudaError_t decode_launch(int fmt, int D, int G, int grid, const CUtensorMap& tk
                           const DecodeParams& p, cudaStream_t st);
 int decode_heads_per_cta(int Gtot);
 // int8 K/V on tcgen05 tensor cores (decode_tc.cu): D 128 or 256, G in {1, 2, 4, 8}
-cudaError_t decode_tc_launch(int D, int G, int grid, bool v_q4, const CUtensorMap& tk, const CUtensorMap& tv,
+cudaError_t decode_tc_launch(int D, int G, int grid, int fmt, const CUtensorMap& tk, const CUtensorMap& tv,
                              const DecodeParams& p, cudaStream_t st);
+cudaError_t decode_tc_upload_levels(const float* lv3, const float* lv4);
 cudaError_t decode_tc_read_error(unsigned* out, bool clear);
 
 cudaError_t extend_read_error(unsigned* out, bool clear);
