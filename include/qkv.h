@@ -146,9 +146,10 @@ QKV_API int iso_kv_append(const qkv_cache_desc* cache, const void* k, const void
  * max_seq_len: host-side upper bound on seq_lens used to size the schedule.
  * out: [batch][num_q_heads][head_dim] in bf16 or fp32. scale is the softmax
  * scale (usually 1/sqrt(head_dim)). An empty sequence gives a zero row.
- * workspace: device scratch of at least kv_decode_workspace_size() bytes,
- * zero-filled before its first use; every call leaves its counter region
- * zeroed again. Calls sharing a workspace must not overlap in time.
+ * workspace: device scratch of at least kv_decode_workspace_size() bytes (the
+ * partial results of sequences split across thread blocks and the records of
+ * their merge), 16-byte aligned; no initialization needed: every call writes
+ * what it later reads. Calls sharing a workspace must not overlap in time.
  * batch <= 1024; num_q_heads / num_kv_heads in {1, 2, 4} or a multiple of 8.
  */
 QKV_API size_t kv_decode_workspace_size(const qkv_cache_desc* cache, int batch, int num_q_heads, int max_seq_len);
@@ -177,9 +178,12 @@ QKV_API int kv_decode_attn(const qkv_cache_desc* cache, const void* q, const voi
  * keys and values into it (fp16 planes, read by the attention kernel with TMA);
  * calls sharing a workspace must not overlap in time. A chunk longer than
  * max_q_len sets the position bit of qkv_device_error and is cut at max_q_len.
- * This build covers the int8 format, head_dim 128 or 256, num_q_heads /
- * num_kv_heads in {1, 2, 4} or a multiple of 8; other requests return
- * QKV_ERR_UNSUPPORTED.
+ * Formats: int8 (head_dim 128 or 256), k8v4 (256), ISO3 / ISO4 (128; head_dim
+ * 256 returns QKV_ERR_UNSUPPORTED), with num_q_heads / num_kv_heads in {1, 2,
+ * 4} or a multiple of 8. V is dequantized into the original domain first (k8v4
+ * rotated back by the FWHT-256, ISO by the conjugate quaternion), so the output
+ * needs no transform; ISO keys stay as their levels and the prefix tiles take
+ * the query rotated by the pool quaternion.
  */
 QKV_API size_t kv_extend_workspace_size(const qkv_cache_desc* cache, int batch, int max_q_len, int max_pages_per_seq);
 

@@ -152,7 +152,7 @@ def extend(cache: PagedKVCache, q, k_new, v_new, cu_seqlens, prefix_lens, page_t
         out = torch.empty((total, Hq, D), dtype=out_dtype or torch.bfloat16, device=q.device)
     odt = _lib.QKV_OUT_F32 if out.dtype == torch.float32 else _lib.QKV_OUT_BF16
     B, maxp = int(prefix_lens.numel()), int(page_table.shape[1])
-    if workspace is None and cache.desc.format == _lib.QKV_INT8 and B > 0 and max_q_len > 0:
+    if workspace is None and B > 0 and max_q_len > 0:
         workspace = extend_workspace(cache, B, int(max_q_len), maxp, device=q.device)
     ws_ptr, ws_bytes = (_ptr(workspace), workspace.numel() * workspace.element_size()) if workspace is not None else (None, 0)
     rc = _lib.lib().kv_extend_attn(C.byref(cache.desc), _ptr(q), _ptr(k_new), _ptr(v_new), Hq, _ptr(cu_seqlens),

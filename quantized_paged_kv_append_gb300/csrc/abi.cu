@@ -115,8 +115,8 @@ int device_setup(int* dev_out) {
     if (!g_dev_ready[dev]) {
         const Levels& L = levels();
         if ((e = append_upload_levels(L.l3, L.l4)) != cudaSuccess) return cuda_fail(e);
-        if ((e = decode_upload_levels(L.l3, L.l4)) != cudaSuccess) return cuda_fail(e);
         if ((e = decode_tc_upload_levels(L.l3, L.l4)) != cudaSuccess) return cuda_fail(e);
+        if ((e = extend_upload_levels(L.l3, L.l4)) != cudaSuccess) return cuda_fail(e);
         int sms = 0;
         if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return cuda_fail(e);
         g_dev_sms[dev] = sms;
@@ -213,7 +213,7 @@ struct DecodeLayout {
     int S;          // segments
     int Cmax;       // CTA upper bound
     int slot_floats;
-    size_t off_p2, off_seg, off_grp, off_rec, bytes;
+    size_t off_rec, bytes;
 };
 
 int decode_layout(const qkv_cache_desc* d, int batch, int num_q_heads, int sms, DecodeLayout* L) {
@@ -225,14 +225,11 @@ int decode_layout(const qkv_cache_desc* d, int batch, int num_q_heads, int sms, 
     L->S = batch * L->NH;
     L->Cmax = sms;
     L->slot_floats = 16 + 8 * d->head_dim;
+    // partial slots (m, l, O) of the pieces, then the merge records (per CTA or per segment)
     const size_t slots = (size_t)L->Cmax + L->S;
     auto al = [](size_t x) { return (x + 255) / 256 * 256; };
-    const size_t part = al(slots * L->slot_floats * sizeof(float));
-    L->off_p2 = part;
-    L->off_seg = 2 * part;
-    L->off_grp = L->off_seg + al((size_t)L->S * sizeof(int));
-    L->off_rec = L->off_grp + al(slots * sizeof(int));
-    L->bytes = L->off_rec + al((size_t)L->Cmax * 8 * sizeof(int));
+    L->off_rec = al(slots * L->slot_floats * sizeof(float));
+    L->bytes = L->off_rec + al((size_t)L->Cmax * 8 * sizeof(int));   // records: per segment only when S <= grid
     return QKV_OK;
 }
 
@@ -377,9 +374,6 @@ int kv_decode_attn(const qkv_cache_desc* cache, const void* q, const void* k_new
     for (int i = 0; i < 4; ++i) p.quat[i] = cache->quat[i];
     uint8_t* ws = (uint8_t*)workspace;
     p.part1 = (float*)ws;
-    p.part2 = (float*)(ws + L.off_p2);
-    p.seg_cnt = (int*)(ws + L.off_seg);
-    p.grp_cnt = (int*)(ws + L.off_grp);
     p.rec = (int*)(ws + L.off_rec);
     p.slot_floats = L.slot_floats;
     p.k_new = (const uint16_t*)k_new;
@@ -412,7 +406,8 @@ int kv_extend_attn(const qkv_cache_desc* cache, const void* q, const void* k_new
     if (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads) return QKV_ERR_GQA;
     const int Gtot = num_q_heads / cache->num_kv_heads;
     if (!(Gtot == 1 || Gtot == 2 || Gtot == 4 || Gtot % 8 == 0)) return QKV_ERR_GQA;
-    if (cache->format != QKV_INT8) return QKV_ERR_UNSUPPORTED;
+    // ISO prefixes take the rotated query as two extra fp16 tiles, which fit in shared memory at head_dim 128
+    if ((cache->format == QKV_ISO3 || cache->format == QKV_ISO4) && cache->head_dim != 128) return QKV_ERR_UNSUPPORTED;
     ExtendLayout XL;
     if ((rc = extend_layout(cache, batch, max_q_len, max_pages_per_seq, &XL))) return rc;
     if (!workspace || workspace_bytes < XL.bytes || ((uintptr_t)workspace & 255u)) return QKV_ERR_WORKSPACE;
@@ -452,6 +447,7 @@ int kv_extend_attn(const qkv_cache_desc* cache, const void* q, const void* k_new
     p.xk = (uint16_t*)ws;
     p.xv = (uint16_t*)(ws + XL.off_v);
     p.xs = (float*)(ws + XL.off_s);
+    for (int i = 0; i < 4; ++i) p.quat[i] = cache->quat[i];
     const int NH = cache->num_kv_heads * (Gtot / G);
     cudaError_t e = extend_launch(cache->format, D, G, max_q_len, NH, batch, tk, tv, p, (cudaStream_t)stream);
     if (e == cudaErrorInvalidValue) return QKV_ERR_UNSUPPORTED;
@@ -477,17 +473,15 @@ const char* qkv_strerror(int code) {
 int qkv_last_cuda_error(void) { return g_last_cuda; }
 
 int qkv_device_error(int clear) {
-    unsigned a = 0, b = 0;
+    unsigned a = 0;
     cudaError_t e = append_read_error(&a, clear != 0);
-    if (e != cudaSuccess) return cuda_fail(e);
-    e = decode_read_error(&b, clear != 0);
     if (e != cudaSuccess) return cuda_fail(e);
     unsigned x = 0, t = 0;
     e = extend_read_error(&x, clear != 0);
     if (e != cudaSuccess) return cuda_fail(e);
     e = decode_tc_read_error(&t, clear != 0);
     if (e != cudaSuccess) return cuda_fail(e);
-    return (int)(a | b | x | t);
+    return (int)(a | x | t);
 }
 
 }  // extern "C"

@@ -1,13 +1,15 @@
-// decode_tc.cu -- paged decode attention over an int8 KV cache on tcgen05 tensor
-// cores (TMEM accumulators), with the newest token's quantize-on-write fused in.
+// decode_tc.cu -- paged decode attention over a quantized KV cache (int8, k8v4,
+// ISO3, ISO4) on tcgen05 tensor cores (TMEM accumulators), with the newest
+// token's quantize-on-write fused in.
 //
 // Method (page title, section): "qwen35/q36: --kv - int8 K/V caches", "What it
 // does" (int8 K/V planes, one fp16 absmax/127 scale per 64 values, dequantized on
-// the fly by the attention kernels; the decode step quantizes the new token into
-// its page before attending); "Paged KV-cache decode with a split-K partial
-// softmax merge", "Algorithm" (each thread block attends a contiguous range of
-// one sequence's pages and the partial results are merged with the log-sum-exp
-// rule).
+// the fly by the partial-attention decode kernels); "--kv k8v4: hybrid KV cache",
+// "How" (q4_0 V in the FWHT-rotated domain, output rotated back); "feat(kvcache):
+// add ISO3/ISO4 KV-cache quantization", "What" (ISO blocks; decode quantizes the
+// new token into its page before attending). The partial results of a sequence
+// split across CTAs are merged with the log-sum-exp rule (the pages name the
+// partial kernels but do not print the rule; it is the standard one).
 //
 // GB300 design (one CTA of 15 warps per SM, persistent over an equal share of
 // the (sequence, KV-head group, page) units -- stream-K):
@@ -31,8 +33,9 @@
 //     sums), run a lazy online softmax (the frame max moves only when a score
 //     exceeds it by 2^8; all four warps agree on it once per tile), and write P'
 //     = p * V-scale * 2^E as fp16 hi + lo parts;
-//   * pieces that do not cover a whole sequence are merged through the caller's
-//     workspace by the last-arriving CTA (atomic ticket, two levels).
+//   * pieces that do not cover a whole sequence write a partial slot (m, l, O) to
+//     the caller's workspace; a second kernel (decode_tc_combine), launched with
+//     programmatic stream serialization, merges them.
 #include "qkv_device.cuh"
 #include "qkv_params.h"
 #include "quant_rows.cuh"
@@ -618,22 +621,23 @@ __global__ void __launch_bounds__(kThr, 1)
                     *reinterpret_cast<uint4*>(atom + sw_off(r, ch + 2)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
                     *reinterpret_cast<uint4*>(atom + sw_off(r, ch + 3)) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
                 }
-            } else
+            } else {
 #pragma unroll
-            for (int i = 0; i < NCH; ++i) {
-                const int gc = hf * NCH + i;
-                const uint4 x = *reinterpret_cast<const uint4*>(slot + (gc >> 3) * 2048 + sw_off(rr, gc & 7));
-                const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
-                uint32_t w[8];
+                for (int i = 0; i < NCH; ++i) {
+                    const int gc = hf * NCH + i;
+                    const uint4 x = *reinterpret_cast<const uint4*>(slot + (gc >> 3) * 2048 + sw_off(rr, gc & 7));
+                    const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+                    uint32_t w[8];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    w[2 * k] = hsub2_u32(lop3_and_xor(xs[k], 0x00ff00ffu, 0x64806480u), 0x64806480u);
-                    w[2 * k + 1] = hsub2_u32(lop3_and_xor(xs[k] >> 8, 0x00ff00ffu, 0x64806480u), 0x64806480u);
+                    for (int k = 0; k < 4; ++k) {
+                        w[2 * k] = hsub2_u32(lop3_and_xor(xs[k], 0x00ff00ffu, 0x64806480u), 0x64806480u);
+                        w[2 * k + 1] = hsub2_u32(lop3_and_xor(xs[k] >> 8, 0x00ff00ffu, 0x64806480u), 0x64806480u);
+                    }
+                    uint8_t* atom = vp + (gc >> 2) * 16384;
+                    const int ch = 2 * (gc & 3);
+                    *reinterpret_cast<uint4*>(atom + sw_off(r, ch)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *reinterpret_cast<uint4*>(atom + sw_off(r, ch + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
                 }
-                uint8_t* atom = vp + (gc >> 2) * 16384;
-                const int ch = 2 * (gc & 3);
-                *reinterpret_cast<uint4*>(atom + sw_off(r, ch)) = make_uint4(w[0], w[1], w[2], w[3]);
-                *reinterpret_cast<uint4*>(atom + sw_off(r, ch + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
             }
             fence_proxy_async();
             __syncwarp();
@@ -1208,6 +1212,9 @@ cudaError_t decode_tc_upload_levels(const float* lv3, const float* lv4) {
     if (e != cudaSuccess) return e;
     return cudaMemcpyToSymbol(c_tc_mids, mid, sizeof(mid));
 }
+
+int decode_heads_per_cta(int Gtot) { return Gtot >= 8 ? 8 : Gtot; }
+int decode_max_batch() { return 1024; }
 
 cudaError_t decode_tc_read_error(unsigned* out, bool clear) {
     cudaError_t e = cudaMemcpyFromSymbol(out, g_err_dtc, sizeof(unsigned));

@@ -48,8 +48,9 @@ constexpr int kXSoft = 128 * kXSplit;      // softmax warps: row r = lane + 32 (
 constexpr int kXThreads = kXSoft + 96;     // + 2 producer warps (K, V) + 1 MMA warp
 constexpr int kXProd = kXSoft / 32, kXMma = kXProd + 2;
 
-// shared-memory map (bytes from a 1 KB aligned base)
-template <int D>
+// shared-memory map (bytes from a 1 KB aligned base). ISO adds the rotated query of
+// the prefix tiles as two fp16 tiles (hi, and the fp16 remainder lo) after the rest.
+template <int D, bool ISO = false>
 struct XGeo {
     static constexpr int NA = D / 64;                    // 64-dim atoms (= K scale groups)
     static constexpr int OFF_Q = 0;                      // NA atoms x 128 rows x 128 B
@@ -64,7 +65,8 @@ struct XGeo {
     static constexpr int OFF_RED = OFF_KS + 2 * KS_BYTES;   // [2 tiles][kXSplit parts][128 rows] row-max / row-sum exchange
     static constexpr int OFF_BAR = OFF_RED + 2 * kXSplit * 128 * 4;
     static constexpr int OFF_TMEM = OFF_BAR + 16 * 8;
-    static constexpr int SMEM = OFF_TMEM + 16;
+    static constexpr int OFF_QR = (OFF_TMEM + 16 + 1023) / 1024 * 1024;   // ISO: [hi, lo] x Q_BYTES
+    static constexpr int SMEM = ISO ? OFF_QR + 2 * Q_BYTES : OFF_TMEM + 16;
     static constexpr int S_COLS = NA * 64;               // TMEM columns of the group scores
     static constexpr int TMEM_COLS = 512;
     static_assert(S_COLS + D <= TMEM_COLS, "TMEM budget");
@@ -94,10 +96,34 @@ __device__ __forceinline__ uint32_t bf16x2_to_h2(uint32_t w) {
 // Positions past the prefix or the chunk are zero (their scores are masked and
 // their P is 0, so V must be finite). Thread (i, qd): position i, dims
 // [qd D/4, (qd + 1) D/4). V^T goes through a transposed shared tile.
+// What the prefix rows hold, per format (FMT = qkv_format):
+//   0 int8 : K' = the exact code c, key scale = the fp16 group scale;
+//            V = fp16(c * scale), one rounding.
+//   1 k8v4 : K as int8. V: the q4_0 values (q - 8) * d of the FWHT-rotated row,
+//            rotated back with the same transform (H / 16 is its own inverse) in
+//            fp32 across the four threads of the row, then rounded to fp16 once.
+//   2, 3 ISO3 / ISO4 (head_dim 128): K' = the Lloyd-Max levels c (exact in
+//            fp16) with the block's fp16 norm as the key scale of both its
+//            64-dim groups; the attention kernel rotates the query for these
+//            tiles. V: each 4-D group rotated back, u = conj(q) (x) c in fp32,
+//            then fp16(norm * u), one rounding.
+// V reaches the attention kernel in the original domain, so the output needs
+// no inverse transform.
 // ---------------------------------------------------------------------------
-template <int D>
+__constant__ float c_x_levels[2][16];   // [0] ISO3 (8 levels), [1] ISO4 (16 levels)
+
+// conj(q) (x) c for one 4-D group (q = (w, x, y, z) unit quaternion)
+__device__ __forceinline__ void quat_conj_mul(const float* q, float a, float b, float c, float d, float (&u)[4]) {
+    u[0] = q[0] * a + q[1] * b + q[2] * c + q[3] * d;
+    u[1] = q[0] * b - q[1] * a - q[2] * d + q[3] * c;
+    u[2] = q[0] * c + q[1] * d - q[2] * a - q[3] * b;
+    u[3] = q[0] * d - q[1] * c + q[2] * b - q[3] * a;
+}
+
+template <int D, int FMT>
 __global__ void __launch_bounds__(256) extend_prep_kernel(const ExtendParams p) {
     constexpr int NA = D / 64, QD = D / 4;
+    constexpr bool ISO = FMT >= 2;
     __shared__ __align__(16) uint16_t vt[D][kXT + 8];
     const int b = blockIdx.z, kvh = blockIdx.y, t = blockIdx.x;
     const int cu0 = p.cu[b], T = max(0, p.cu[b + 1] - cu0);
@@ -110,6 +136,11 @@ __global__ void __launch_bounds__(256) extend_prep_kernel(const ExtendParams p) 
     const size_t krow = ((size_t)b * p.Hkv + kvh) * p.Lmax + (size_t)kXT * t + i;
     uint32_t kw[QD / 2], vw[QD / 2];
     float ksv[NA];
+    // k8v4: the thread's 64 rotated V values; zero for rows past the prefix, so that the
+    // cross-thread butterflies below run on every lane of the warp
+    float xr[FMT == 1 ? 64 : 1];
+#pragma unroll
+    for (int e = 0; e < (FMT == 1 ? 64 : 1); ++e) xr[e] = 0.0f;
 #pragma unroll
     for (int g = 0; g < NA; ++g) ksv[g] = 0.0f;
 #pragma unroll
@@ -126,32 +157,133 @@ __global__ void __launch_bounds__(256) extend_prep_kernel(const ExtendParams p) 
         }
         if (page >= 0) {
             const long long row = ((long long)page * p.Hkv + kvh) * kPage + (pos & 15);
-            const uint8_t* ksrc = p.kc + row * D + QD * qd;
-            const uint8_t* vsrc = p.vc + row * D + QD * qd;
-            const uint32_t vsb = reinterpret_cast<const uint16_t*>(p.vs + row * NA * 2)[(QD * qd) / 64];
-            const uint32_t sv2 = vsb | (vsb << 16);
+            if constexpr (!ISO) {
+                // int8 K: exact codes, fp32 group scales
+                const uint8_t* ksrc = p.kc + row * D + QD * qd;
 #pragma unroll
-            for (int c = 0; c < QD / 16; ++c) {
-                const uint4 kx = *reinterpret_cast<const uint4*>(ksrc + 16 * c);
-                const uint4 vx = *reinterpret_cast<const uint4*>(vsrc + 16 * c);
-                const uint32_t ks4[4] = {kx.x, kx.y, kx.z, kx.w}, vs4[4] = {vx.x, vx.y, vx.z, vx.w};
+                for (int c = 0; c < QD / 16; ++c) {
+                    const uint4 kx = *reinterpret_cast<const uint4*>(ksrc + 16 * c);
+                    const uint32_t ks4[4] = {kx.x, kx.y, kx.z, kx.w};
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const uint32_t x = ks4[u] ^ 0x80808080u;   // 1152 + code, then the exact code
-                    kw[8 * c + 2 * u] = hsub2_u32(prmt(x, 0x64646464u, 0x4140u), 0x64806480u);
-                    kw[8 * c + 2 * u + 1] = hsub2_u32(prmt(x, 0x64646464u, 0x4342u), 0x64806480u);
-                    const uint32_t y = vs4[u] ^ 0x80808080u;
-                    const uint32_t c01 = hsub2_u32(prmt(y, 0x64646464u, 0x4140u), 0x64806480u);
-                    const uint32_t c23 = hsub2_u32(prmt(y, 0x64646464u, 0x4342u), 0x64806480u);
-                    vw[8 * c + 2 * u] = hfma2_u32(c01, sv2, 0u);       // fp16(code * scale), rounded once
-                    vw[8 * c + 2 * u + 1] = hfma2_u32(c23, sv2, 0u);
+                    for (int u = 0; u < 4; ++u) {
+                        const uint32_t x = ks4[u] ^ 0x80808080u;   // 1152 + code, then the exact code
+                        kw[8 * c + 2 * u] = hsub2_u32(prmt(x, 0x64646464u, 0x4140u), 0x64806480u);
+                        kw[8 * c + 2 * u + 1] = hsub2_u32(prmt(x, 0x64646464u, 0x4342u), 0x64806480u);
+                    }
+                }
+                if (qd == 0) {
+#pragma unroll
+                    for (int g = 0; g < NA; ++g)
+                        ksv[g] = f16_bits_to_f32(reinterpret_cast<const uint16_t*>(p.ks + row * NA * 2)[g]) * p.scale_log2;
                 }
             }
-            if (qd == 0) {
+            if constexpr (FMT == 0) {
+                const uint8_t* vsrc = p.vc + row * D + QD * qd;
+                const uint32_t vsb = reinterpret_cast<const uint16_t*>(p.vs + row * NA * 2)[(QD * qd) / 64];
+                const uint32_t sv2 = vsb | (vsb << 16);
 #pragma unroll
-                for (int g = 0; g < NA; ++g)
-                    ksv[g] = f16_bits_to_f32(reinterpret_cast<const uint16_t*>(p.ks + row * NA * 2)[g]) * p.scale_log2;
+                for (int c = 0; c < QD / 16; ++c) {
+                    const uint4 vx = *reinterpret_cast<const uint4*>(vsrc + 16 * c);
+                    const uint32_t vs4[4] = {vx.x, vx.y, vx.z, vx.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const uint32_t y = vs4[u] ^ 0x80808080u;
+                        const uint32_t c01 = hsub2_u32(prmt(y, 0x64646464u, 0x4140u), 0x64806480u);
+                        const uint32_t c23 = hsub2_u32(prmt(y, 0x64646464u, 0x4342u), 0x64806480u);
+                        vw[8 * c + 2 * u] = hfma2_u32(c01, sv2, 0u);       // fp16(code * scale), rounded once
+                        vw[8 * c + 2 * u + 1] = hfma2_u32(c23, sv2, 0u);
+                    }
+                }
+            } else if constexpr (FMT == 1) {
+                // q4_0 V, blocks 2 qd and 2 qd + 1 of the rotated row (16 code bytes + one fp16 d each)
+                static_assert(D == 256, "k8v4 V is FWHT-256 rotated");
+                float (&x)[64] = xr;
+                const uint8_t* vsrc = p.vc + row * (D / 2) + 32 * qd;
+                const uint16_t* vsc = reinterpret_cast<const uint16_t*>(p.vs + row * (D / 16));
+#pragma unroll
+                for (int lb = 0; lb < 2; ++lb) {
+                    const float d16 = f16_bits_to_f32(vsc[2 * qd + lb]);
+                    const uint4 v4 = *reinterpret_cast<const uint4*>(vsrc + 16 * lb);
+                    const uint32_t w4[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const uint32_t byte = (w4[j >> 2] >> (8 * (j & 3))) & 0xffu;
+                        x[32 * lb + j] = (float)((int)(byte & 15u) - 8) * d16;
+                        x[32 * lb + j + 16] = (float)((int)(byte >> 4) - 8) * d16;
+                    }
+                }
+                // rotated back after this branch, where every lane of the warp takes part
+            } else {
+                // ISO3 / ISO4: dims [QD qd, QD qd + QD) lie in block nb at offset j0
+                constexpr int RB = FMT == 2 ? 48 : 64, SB = FMT == 2 ? 2 : 4;
+                constexpr int TT = FMT == 3 ? 1 : 0;
+                const int nb = (QD * qd) / 128, j0 = (QD * qd) % 128;
+                const float qv[4] = {p.quat[0], p.quat[1], p.quat[2], p.quat[3]};
+#pragma unroll
+                for (int s2 = 0; s2 < 2; ++s2) {
+                    const uint8_t* cb = (s2 ? p.vc : p.kc) + row * (RB * D / 128) + RB * nb;
+                    const uint16_t* sc = reinterpret_cast<const uint16_t*>((s2 ? p.vs : p.ks) + row * (SB * D / 128));
+                    const float nrm = f16_bits_to_f32(sc[nb * (SB / 2)]);
+                    if (s2 == 0 && qd == 0) {
+#pragma unroll
+                        for (int g = 0; g < NA; ++g) ksv[g] = f16_bits_to_f32(sc[(g >> 1) * (SB / 2)]) * p.scale_log2;
+                    }
+#pragma unroll
+                    for (int g4 = 0; g4 < QD / 4; ++g4) {
+                        int code[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int j = j0 + 4 * g4 + e;
+                            if constexpr (FMT == 3) {
+                                code[e] = (cb[j >> 1] >> (4 * (j & 1))) & 15;
+                            } else {
+                                code[e] = ((cb[j >> 2] >> (2 * (j & 3))) & 3) | (((cb[32 + (j >> 3)] >> (j & 7)) & 1) << 2);
+                            }
+                        }
+                        const float c0 = c_x_levels[TT][code[0]], c1 = c_x_levels[TT][code[1]];
+                        const float c2 = c_x_levels[TT][code[2]], c3 = c_x_levels[TT][code[3]];
+                        if (s2 == 0) {
+                            // K': the levels themselves (exact in fp16); the attention kernel rotates
+                            // the query instead
+                            kw[2 * g4] = f32x2_to_h2(c0, c1);
+                            kw[2 * g4 + 1] = f32x2_to_h2(c2, c3);
+                        } else {
+                            float u[4];
+                            quat_conj_mul(qv, c0, c1, c2, c3, u);
+                            vw[2 * g4] = f32x2_to_h2(nrm * u[0], nrm * u[1]);
+                            vw[2 * g4 + 1] = f32x2_to_h2(nrm * u[2], nrm * u[3]);
+                        }
+                    }
+                }
             }
+        }
+        if constexpr (FMT == 1) {
+            // k8v4 V back to the original domain: the FWHT-256 (x 1/16) is its own inverse.
+            // Butterflies at distances 1 .. 32 inside the thread's 64 values, then 64 and 128
+            // across the four threads of the row (lanes qd ^ 1, qd ^ 2). `prefix` is uniform
+            // over the block, so every lane of the warp reaches the shuffles; rows past the
+            // prefix carry zeros and stay zero.
+#pragma unroll
+            for (int h = 1; h < 64; h <<= 1) {
+#pragma unroll
+                for (int e = 0; e < 64; ++e) {
+                    if (e & h) continue;
+                    const float a = xr[e], c = xr[e + h];
+                    xr[e] = a + c;
+                    xr[e + h] = a - c;
+                }
+            }
+#pragma unroll
+            for (int m = 1; m <= 2; m <<= 1) {
+                const bool upper = (qd & m) != 0;
+#pragma unroll
+                for (int e = 0; e < 64; ++e) {
+                    const float o = __shfl_xor_sync(0xffffffffu, xr[e], m);
+                    xr[e] = upper ? o - xr[e] : xr[e] + o;
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 32; ++k) vw[k] = f32x2_to_h2(xr[2 * k] * 0.0625f, xr[2 * k + 1] * 0.0625f);
         }
     } else {
         const int n = kXT * (t - NTP) + i;
@@ -196,10 +328,15 @@ __global__ void __launch_bounds__(256) extend_prep_kernel(const ExtendParams p) 
     }
 }
 
-template <int D, int G>
+// ISO: the prefix keys are the raw Lloyd-Max levels (exact fp16) with the block norm as
+// key scale, and the prefix tiles take the query rotated per 4-D group (<q_h, conj(R) c>
+// = <R q_h, c>), held as fp16 hi + lo so that Q K^T sees the fp32 rotated query; the
+// bf16 new tokens take the plain query.
+template <int D, int G, bool ISO>
 __global__ void __launch_bounds__(kXThreads, 1)
     extend_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const ExtendParams p) {
-    using X = XGeo<D>;
+    using X = XGeo<D, ISO>;
+    static_assert(!ISO || D == 128, "the rotated query tiles fit in shared memory at head_dim 128");
     constexpr int NA = X::NA;
     constexpr int TPT = 128 / G;   // tokens per tile
     extern __shared__ __align__(1024) uint8_t xsmem_raw[];
@@ -298,12 +435,25 @@ __global__ void __launch_bounds__(kXThreads, 1)
                 if (j >= 1) wait(B_SFREE, (j - 1) & 1);
                 tc_fence_after();
                 const uint32_t ks = smem_addr(sm + X::OFF_K + buf * X::K_BYTES);
+                if (ISO && j < NTP) {
+                    // prefix tile: rotated query, hi then lo into the same accumulator
+                    const uint32_t qr = smem_addr(sm + X::OFF_QR);
 #pragma unroll
-                for (int g = 0; g < NA; ++g)
+                    for (int g = 0; g < NA; ++g)
 #pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        umma_f16(tmem_S + 64 * g, sw128_desc(qs + g * 16384 + 32 * u), sw128_desc(ks + g * 8192 + 32 * u),
-                                 IDQK, u > 0);
+                        for (int hl = 0; hl < 2; ++hl)
+#pragma unroll
+                            for (int u = 0; u < 4; ++u)
+                                umma_f16(tmem_S + 64 * g, sw128_desc(qr + hl * X::Q_BYTES + g * 16384 + 32 * u),
+                                         sw128_desc(ks + g * 8192 + 32 * u), IDQK, (hl | u) > 0);
+                } else {
+#pragma unroll
+                    for (int g = 0; g < NA; ++g)
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            umma_f16(tmem_S + 64 * g, sw128_desc(qs + g * 16384 + 32 * u),
+                                     sw128_desc(ks + g * 8192 + 32 * u), IDQK, u > 0);
+                }
                 umma_commit(&bars[B_SFULL]);
             };
             wait(B_Q, 0);
@@ -340,11 +490,43 @@ __global__ void __launch_bounds__(kXThreads, 1)
 #pragma unroll 4
             for (int c = part * (D / 8 / kXSplit); c < (part + 1) * (D / 8 / kXSplit); ++c) {
                 uint4 o = make_uint4(0, 0, 0, 0);
+                uint4 ohi = o, olo = o;
                 if (rvalid) {
                     const uint4 w = *reinterpret_cast<const uint4*>(qrow + 8 * c);
                     o = make_uint4(bf16x2_to_h2(w.x), bf16x2_to_h2(w.y), bf16x2_to_h2(w.z), bf16x2_to_h2(w.w));
+                    if constexpr (ISO) {
+                        // R q_h per 4-D group (left Hamilton product by the pool quaternion) in fp32,
+                        // then hi = fp16(v), lo = fp16(v - hi)
+                        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+                        float v[8], y[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(e & 1 ? ww[e >> 1] & 0xffff0000u : ww[e >> 1] << 16);
+                        const float q0 = p.quat[0], q1 = p.quat[1], q2 = p.quat[2], q3 = p.quat[3];
+#pragma unroll
+                        for (int g4 = 0; g4 < 2; ++g4) {
+                            const float a = v[4 * g4], b = v[4 * g4 + 1], cc = v[4 * g4 + 2], d = v[4 * g4 + 3];
+                            y[4 * g4] = q0 * a - q1 * b - q2 * cc - q3 * d;
+                            y[4 * g4 + 1] = q0 * b + q1 * a + q2 * d - q3 * cc;
+                            y[4 * g4 + 2] = q0 * cc - q1 * d + q2 * a + q3 * b;
+                            y[4 * g4 + 3] = q0 * d + q1 * cc - q2 * b + q3 * a;
+                        }
+                        uint32_t hi[4], lo[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            hi[k] = f32x2_to_h2(y[2 * k], y[2 * k + 1]);
+                            const float2 f = h2_to_f32x2(hi[k]);
+                            lo[k] = f32x2_to_h2(y[2 * k] - f.x, y[2 * k + 1] - f.y);
+                        }
+                        ohi = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                        olo = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    }
                 }
                 *reinterpret_cast<uint4*>(qs + (c >> 3) * 16384 + sw_off(r, c & 7)) = o;
+                if constexpr (ISO) {
+                    uint8_t* qr = sm + X::OFF_QR;
+                    *reinterpret_cast<uint4*>(qr + (c >> 3) * 16384 + sw_off(r, c & 7)) = ohi;
+                    *reinterpret_cast<uint4*>(qr + X::Q_BYTES + (c >> 3) * 16384 + sw_off(r, c & 7)) = olo;
+                }
             }
             fence_proxy_async();
             mbar_arrive(&bars[B_Q]);
@@ -505,11 +687,11 @@ cudaError_t extend_read_error(unsigned* out, bool clear) {
     return cudaMemcpyToSymbol(g_err_extend, &z, sizeof(unsigned));
 }
 
-template <int D, int G>
+template <int D, int G, bool ISO>
 static cudaError_t xlaunch(dim3 grid, const CUtensorMap& tk, const CUtensorMap& tv, const ExtendParams& p,
                            cudaStream_t st) {
-    auto fn = extend_kernel<D, G>;
-    constexpr int smem = XGeo<D>::SMEM + 1024;
+    auto fn = extend_kernel<D, G, ISO>;
+    constexpr int smem = XGeo<D, ISO>::SMEM + 1024;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -520,32 +702,54 @@ static cudaError_t xlaunch(dim3 grid, const CUtensorMap& tk, const CUtensorMap& 
     return cudaGetLastError();
 }
 
-// int8 pools; returns cudaErrorInvalidValue for shapes this kernel does not cover.
-// Two launches: the prep kernel (one block per 64-key tile of every sequence and
-// KV head) writes the workspace planes, the attention kernel reads them.
+cudaError_t extend_upload_levels(const float* lv3, const float* lv4) {
+    float lv[2][16] = {};
+    for (int j = 0; j < 8; ++j) lv[0][j] = lv3[j];
+    for (int j = 0; j < 16; ++j) lv[1][j] = lv4[j];
+    return cudaMemcpyToSymbol(c_x_levels, lv, sizeof(lv));
+}
+
+// Every format (qkv_format) at D 128 or 256 (k8v4: 256); returns cudaErrorInvalidValue
+// for shapes this kernel does not cover. Two launches: the prep kernel (one block per
+// 64-key tile of every sequence and KV head) writes the workspace planes, the attention
+// kernel reads them.
 cudaError_t extend_launch(int fmt, int D, int G, int max_q_len, int NH, int B, const CUtensorMap& tk,
                           const CUtensorMap& tv, const ExtendParams& p, cudaStream_t st) {
-    if (fmt != 0 || (D != 128 && D != 256) || !(G == 1 || G == 2 || G == 4 || G == 8)) return cudaErrorInvalidValue;
+    if (fmt < 0 || fmt > 3 || (D != 128 && D != 256) || (fmt == 1 && D != 256) || (fmt >= 2 && D != 128) ||
+        !(G == 1 || G == 2 || G == 4 || G == 8))
+        return cudaErrorInvalidValue;
     const dim3 pgrid((unsigned)(p.Lmax / kXT), (unsigned)p.Hkv, (unsigned)B);
-    if (D == 256) extend_prep_kernel<256><<<pgrid, 256, 0, st>>>(p);
-    else extend_prep_kernel<128><<<pgrid, 256, 0, st>>>(p);
+    switch (fmt * 1000 + D) {
+        case 256: extend_prep_kernel<256, 0><<<pgrid, 256, 0, st>>>(p); break;
+        case 128: extend_prep_kernel<128, 0><<<pgrid, 256, 0, st>>>(p); break;
+        case 1256: extend_prep_kernel<256, 1><<<pgrid, 256, 0, st>>>(p); break;
+        case 2128: extend_prep_kernel<128, 2><<<pgrid, 256, 0, st>>>(p); break;
+        case 3128: extend_prep_kernel<128, 3><<<pgrid, 256, 0, st>>>(p); break;
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int tpt = 128 / G;
     dim3 grid((unsigned)((max_q_len + tpt - 1) / tpt), (unsigned)NH, (unsigned)B);
-    if (D == 256) {
+    if (fmt >= 2) {
         switch (G) {
-            case 1: return xlaunch<256, 1>(grid, tk, tv, p, st);
-            case 2: return xlaunch<256, 2>(grid, tk, tv, p, st);
-            case 4: return xlaunch<256, 4>(grid, tk, tv, p, st);
-            case 8: return xlaunch<256, 8>(grid, tk, tv, p, st);
+            case 1: return xlaunch<128, 1, true>(grid, tk, tv, p, st);
+            case 2: return xlaunch<128, 2, true>(grid, tk, tv, p, st);
+            case 4: return xlaunch<128, 4, true>(grid, tk, tv, p, st);
+            case 8: return xlaunch<128, 8, true>(grid, tk, tv, p, st);
+        }
+    } else if (D == 256) {
+        switch (G) {
+            case 1: return xlaunch<256, 1, false>(grid, tk, tv, p, st);
+            case 2: return xlaunch<256, 2, false>(grid, tk, tv, p, st);
+            case 4: return xlaunch<256, 4, false>(grid, tk, tv, p, st);
+            case 8: return xlaunch<256, 8, false>(grid, tk, tv, p, st);
         }
     } else {
         switch (G) {
-            case 1: return xlaunch<128, 1>(grid, tk, tv, p, st);
-            case 2: return xlaunch<128, 2>(grid, tk, tv, p, st);
-            case 4: return xlaunch<128, 4>(grid, tk, tv, p, st);
-            case 8: return xlaunch<128, 8>(grid, tk, tv, p, st);
+            case 1: return xlaunch<128, 1, false>(grid, tk, tv, p, st);
+            case 2: return xlaunch<128, 2, false>(grid, tk, tv, p, st);
+            case 4: return xlaunch<128, 4, false>(grid, tk, tv, p, st);
+            case 8: return xlaunch<128, 8, false>(grid, tk, tv, p, st);
         }
     }
     return cudaErrorInvalidValue;

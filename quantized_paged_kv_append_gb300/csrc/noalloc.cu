@@ -1,7 +1,7 @@
 // noalloc.cu -- decode attention for callers that cannot allocate device memory.
 //
 // kv_decode_attn needs a caller-provided workspace (split-K partial results and
-// merge counters). Some callers have no way to provide one: code that runs
+// merge records). Some callers have no way to provide one: code that runs
 // while a stream is being captured into a CUDA graph (device allocation is not
 // allowed there), hosts whose device memory belongs entirely to another pool or
 // framework, and latency-critical loops that must never allocate. For them this
@@ -57,9 +57,10 @@ extern "C" int kv_decode_attn_noalloc(const qkv_cache_desc* cache, const void* q
     void* scratch = nullptr;
     int rc = scratch_for_current_device(&scratch);
     if (rc) return rc;
-    // The scratch keeps the previous call's contents. The merge counters must
-    // start at zero; a completed call leaves them zero, but clearing the used
-    // span makes an interrupted earlier call harmless.
+    // The scratch keeps the previous call's contents. Every call writes its merge
+    // records before the merge reads them, so nothing has to start at zero;
+    // clearing the used span still keeps each call independent of whatever an
+    // interrupted earlier call left there.
     if (cudaMemsetAsync(scratch, 0, need, (cudaStream_t)stream) != cudaSuccess) return QKV_ERR_CUDA;
     return kv_decode_attn(cache, q, k_new, v_new, batch, num_q_heads, page_table, max_pages_per_seq, seq_lens,
                           max_seq_len, scale, out, out_dtype, scratch, kNoAllocScratchBytes, stream);

@@ -122,22 +122,6 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                  : "memory");
 }
 
-// ---------------------------------------------------------------------------
-// warp-level tensor-core product: D(16x8, f32) += A(16x16, f16) * B(16x8, f16)
-// Fragment ownership (g = lane / 4, t = lane % 4):
-//   A: a[0] = rows g  , cols 2t..2t+1   a[1] = rows g+8, cols 2t..2t+1
-//      a[2] = rows g  , cols 2t+8..+9   a[3] = rows g+8, cols 2t+8..+9
-//   B: b[0] = rows 2t..2t+1, col g      b[1] = rows 2t+8..2t+9, col g
-//   C: c[0..1] = row g, cols 2t..2t+1   c[2..3] = row g+8, cols 2t..2t+1
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void mma_f16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                              uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t r;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));

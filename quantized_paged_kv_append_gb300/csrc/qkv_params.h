@@ -1,5 +1,5 @@
 // qkv_params.h -- kernel parameter blocks and the host-side entry points of the
-// kernel translation units (append.cu, decode.cu), shared with abi.cu.
+// kernel translation units (append.cu, decode_tc.cu, extend.cu), shared with abi.cu.
 #pragma once
 
 #include <cuda.h>
@@ -35,12 +35,9 @@ struct DecodeParams {
     void* out;
     int out_f32;
     float quat[4];
-    float* part1;        // (C + S) partial slots
-    float* part2;        // (C + S) group slots
-    int* seg_cnt;        // [S]
-    int* grp_cnt;        // [C + S]
+    float* part1;        // (C + S) partial slots: m[8], l[8], O[8][D] per piece
     int slot_floats;     // 16 + 8 * D
-    int* rec;            // [C][8]: multi-piece segment records for the merge (int8 tensor-core path)
+    int* rec;            // [max(C, S)][8]: multi-piece segment records for the merge
     int rec_by_seg;      // records indexed by segment (when segments <= CTAs), else by the closing CTA
     const uint16_t* k_new;   // optional bf16 [B][Hkv][D]: quantize-on-write of position seq_lens[b] - 1
     const uint16_t* v_new;
@@ -69,26 +66,25 @@ struct ExtendParams {
     uint16_t* xk;        // workspace: fp16 K' [B * Hkv][Lmax][D]
     uint16_t* xv;        // workspace: fp16 V^T [B * Hkv][D][Lmax]
     float* xs;           // workspace: fp32 key scales x softmax scale [B * Hkv][Lmax][D / 64]
+    float quat[4];       // ISO formats: the pool's unit quaternion (w, x, y, z)
 };
 
 cudaError_t append_upload_levels(const float* lv3, const float* lv4);
 cudaError_t append_read_error(unsigned* out, bool clear);
 cudaError_t append_launch(int fmt, int D, const AppendParams& p, cudaStream_t st);
 
-cudaError_t decode_upload_levels(const float* lv3, const float* lv4);
-cudaError_t decode_read_error(unsigned* out, bool clear);
-cudaError_t decode_launch(int fmt, int D, int G, int grid, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const DecodeParams& p, cudaStream_t st);
+// query heads per CTA of the decode kernel, and the largest batch of one decode call
 int decode_heads_per_cta(int Gtot);
-// int8 K/V on tcgen05 tensor cores (decode_tc.cu): D 128 or 256, G in {1, 2, 4, 8}
+int decode_max_batch();
+// decode on tcgen05 tensor cores (decode_tc.cu): every format, D 128 or 256, G in {1, 2, 4, 8}
 cudaError_t decode_tc_launch(int D, int G, int grid, int fmt, const CUtensorMap& tk, const CUtensorMap& tv,
                              const DecodeParams& p, cudaStream_t st);
 cudaError_t decode_tc_upload_levels(const float* lv3, const float* lv4);
 cudaError_t decode_tc_read_error(unsigned* out, bool clear);
 
 cudaError_t extend_read_error(unsigned* out, bool clear);
+cudaError_t extend_upload_levels(const float* lv3, const float* lv4);
 cudaError_t extend_launch(int fmt, int D, int G, int max_q_len, int NH, int B, const CUtensorMap& tk,
                           const CUtensorMap& tv, const ExtendParams& p, cudaStream_t st);
-int decode_max_batch();
 
 }  // namespace qkv

@@ -22,14 +22,14 @@ def env():
     return torch, qkv
 
 
-def _case(orc, prefix, chunk, hkv, hq, d, seed, spare_pages=2):
-    """Pool holding `prefix[b]` packed tokens per sequence (table sized for
-    prefix + chunk), plus the chunk's bf16 q / k_new / v_new."""
+def _case(orc, prefix, chunk, hkv, hq, d, seed, spare_pages=2, fmt="int8"):
+    """Pool of format `fmt` holding `prefix[b]` packed tokens per sequence (table
+    sized for prefix + chunk), plus the chunk's bf16 q / k_new / v_new."""
     total_pages = [max(1, (p + c + 15) // 16) for p, c in zip(prefix, chunk)]
-    w = Workload("int8", prefix, hkv, hq, d, seed=seed)
+    w = Workload(fmt, prefix, hkv, hq, d, seed=seed)
     table, npages = synth.page_table(seed, total_pages, num_pages=sum(total_pages) + spare_pages)
     w.table, w.num_pages = table, npages
-    pool = orc.Pool(0, npages, hkv, d)
+    pool = orc.Pool(w.fmt, npages, hkv, d, quat=w.quat)
     if w.seq_id.size:
         pool.append(w.k, w.v, w.seq_id, w.pos, table)
     T = int(sum(chunk))
@@ -68,6 +68,43 @@ def test_extend_small(env, orc, prefix, chunk, hkv, hq, d):
     ref = pool.extend(q, kn, vn, cu, pre, table, scale, causal=True)
     got = _run(torch, qkv, w, pool, table, q, kn, vn, cu, pre, scale=scale)
     r = compare_attention(got, ref)
+    assert r["ok"], r
+
+
+@pytest.mark.parametrize("fmt,prefix,chunk,hkv,hq,d", [
+    ("k8v4", [100], [37], 2, 16, 256),
+    ("k8v4", [0, 200, 33], [20, 70, 1], 2, 16, 256),
+    ("iso3", [90], [33], 4, 16, 128),
+    ("iso4", [90], [33], 4, 16, 128),
+    ("iso3", [0, 150, 64], [17, 40, 64], 4, 16, 128),
+    ("iso4", [130], [50], 2, 16, 128),
+    ("iso3", [77], [19], 2, 32, 128),
+    ("iso4", [60], [25], 4, 4, 128),
+])
+def test_extend_formats(env, orc, fmt, prefix, chunk, hkv, hq, d):
+    """k8v4 (V rotated back from the FWHT domain) and ISO3 / ISO4 (raw levels as
+    keys against the rotated query; V rotated back by the conjugate quaternion)
+    prefixes, with the x20 K outlier channels."""
+    torch, qkv = env
+    w, pool, table, q, kn, vn, cu, pre = _case(orc, prefix, chunk, hkv, hq, d, seed=44, fmt=fmt)
+    scale = float(np.float32(1.0 / np.sqrt(d)))
+    ref = pool.extend(q, kn, vn, cu, pre, table, scale, causal=True)
+    got = _run(torch, qkv, w, pool, table, q, kn, vn, cu, pre, scale=scale)
+    r = compare_attention(got, ref)
+    assert r["ok"], r
+
+
+@pytest.mark.parametrize("fmt,hkv,d", [("k8v4", 2, 256), ("iso3", 4, 128), ("iso4", 4, 128)])
+def test_extend_formats_long_prefix_sampled(env, orc, fmt, hkv, d):
+    """A 256-token chunk over an 8192-token prefix (Hq 16); the oracle computes a
+    sample of rows one by one."""
+    torch, qkv = env
+    w, pool, table, q, kn, vn, cu, pre = _case(orc, [8192], [256], hkv, 16, d, seed=45, fmt=fmt)
+    scale = float(np.float32(1.0 / np.sqrt(d)))
+    got = _run(torch, qkv, w, pool, table, q, kn, vn, cu, pre, scale=scale)
+    rows = np.array([0, 1, 63, 64, 200, 255], np.int32)
+    ref = pool.extend(q, kn, vn, cu, pre, table, scale, causal=True, rows=rows)
+    r = compare_attention(got[rows], ref)
     assert r["ok"], r
 
 
@@ -115,9 +152,23 @@ def test_extend_then_deferred_pack_matches_oracle(env, orc):
         assert np.array_equal(g, r)
 
 
-def test_extend_rejects_other_formats(env):
+def test_extend_rejects_unsupported_gqa(env):
+    """num_q_heads / num_kv_heads = 3 is outside {1, 2, 4, 8k}: QKV_ERR_GQA, nothing launched."""
     torch, qkv = env
     c = qkv.PagedKVCache("k8v4", 4, 2, 256)
+    z = torch.zeros((4, 6, 256), dtype=torch.bfloat16, device="cuda")
+    zk = torch.zeros((4, 2, 256), dtype=torch.bfloat16, device="cuda")
+    i32 = lambda a: torch.tensor(a, dtype=torch.int32, device="cuda")
+    with pytest.raises(qkv.QkvError) as e:
+        qkv.extend(c, z, zk, zk, i32([0, 4]), i32([0]), i32([[0, 1, 2, 3]]), 4)
+    assert e.value.code == -3
+
+
+def test_extend_iso_head_dim_256_unsupported(env):
+    """ISO extend runs at head_dim 128 (the rotated query tiles need the shared
+    memory); head_dim 256 returns QKV_ERR_UNSUPPORTED and launches nothing."""
+    torch, qkv = env
+    c = qkv.PagedKVCache("iso3", 4, 2, 256, quat=[0.5, 0.5, 0.5, 0.5])
     z = torch.zeros((4, 16, 256), dtype=torch.bfloat16, device="cuda")
     zk = torch.zeros((4, 2, 256), dtype=torch.bfloat16, device="cuda")
     i32 = lambda a: torch.tensor(a, dtype=torch.int32, device="cuda")

@@ -144,7 +144,7 @@ def test_decode_empty_sequence_is_zero(orc):
     assert np.all(out == 0)
 
 
-@pytest.mark.parametrize("fmt", [0, 1, 2])
+@pytest.mark.parametrize("fmt", FMTS)
 def test_extend_reduces_to_decode_and_dense(orc, fmt):
     d = DIMS[fmt]
     hkv, hq, L0, T = 2, 4, 40, 6
