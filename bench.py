@@ -35,8 +35,10 @@ LAYERS = 8   # default; --layers overrides
 LAUNCHES_PER_STEP = 2   # int8 decode: the tensor-core kernel and the split-merge (combine) kernel
 KV_BYTES_PER_TOKEN = 2 * HKV * (D + 2 * D // 64)        # int8 codes + fp16 scales, K and V: 1056
 # dram__bytes_read.sum + dram__bytes_write.sum of one decode_tc_kernel<256,8> launch at this workload,
-# from an ncu capture of the current kernel build (138.56 MB read + 3.77 MB written)
-NCU_TRAFFIC_BYTES = 142_334_208
+# from an ncu capture of the current kernel build (138.57 MB read + 3.48 MB written)
+NCU_TRAFFIC_BYTES = 142_051_840
+# the same counters for the other decode workloads where a capture of the current kernel exists
+WORKLOAD_NCU_TRAFFIC = {"iso3_82k": 32_894_976}
 DECODE_BYTES = L * KV_BYTES_PER_TOKEN                     # 138,412,032 packed bytes read per step
 WORKLOAD = ("int8 KV decode at 128K context: batch 1, 16 q heads / 2 KV heads, head_dim 256, "
             "131072 cached tokens, page 16, shuffled page table; step = quantize-on-write of 1 token + decode")
@@ -501,8 +503,7 @@ def run_decode_config(args, name):
     peak, peak_kind = peaks()
     value = step_bytes / (per_ms / 1e3) / 1e9
     achieved = step_bytes / (one_ms / 1e3) / 1e9
-    kernel = ("decode_tc_kernel + decode_tc_combine" if fmt in ("int8", "k8v4")
-              else f"decode_kernel<{fmt}> (warp-level mma)")
+    kernel = f"decode_tc_kernel<{d},{min(hq // hkv, 8)},{fmt}> (+ decode_tc_combine)"
     res = {"metric": f"decode-attn packed-KV HBM GB/s, {name}", "value": round(value, 1), "unit": "GB/s",
            "n_gpus": 1, "steps": args.steps * max(3, args.reps), "warmup": max(3, args.warmup),
            "ms_per_step": round(per_ms, 5), "us_per_step": round(per_ms * 1e3, 2), "higher_is_better": True,
@@ -513,7 +514,8 @@ def run_decode_config(args, name):
                       "l2": f"inputs larger than L2: {copies} caches ({copies * step_bytes / 1e9:.2f} GB) cycled"},
            "pct_of_peak": round(100.0 * value / peak, 2),
            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                        "frac": round(achieved / peak, 4), "traffic": None, "peak_kind": peak_kind, "kernel": kernel,
+                        "frac": round(achieved / peak, 4), "traffic": WORKLOAD_NCU_TRAFFIC.get(name),
+                        "peak_kind": peak_kind, "kernel": kernel,
                         "bytes_per_launch": step_bytes, "timing": "CUDA events around each decode call in a graph"},
            "clocks": clocks}
     print(json.dumps(res))
