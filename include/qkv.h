@@ -193,6 +193,24 @@ QKV_API int kv_extend_attn(const qkv_cache_desc* cache, const void* q, const voi
                            void* out, int out_dtype, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * kv_gather_dequant -- the dequantized K and V of one sequence as dense fp32
+ * rows [S8 "What it does": the prompt-chunk path turns the int8 cache back into
+ * a dense buffer before a library GEMM; FT "What": the extend fast path unpacks
+ * ISO blocks into a scratch buffer; K4 "How": V is stored FWHT-rotated].
+ * page_row: int32 device array, the sequence's page-table row: position t lives
+ * in page page_row[t / 16], slot t % 16 (pass page_table + b * max_pages_per_seq).
+ * k_out, v_out: fp32 device [length][num_kv_heads][head_dim], 16-byte aligned,
+ * caller-owned. Values are in the original domain, computed in fp32: int8
+ * c * d; k8v4 V (q - 8) * d per block, rotated back by the FWHT-256 (x 1/16);
+ * ISO s * (conj(q) (x) c) per 4-D group of levels. A page entry outside
+ * [0, num_pages) gives zero rows and sets bit 0 of the device error word.
+ * length == 0 is a no-op. A debug / interoperability call, not on the
+ * attention path.
+ */
+QKV_API int kv_gather_dequant(const qkv_cache_desc* cache, const int32_t* page_row, int length, float* k_out,
+                              float* v_out, void* stream);
+
+/*
  * kv_decode_attn_noalloc -- kv_decode_attn without a caller-provided workspace.
  * The reference pages have no counterpart to this entry point; it exists for
  * callers that cannot allocate device memory: code running while a stream is

@@ -160,3 +160,17 @@ def extend(cache: PagedKVCache, q, k_new, v_new, cu_seqlens, prefix_lens, page_t
                                    int(bool(causal)), _ptr(out), odt, ws_ptr, ws_bytes, _stream(stream))
     _lib.check(rc, "kv_extend_attn")
     return out
+
+
+def gather_dequant(cache: PagedKVCache, page_row, length: int, stream=None):
+    """The dequantized K and V of one sequence (fp32 [length, Hkv, D] each, in
+    the original domain), read through its page-table row (int32 device)."""
+    torch = _torch()
+    dev = page_row.device
+    k = torch.empty((length, cache.desc.num_kv_heads, cache.desc.head_dim), dtype=torch.float32, device=dev)
+    v = torch.empty_like(k)
+    rc = _lib.lib().kv_gather_dequant(C.byref(cache.desc), _ptr(page_row), int(length), _ptr(k), _ptr(v),
+                                      _stream(stream))
+    _lib.check(rc, "kv_gather_dequant")
+    return k, v
+

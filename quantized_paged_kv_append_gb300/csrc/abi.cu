@@ -117,6 +117,7 @@ int device_setup(int* dev_out) {
         if ((e = append_upload_levels(L.l3, L.l4)) != cudaSuccess) return cuda_fail(e);
         if ((e = decode_tc_upload_levels(L.l3, L.l4)) != cudaSuccess) return cuda_fail(e);
         if ((e = extend_upload_levels(L.l3, L.l4)) != cudaSuccess) return cuda_fail(e);
+        if ((e = gather_upload_levels(L.l3, L.l4)) != cudaSuccess) return cuda_fail(e);
         int sms = 0;
         if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return cuda_fail(e);
         g_dev_sms[dev] = sms;
@@ -455,6 +456,33 @@ int kv_extend_attn(const qkv_cache_desc* cache, const void* q, const void* k_new
     return QKV_OK;
 }
 
+int kv_gather_dequant(const qkv_cache_desc* cache, const int32_t* page_row, int length, float* k_out, float* v_out,
+                      void* stream) {
+    int rc = check_desc(cache);
+    if (rc) return rc;
+    if (length < 0) return QKV_ERR_ARG;
+    if (length == 0) return QKV_OK;
+    if (!page_row || !k_out || !v_out || !aligned16(k_out) || !aligned16(v_out)) return QKV_ERR_ARG;
+    int dev;
+    if ((rc = device_setup(&dev))) return rc;
+    GatherParams p;
+    p.kc = (const uint8_t*)cache->k_codes;
+    p.ks = (const uint8_t*)cache->k_scales;
+    p.vc = (const uint8_t*)cache->v_codes;
+    p.vs = (const uint8_t*)cache->v_scales;
+    p.num_pages = cache->num_pages;
+    p.Hkv = cache->num_kv_heads;
+    p.page_row = page_row;
+    p.length = length;
+    p.k_out = k_out;
+    p.v_out = v_out;
+    for (int i = 0; i < 4; ++i) p.quat[i] = cache->quat[i];
+    cudaError_t e = gather_launch(cache->format, cache->head_dim, p, (cudaStream_t)stream);
+    if (e == cudaErrorInvalidValue) return QKV_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return cuda_fail(e);
+    return QKV_OK;
+}
+
 const char* qkv_strerror(int code) {
     switch (code) {
         case QKV_OK: return "ok";
@@ -481,7 +509,10 @@ int qkv_device_error(int clear) {
     if (e != cudaSuccess) return cuda_fail(e);
     e = decode_tc_read_error(&t, clear != 0);
     if (e != cudaSuccess) return cuda_fail(e);
-    return (int)(a | x | t);
+    unsigned g = 0;
+    e = gather_read_error(&g, clear != 0);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return (int)(a | x | t | g);
 }
 
 }  // extern "C"

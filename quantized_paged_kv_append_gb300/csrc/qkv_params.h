@@ -1,5 +1,5 @@
 // qkv_params.h -- kernel parameter blocks and the host-side entry points of the
-// kernel translation units (append.cu, decode_tc.cu, extend.cu), shared with abi.cu.
+// kernel translation units (append.cu, decode_tc.cu, extend.cu, gather.cu), shared with abi.cu.
 #pragma once
 
 #include <cuda.h>
@@ -69,6 +69,19 @@ struct ExtendParams {
     float quat[4];       // ISO formats: the pool's unit quaternion (w, x, y, z)
 };
 
+struct GatherParams {
+    const uint8_t* kc;
+    const uint8_t* ks;
+    const uint8_t* vc;
+    const uint8_t* vs;
+    int num_pages, Hkv;
+    const int32_t* page_row;   // the sequence's page-table row: page of position t = page_row[t / 16]
+    int length;                // positions [0, length)
+    float* k_out;              // fp32 [length][Hkv][D]
+    float* v_out;
+    float quat[4];
+};
+
 cudaError_t append_upload_levels(const float* lv3, const float* lv4);
 cudaError_t append_read_error(unsigned* out, bool clear);
 cudaError_t append_launch(int fmt, int D, const AppendParams& p, cudaStream_t st);
@@ -84,6 +97,10 @@ cudaError_t decode_tc_read_error(unsigned* out, bool clear);
 
 cudaError_t extend_read_error(unsigned* out, bool clear);
 cudaError_t extend_upload_levels(const float* lv3, const float* lv4);
+
+cudaError_t gather_upload_levels(const float* lv3, const float* lv4);
+cudaError_t gather_read_error(unsigned* out, bool clear);
+cudaError_t gather_launch(int fmt, int D, const GatherParams& p, cudaStream_t st);
 cudaError_t extend_launch(int fmt, int D, int G, int max_q_len, int NH, int B, const CUtensorMap& tk,
                           const CUtensorMap& tv, const ExtendParams& p, cudaStream_t st);
 

@@ -93,6 +93,20 @@ def test_validation_rejects_before_launch(qlib):
     assert call(kn=good) == -1            # k_new without v_new
 
 
+def test_gather_validation_rejects_before_launch(qlib):
+    L = qlib.lib()
+    P = C.c_void_p
+    good = P(1 << 20)
+    g = lambda desc, row=good, n=16, k=good, v=good: L.kv_gather_dequant(desc, row, n, k, v, None)
+    assert g(None) == -1
+    assert g(C.byref(_desc(qlib, fmt=9))) == -5
+    assert g(C.byref(_desc(qlib, fmt=1, d=128))) == -2
+    assert g(C.byref(_desc(qlib)), n=-1) == -1
+    assert g(C.byref(_desc(qlib)), n=0, row=None, k=None, v=None) == 0   # no-op
+    assert g(C.byref(_desc(qlib)), row=None) == -1
+    assert g(C.byref(_desc(qlib)), k=P((1 << 20) + 4)) == -1            # fp32 rows must be 16-byte aligned
+
+
 def test_strerror_covers_codes(qlib):
     L = qlib.lib()
     for code in range(-8, 1):
