@@ -93,6 +93,24 @@ def test_decode_mixed_batch_subset(env, orc):
     assert r["ok"], r
 
 
+@pytest.mark.parametrize("B,lo,hi", [(200, 1, 700), (1024, 0, 40)])
+def test_decode_many_sequences(env, orc, B, lo, hi):
+    """More (sequence, head group) segments than CTAs: the merge records are
+    kept per CTA instead of per segment. B = 1024 is the largest batch a call
+    takes; empty sequences are mixed in when lo = 0."""
+    torch, qkv = env
+    rng = np.random.default_rng(B)
+    lens = rng.integers(lo, hi + 1, size=B).astype(np.int32)
+    w = Workload("int8", lens, 2, 16, 256, seed=8, spare=0)
+    pool = w.oracle_pool(orc)
+    got = _run(torch, qkv, w, pool)
+    pick = np.unique(np.concatenate([np.arange(0, B, max(1, B // 24)), [B - 1], np.argmax(lens)[None]]))
+    ref = pool.decode(w.q[pick], w.table[pick], w.lens[pick], w.scale)
+    r = compare_attention(got[pick], ref)
+    assert r["ok"], r
+    assert np.all(got[lens == 0] == 0)
+
+
 def test_decode_empty_and_single_token(env, orc):
     torch, qkv = env
     w = Workload("int8", [0, 1, 17, 0], 2, 16, 256, seed=4)
