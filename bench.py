@@ -618,6 +618,78 @@ def run_mixed(args):
     print(json.dumps(res))
 
 
+EXTEND_CONFIGS = {
+    # format, q heads, KV heads, head_dim: the serving-step chunk (2048 new tokens over a 32768-token
+    # prefix) at each format's decode shape
+    "extend_k8v4": ("k8v4", 16, 2, 256),
+    "extend_iso3": ("iso3", 16, 4, 128),
+    "extend_iso4": ("iso4", 16, 4, 128),
+}
+
+
+def run_extend_config(args, name):
+    """Extend alone over a k8v4 / ISO prefix: prep (dequantize prefix and chunk) +
+    tensor-core attention, timed as one call."""
+    import torch
+
+    import quantized_paged_kv_append_gb300 as qkv
+    from quantized_paged_kv_append_gb300 import build as qbuild
+    from quantized_paged_kv_append_gb300 import synth
+
+    qbuild.build()
+    fmt, hq, hkv, d = EXTEND_CONFIGS[name]
+    T, L0 = 2048, 32768
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    seed = args.seed
+    table, npages = synth.page_table(seed, [(L0 + T + 15) // 16])
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+    quat = synth.unit_quaternion(seed).tolist() if fmt.startswith("iso") else None
+    cache = qkv.PagedKVCache(fmt, npages, hkv, d, device=dev, quat=quat)
+    tab = i32(table)
+    qkv.append(cache, bf(synth.tensor_bf16(seed, "k", (L0, hkv, d), outlier_scale=20.0)),
+               bf(synth.tensor_bf16(seed, "v", (L0, hkv, d))), i32(np.zeros(L0, np.int32)),
+               i32(np.arange(L0, dtype=np.int32)), tab)
+    q = bf(synth.tensor_bf16(seed, "q_ext", (T, hq, d)))
+    kn = bf(synth.tensor_bf16(seed, "k_ext", (T, hkv, d), outlier_scale=20.0))
+    vn = bf(synth.tensor_bf16(seed, "v_ext", (T, hkv, d)))
+    cu, pre = i32(np.array([0, T], np.int32)), i32(np.array([L0], np.int32))
+    out = torch.empty((T, hq, d), dtype=torch.bfloat16, device=dev)
+    ws = qkv.extend_workspace(cache, 1, T, int(tab.shape[1]), device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    scale = 1.0 / math.sqrt(d)
+
+    def step(i):
+        qkv.extend(cache, q, kn, vn, cu, pre, tab, T, scale=scale, out=out, stream=stream, workspace=ws)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(3, args.warmup)):
+            step(i)
+    torch.cuda.synchronize()
+    assert qkv.device_error() == 0
+    proc, cpath = _clock_sampler()
+    steps = max(10, min(args.steps, 50))
+    per_ms, _ = _time_graph(torch, stream, step, steps, 3)
+    clocks = _clock_summary(proc, cpath, 0)
+    tflops_peak = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["bf16_tflops"]) \
+        if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else 1900.0
+    flop = 4.0 * T * hq * d * (L0 + (T + 1) / 2)
+    tflops = flop / (per_ms / 1e3) / 1e12
+    res = {"metric": f"extend attention TFLOP/s, {name}", "value": round(tflops, 1), "unit": "TFLOP/s", "n_gpus": 1,
+           "steps": steps * 3, "warmup": max(3, args.warmup), "ms_per_step": round(per_ms, 5),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16 (fp32 accumulate)",
+           "data": "synthetic (seeded splitmix64 + Box-Muller, bf16)",
+           "config": {"workload": f"{fmt} extend: 2048 new bf16 tokens over a 32768-token packed prefix, causal, "
+                                  f"{hq} q heads / {hkv} KV heads, head_dim {d}, page 16",
+                      "l2": "prefix and dequantized planes re-read per call (L2-resident working set)"},
+           "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": tflops_peak, "unit": "TFLOP/s",
+                        "frac": round(tflops / tflops_peak, 4), "traffic": None,
+                        "kernel": "extend_prep_kernel + extend_kernel", "flop_per_launch": flop},
+           "clocks": clocks}
+    print(json.dumps(res))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -630,7 +702,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layers", type=int, default=8, help="layer caches cycled (8 keeps the working set >> L2)")
     ap.add_argument("--workload", default="int8_128k",
-                    choices=["int8_128k", "mixed"] + sorted(DECODE_CONFIGS),
+                    choices=["int8_128k", "mixed"] + sorted(DECODE_CONFIGS) + sorted(EXTEND_CONFIGS),
                     help="int8_128k (default) is the headline line; the others print their own line")
     args = ap.parse_args()
     global LAYERS
@@ -638,6 +710,8 @@ def main():
     if args.workload != "int8_128k" and args.impl == "cuda":
         if args.workload == "mixed":
             run_mixed(args)
+        elif args.workload in EXTEND_CONFIGS:
+            run_extend_config(args, args.workload)
         else:
             run_decode_config(args, args.workload)
         return
