@@ -193,6 +193,33 @@ QKV_API int kv_extend_attn(const qkv_cache_desc* cache, const void* q, const voi
                            void* out, int out_dtype, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * kv_verify_attn -- the verify window of speculative decoding: several decode
+ * queries per sequence [S8 "What it does": the verify windows go through the
+ * decode kernels; K4 "Tests": batched forms with per-query step arrays].
+ * Sequence b owns query rows [cu_seqlens[b], cu_seqlens[b+1]) of q (bf16
+ * [total_q][num_q_heads][head_dim]); with W = cu_seqlens[b+1] - cu_seqlens[b],
+ * its query j sits at position seq_lens[b] - W + j and attends positions
+ * [0, seq_lens[b] - W + j + 1), all read from the pool (the window's tokens were
+ * appended, and packed, before the call). cu_seqlens (int32 [batch + 1]) and
+ * seq_lens (int32 [batch]) are device arrays; total_q = cu_seqlens[batch] is
+ * given on the host too, total_q <= 1024. out: [total_q][num_q_heads][head_dim],
+ * bf16 or fp32. Every format; num_q_heads / num_kv_heads as for decode.
+ * workspace: at least kv_verify_workspace_size() bytes, 256-byte aligned, no
+ * initialization needed. The call expands the window into one decode row per
+ * query in the workspace (the sequence's page-table row and the query's own
+ * length), then runs kv_decode_attn on those rows: each query reads its own
+ * prefix. A window longer than its sequence sets the position bit of the device
+ * error word; its queries that would sit before position 0 give zero rows.
+ */
+QKV_API size_t kv_verify_workspace_size(const qkv_cache_desc* cache, int num_q_heads, int total_q,
+                                        int max_pages_per_seq);
+
+QKV_API int kv_verify_attn(const qkv_cache_desc* cache, const void* q, int batch, int num_q_heads,
+                           const int32_t* cu_seqlens, const int32_t* seq_lens, int total_q, const int32_t* page_table,
+                           int max_pages_per_seq, int max_seq_len, float scale, void* out, int out_dtype,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * kv_gather_dequant -- the dequantized K and V of one sequence as dense fp32
  * rows [S8 "What it does": the prompt-chunk path turns the int8 cache back into
  * a dense buffer before a library GEMM; FT "What": the extend fast path unpacks

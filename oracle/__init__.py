@@ -75,6 +75,7 @@ def _declare(L):
         "orc_append": (I, [I, I, I, I, I, P, P, P, P, P, P, I, P, P, P, I, P]),
         "orc_gather_dequant": (I, [I, I, I, I, I, P, P, P, P, P, I, I, I, P, P, P]),
         "orc_decode": (I, [I, I, I, I, I, P, P, P, P, P, I, I, P, I, P, F, P, P]),
+        "orc_verify": (I, [I, I, I, I, I, P, P, P, P, P, I, I, P, P, I, P, F, P, P]),
         "orc_decode_split": (I, [I, I, I, I, I, P, P, P, P, P, I, P, I, I, F, P, P, I, P]),
         "orc_extend": (I, [I, I, I, I, I, P, P, P, P, P, P, P, I, P, P, I, P, I, F, I, P, P, I, P]),
     }
@@ -278,6 +279,19 @@ class Pool:
                               _p(self.quat), _p(out))
         if rc != 0:
             raise ValueError(f"orc_decode failed ({rc})")
+        return out
+
+    def verify(self, q_bf16, page_table, seq_lens, cu_seqlens, scale):
+        """Verify window: rows cu[b] .. cu[b+1]-1 of q are the last W_b positions of
+        sequence b, query j attending [0, seq_lens[b] - W_b + j + 1)."""
+        q = _c(q_bf16, np.uint16)
+        pt, sl, cu = _c(page_table, np.int32), _c(seq_lens, np.int32), _c(cu_seqlens, np.int32)
+        T, Hq, Dh = q.shape
+        out = np.empty((T, Hq, Dh), np.float64)
+        rc = lib().orc_verify(*self._head(), _p(q), sl.size, Hq, _p(cu), _p(pt), pt.shape[1], _p(sl), scale,
+                              _p(self.quat), _p(out))
+        if rc != 0:
+            raise ValueError(f"orc_verify failed ({rc})")
         return out
 
     def decode_split(self, q_bf16, page_table, length, scale, bounds):

@@ -681,6 +681,33 @@ int orc_decode_split(int fmt, int num_pages, int Hkv, int D, int P,
     return 0;
 }
 
+// ---- verify window (several decode queries per sequence) ----
+// [S8 "What it does": the verify windows go through the decode kernels; K4
+// "Tests": the batched forms with per-query step arrays]. Sequence b has
+// W = cu[b+1] - cu[b] queries (rows cu[b] .. cu[b+1]-1 of q) for its last W
+// positions: query j sits at position seq_lens[b] - W + j and attends
+// positions [0, seq_lens[b] - W + j + 1), all read back from the pool (the
+// window's tokens were packed when they were appended). This is decode, run
+// once per query with its own length. Returns -3 if W > seq_lens[b].
+int orc_verify(int fmt, int num_pages, int Hkv, int D, int P,
+               const uint8_t* kc, const uint8_t* ks, const uint8_t* vc, const uint8_t* vs,
+               const uint16_t* q_bf16, int B, int Hq, const int32_t* cu, const int32_t* page_table, int max_pages,
+               const int32_t* seq_lens, float scale, const float* quat, double* out) {
+    for (int b = 0; b < B; ++b) {
+        int W = cu[b + 1] - cu[b];
+        if (W > seq_lens[b]) return -3;
+        for (int j = 0; j < W; ++j) {
+            int row = cu[b] + j;
+            int len = seq_lens[b] - W + j + 1;
+            int rc = orc_decode(fmt, num_pages, Hkv, D, P, kc, ks, vc, vs, q_bf16 + (size_t)row * Hq * D, 1, Hq,
+                                page_table + (size_t)b * max_pages, max_pages, &len, scale, quat,
+                                out + (size_t)row * Hq * D);
+            if (rc) return rc;
+        }
+    }
+    return 0;
+}
+
 // ---- extend (prefill-chunk) attention ----
 // [FT "What"]: the chunk attends the packed prefix plus the bf16 new tokens,
 // which are packed only after attention (prefill never reads its own quantized

@@ -174,3 +174,35 @@ def gather_dequant(cache: PagedKVCache, page_row, length: int, stream=None):
     _lib.check(rc, "kv_gather_dequant")
     return k, v
 
+
+def verify_workspace(cache: PagedKVCache, num_q_heads: int, total_q: int, max_pages_per_seq: int, device="cuda"):
+    """Scratch for verify (expanded page-table rows, per-query lengths, decode partials)."""
+    torch = _torch()
+    n = _lib.lib().kv_verify_workspace_size(C.byref(cache.desc), num_q_heads, total_q, max_pages_per_seq)
+    if n == 0:
+        raise QkvError(-1, "kv_verify_workspace_size")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def verify(cache: PagedKVCache, q, cu_seqlens, seq_lens, page_table, max_seq_len: int, scale=None, out=None,
+           out_dtype=None, workspace=None, stream=None):
+    """Verify window: q bf16 [total_q, Hq, D]; rows cu_seqlens[b]..cu_seqlens[b+1] are the
+    last W_b positions of sequence b (query j attends [0, seq_lens[b] - W_b + j + 1)).
+    Returns out [total_q, Hq, D]."""
+    torch = _torch()
+    total, Hq, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((total, Hq, D), dtype=out_dtype or torch.bfloat16, device=q.device)
+    odt = _lib.QKV_OUT_F32 if out.dtype == torch.float32 else _lib.QKV_OUT_BF16
+    B, maxp = int(seq_lens.numel()), int(page_table.shape[1])
+    if workspace is None and total > 0 and B > 0:
+        workspace = verify_workspace(cache, Hq, total, maxp, device=q.device)
+    ws_ptr, ws_bytes = (_ptr(workspace), workspace.numel() * workspace.element_size()) if workspace is not None else (None, 0)
+    rc = _lib.lib().kv_verify_attn(C.byref(cache.desc), _ptr(q), B, Hq, _ptr(cu_seqlens), _ptr(seq_lens), int(total),
+                                   _ptr(page_table), maxp, int(max_seq_len), float(scale), _ptr(out), odt, ws_ptr,
+                                   ws_bytes, _stream(stream))
+    _lib.check(rc, "kv_verify_attn")
+    return out
+

@@ -456,6 +456,59 @@ int kv_extend_attn(const qkv_cache_desc* cache, const void* q, const void* k_new
     return QKV_OK;
 }
 
+// verify workspace: the expanded page-table rows, the per-query lengths, then a decode
+// workspace for total_q rows
+static int verify_layout(const qkv_cache_desc* cache, int num_q_heads, int total_q, int max_pages_per_seq,
+                         size_t* off_lens, size_t* off_dec, size_t* bytes) {
+    int dev;
+    int rc = device_setup(&dev);
+    if (rc) return rc;
+    DecodeLayout L;
+    if ((rc = decode_layout(cache, total_q, num_q_heads, g_dev_sms[dev], &L))) return rc;
+    auto al = [](size_t x) { return (x + 255) / 256 * 256; };
+    *off_lens = al((size_t)total_q * max_pages_per_seq * sizeof(int32_t));
+    *off_dec = *off_lens + al((size_t)total_q * sizeof(int32_t));
+    *bytes = *off_dec + L.bytes;
+    return QKV_OK;
+}
+
+size_t kv_verify_workspace_size(const qkv_cache_desc* cache, int num_q_heads, int total_q, int max_pages_per_seq) {
+    if (check_desc(cache) || total_q < 0 || max_pages_per_seq <= 0) return 0;
+    size_t a, b, n;
+    if (verify_layout(cache, num_q_heads, total_q, max_pages_per_seq, &a, &b, &n)) return 0;
+    return n;
+}
+
+int kv_verify_attn(const qkv_cache_desc* cache, const void* q, int batch, int num_q_heads, const int32_t* cu_seqlens,
+                   const int32_t* seq_lens, int total_q, const int32_t* page_table, int max_pages_per_seq,
+                   int max_seq_len, float scale, void* out, int out_dtype, void* workspace, size_t workspace_bytes,
+                   void* stream) {
+    int rc = check_desc(cache);
+    if (rc) return rc;
+    if (batch < 0 || total_q < 0 || max_seq_len < 0) return QKV_ERR_ARG;
+    if (batch == 0 || total_q == 0) return QKV_OK;
+    if (total_q > decode_max_batch()) return QKV_ERR_UNSUPPORTED;
+    if (!q || !cu_seqlens || !seq_lens || !page_table || !out || max_pages_per_seq <= 0) return QKV_ERR_ARG;
+    if (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads) return QKV_ERR_GQA;
+    size_t off_lens, off_dec, need;
+    if ((rc = verify_layout(cache, num_q_heads, total_q, max_pages_per_seq, &off_lens, &off_dec, &need))) return rc;
+    if (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 255u)) return QKV_ERR_WORKSPACE;
+    uint8_t* ws = (uint8_t*)workspace;
+    VerifyParams vp;
+    vp.cu = cu_seqlens;
+    vp.seq_lens = seq_lens;
+    vp.page_table = page_table;
+    vp.B = batch;
+    vp.max_pages = max_pages_per_seq;
+    vp.table_rep = (int32_t*)ws;
+    vp.lens_rep = (int32_t*)(ws + off_lens);
+    cudaError_t e = verify_expand_launch(vp, total_q, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return kv_decode_attn(cache, q, nullptr, nullptr, total_q, num_q_heads, vp.table_rep, max_pages_per_seq,
+                          vp.lens_rep, max_seq_len, scale, out, out_dtype, ws + off_dec, workspace_bytes - off_dec,
+                          stream);
+}
+
 int kv_gather_dequant(const qkv_cache_desc* cache, const int32_t* page_row, int length, float* k_out, float* v_out,
                       void* stream) {
     int rc = check_desc(cache);
@@ -509,10 +562,12 @@ int qkv_device_error(int clear) {
     if (e != cudaSuccess) return cuda_fail(e);
     e = decode_tc_read_error(&t, clear != 0);
     if (e != cudaSuccess) return cuda_fail(e);
-    unsigned g = 0;
+    unsigned g = 0, v = 0;
     e = gather_read_error(&g, clear != 0);
     if (e != cudaSuccess) return cuda_fail(e);
-    return (int)(a | x | t | g);
+    e = verify_read_error(&v, clear != 0);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return (int)(a | x | t | g | v);
 }
 
 }  // extern "C"

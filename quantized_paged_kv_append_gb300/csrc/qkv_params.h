@@ -1,5 +1,5 @@
 // qkv_params.h -- kernel parameter blocks and the host-side entry points of the
-// kernel translation units (append.cu, decode_tc.cu, extend.cu, gather.cu), shared with abi.cu.
+// kernel translation units (append.cu, decode_tc.cu, extend.cu, gather.cu, verify.cu), shared with abi.cu.
 #pragma once
 
 #include <cuda.h>
@@ -82,6 +82,15 @@ struct GatherParams {
     float quat[4];
 };
 
+struct VerifyParams {
+    const int32_t* cu;          // [B + 1] query rows of each sequence's window
+    const int32_t* seq_lens;    // [B]
+    const int32_t* page_table;  // [B][max_pages]
+    int B, max_pages;
+    int32_t* table_rep;         // workspace: [total_q][max_pages], row r = the page-table row of its sequence
+    int32_t* lens_rep;          // workspace: [total_q], the query's own length
+};
+
 cudaError_t append_upload_levels(const float* lv3, const float* lv4);
 cudaError_t append_read_error(unsigned* out, bool clear);
 cudaError_t append_launch(int fmt, int D, const AppendParams& p, cudaStream_t st);
@@ -101,6 +110,9 @@ cudaError_t extend_upload_levels(const float* lv3, const float* lv4);
 cudaError_t gather_upload_levels(const float* lv3, const float* lv4);
 cudaError_t gather_read_error(unsigned* out, bool clear);
 cudaError_t gather_launch(int fmt, int D, const GatherParams& p, cudaStream_t st);
+
+cudaError_t verify_read_error(unsigned* out, bool clear);
+cudaError_t verify_expand_launch(const VerifyParams& p, int total_q, cudaStream_t st);
 cudaError_t extend_launch(int fmt, int D, int G, int max_q_len, int NH, int B, const CUtensorMap& tk,
                           const CUtensorMap& tv, const ExtendParams& p, cudaStream_t st);
 

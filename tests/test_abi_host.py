@@ -107,6 +107,21 @@ def test_gather_validation_rejects_before_launch(qlib):
     assert g(C.byref(_desc(qlib)), k=P((1 << 20) + 4)) == -1            # fp32 rows must be 16-byte aligned
 
 
+def test_verify_validation_rejects_before_launch(qlib):
+    L = qlib.lib()
+    P = C.c_void_p
+    good = P(1 << 20)
+    v = lambda desc, B=1, tq=2, q=good, cu=good: L.kv_verify_attn(desc, q, B, 16, cu, good, tq, good, 4, 64, 0.0625,
+                                                                  good, 0, good, 1 << 30, None)
+    assert v(None) == -1
+    assert v(C.byref(_desc(qlib, fmt=7))) == -5
+    assert v(C.byref(_desc(qlib)), B=-1) == -1
+    assert v(C.byref(_desc(qlib)), B=0) == 0          # no-op
+    assert v(C.byref(_desc(qlib)), tq=0) == 0         # no-op
+    assert v(C.byref(_desc(qlib)), tq=2000) == -8     # more query rows than one decode call takes
+    assert v(C.byref(_desc(qlib)), cu=None) == -1
+
+
 def test_strerror_covers_codes(qlib):
     L = qlib.lib()
     for code in range(-8, 1):

@@ -229,3 +229,51 @@ def test_append_reports_bad_page_entries(orc):
     k = synth.tensor_bf16(0, "k", (20, 2, 256))
     skipped = pool.append(k, k, np.zeros(20, np.int32), np.arange(20, dtype=np.int32), bad)
     assert skipped == 4   # positions 16..19 fall on the bad page
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_verify_window_of_one_is_decode(orc, fmt):
+    """A verify window of one query per sequence is plain decode."""
+    d = DIMS[fmt]
+    pool, table, _, _ = _pool(orc, fmt, 90, 2, d, seed=11, B=3)
+    q = synth.tensor_bf16(11, "q", (3, 8, d))
+    lens = np.array([90, 17, 64], np.int32)
+    cu = np.arange(4, dtype=np.int32)
+    ver = pool.verify(q, table, lens, cu, float(np.float32(1 / np.sqrt(d))))
+    dec = pool.decode(q, table, lens, float(np.float32(1 / np.sqrt(d))))
+    assert np.array_equal(ver, dec)
+
+
+def test_verify_equals_extend_on_a_lossless_window(orc):
+    """Window tokens whose int8 packing is lossless (values c / 8 with |c| <= 127
+    and one |c| = 127 per 64-value group, so the scale is exactly 1/8): reading
+    them back from the pool (verify) must give what extend gives when it takes
+    them as raw bf16 new tokens after the same packed prefix."""
+    d, hkv, hq, L0, W = 256, 2, 8, 70, 5
+    rng = np.random.default_rng(3)
+    codes = rng.integers(-127, 128, size=(W, 2, hkv, d))
+    codes[..., ::64] = 127 * np.where(rng.random(codes[..., ::64].shape) < 0.5, -1, 1)
+    win = (codes / 8.0).astype(np.float32)
+    win_bits = (win.view(np.uint32) >> 16).astype(np.uint16)      # exact in bf16
+    assert np.array_equal(synth.bf16_to_f32(win_bits), win)
+    pre_k = synth.tensor_bf16(3, "k", (L0, hkv, d), outlier_scale=20.0)
+    pre_v = synth.tensor_bf16(3, "v", (L0, hkv, d))
+    table, npages = synth.page_table(3, [(L0 + W + 15) // 16])
+    full = orc.Pool(0, npages, hkv, d)
+    full.append(np.concatenate([pre_k, win_bits[:, 0]]), np.concatenate([pre_v, win_bits[:, 1]]),
+                np.zeros(L0 + W, np.int32), np.arange(L0 + W, dtype=np.int32), table)
+    pre = orc.Pool(0, npages, hkv, d)
+    pre.append(pre_k, pre_v, np.zeros(L0, np.int32), np.arange(L0, dtype=np.int32), table)
+    q = synth.tensor_bf16(3, "q", (W, hq, d))
+    scale = 0.0625
+    ver = full.verify(q, table, np.array([L0 + W], np.int32), np.array([0, W], np.int32), scale)
+    ext = pre.extend(q, win_bits[:, 0], win_bits[:, 1], np.array([0, W], np.int32), np.array([L0], np.int32),
+                     table, scale, causal=True)
+    assert np.allclose(ver, ext, rtol=0, atol=1e-12)
+
+
+def test_verify_rejects_window_longer_than_sequence(orc):
+    pool, table, _, _ = _pool(orc, 0, 10, 2, 256, seed=12)
+    q = synth.tensor_bf16(12, "q", (4, 2, 256))
+    with pytest.raises(ValueError):
+        pool.verify(q, table, np.array([3], np.int32), np.array([0, 4], np.int32), 0.0625)
