@@ -690,6 +690,65 @@ def run_extend_config(args, name):
     print(json.dumps(res))
 
 
+def run_verify(args):
+    """The verify window at the 128K int8 shape: 4 queries at positions L - 4 .. L - 1 of one
+    sequence (the window's tokens already packed), one kv_verify_attn call per step."""
+    import torch
+
+    import quantized_paged_kv_append_gb300 as qkv
+    from quantized_paged_kv_append_gb300 import build as qbuild
+    from quantized_paged_kv_append_gb300 import synth
+
+    qbuild.build()
+    W = 4
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    seed = args.seed
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+    pages = (L + 15) // 16
+    k_d = bf(synth.tensor_bf16(seed, "k", (L, HKV, D), outlier_scale=20.0))
+    v_d = bf(synth.tensor_bf16(seed, "v", (L, HKV, D)))
+    caches, tabs = [], []
+    for c in range(LAYERS):
+        cache = qkv.PagedKVCache("int8", pages, HKV, D, device=dev)
+        t = i32(synth.page_table(seed * 100 + c, [pages])[0])
+        qkv.append(cache, k_d, v_d, i32(np.zeros(L, np.int32)), i32(np.arange(L, dtype=np.int32)), t)
+        caches.append(cache)
+        tabs.append(t)
+    del k_d, v_d
+    q_d = bf(synth.tensor_bf16(seed, "q_verify", (LAYERS, W, HQ, D)))
+    cu, lens = i32(np.array([0, W], np.int32)), i32(np.array([L], np.int32))
+    out = torch.empty((W, HQ, D), dtype=torch.bfloat16, device=dev)
+    ws = qkv.verify_workspace(caches[0], HQ, W, pages, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(i):
+        c = i % LAYERS
+        qkv.verify(caches[c], q_d[c], cu, lens, tabs[c], L, scale=1.0 / math.sqrt(D), out=out, workspace=ws,
+                   stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(3, args.warmup)):
+            step(i)
+    torch.cuda.synchronize()
+    assert qkv.device_error() == 0
+    proc, cpath = _clock_sampler()
+    per_ms, _ = _time_graph(torch, stream, step, args.steps, max(3, args.reps))
+    clocks = _clock_summary(proc, cpath, 0)
+    res = {"metric": "verify window call time, int8 128K, W = 4", "value": round(per_ms * 1e3, 2), "unit": "us",
+           "n_gpus": 1, "steps": args.steps * max(3, args.reps), "warmup": max(3, args.warmup),
+           "ms_per_step": round(per_ms, 5), "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+           "dtype": "int8", "data": "synthetic (seeded splitmix64 + Box-Muller, bf16)",
+           "config": {"workload": f"verify window of {W} queries over one {L}-token int8 sequence, {HQ} q heads / "
+                                  f"{HKV} KV heads, head_dim {D}, page 16; expansion kernel + tensor-core decode over "
+                                  f"{W} rows", "layer_copies": LAYERS,
+                      "l2": f"inputs larger than L2: {LAYERS} caches cycled"},
+           "packed_gbs_per_query": round(DECODE_BYTES * W / (per_ms / 1e3) / 1e9, 1),
+           "clocks": clocks}
+    print(json.dumps(res))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -702,7 +761,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layers", type=int, default=8, help="layer caches cycled (8 keeps the working set >> L2)")
     ap.add_argument("--workload", default="int8_128k",
-                    choices=["int8_128k", "mixed"] + sorted(DECODE_CONFIGS) + sorted(EXTEND_CONFIGS),
+                    choices=["int8_128k", "mixed", "verify_int8_128k"] + sorted(DECODE_CONFIGS) + sorted(EXTEND_CONFIGS),
                     help="int8_128k (default) is the headline line; the others print their own line")
     args = ap.parse_args()
     global LAYERS
@@ -712,6 +771,8 @@ def main():
             run_mixed(args)
         elif args.workload in EXTEND_CONFIGS:
             run_extend_config(args, args.workload)
+        elif args.workload == "verify_int8_128k":
+            run_verify(args)
         else:
             run_decode_config(args, args.workload)
         return
