@@ -98,7 +98,7 @@ def append(cache: PagedKVCache, k, v, seq_id, pos, page_table, stream=None):
 
 
 def decode_workspace(cache: PagedKVCache, batch: int, num_q_heads: int, max_seq_len: int, device="cuda"):
-    """Zero-filled workspace for `decode` (the kernel leaves its counters zeroed)."""
+    """Workspace for `decode`: partial results and merge records (no initialization needed)."""
     torch = _torch()
     n = _lib.lib().kv_decode_workspace_size(C.byref(cache.desc), batch, num_q_heads, max_seq_len)
     if n == 0 and batch > 0:
