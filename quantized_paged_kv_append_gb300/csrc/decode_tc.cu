@@ -73,8 +73,8 @@ struct TG {
     static constexpr int VROW = ISO ? KROW : (VQ ? D / 2 : D);
     static constexpr int VSROW = ISO ? KSROW : (VQ ? 2 * (D / 32) : 2 * NA);
     static constexpr int VG = ISO ? D / 128 : (VQ ? D / 32 : D / 64);   // V scale groups
-    static constexpr int PG = VQ ? VG : 4;        // P' column groups of 16 (8 heads hi + lo); padded to 4
-    static constexpr int PM = 16 * PG;            // M of the PV MMA: 64, or 128 for q4 V
+    static constexpr int PG = 4;                  // P' column groups of 16 (8 heads hi + lo)
+    static constexpr int PM = 16 * PG;            // M of the PV MMA: 64
     static constexpr int PAGE_B = KROW * kPage;   // staged K codes of one page
     static constexpr int VPAGE_B = VROW * kPage;  // staged V codes of one page
     static constexpr int VBOX = VPAGE_B / 2048;   // 128-byte TMA boxes per V page (int8, q4)
@@ -599,20 +599,24 @@ __global__ void __launch_bounds__(kThr, 1)
                 }
             } else if constexpr (VQ) {
                 // q4_0 block b (32 dims: 16 code bytes, byte j = element j low, j + 16 high nibble)
-                // -> exact fp16 (q - 8). Pairs come out as (4w, 4w + 2), (4w + 1, 4w + 3): the same
-                // position <-> dimension permutation (perm4) as the int8 path.
+                // -> fp16((q - 8) * d), one rounding (q - 8 is exact in fp16; the block scale d is
+                // folded in here, so P' needs no V scale groups). Pairs come out as (4w, 4w + 2),
+                // (4w + 1, 4w + 3): the same position <-> dimension permutation (perm4) as the int8 path.
+                const uint16_t* vsr = reinterpret_cast<const uint16_t*>(sm + X::OFF_VSC + (buf * kTP + jpage) * X::VSC_B +
+                                                                        rr * X::VSROW);
 #pragma unroll
                 for (int bi = 0; bi < D / 64; ++bi) {
                     const int blk = (D / 64) * hf + bi;
                     const uint4 x = *reinterpret_cast<const uint4*>(slot + sw_off(rr, blk));
                     const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+                    const uint32_t sb = vsr[blk], s2 = sb | (sb << 16);
                     uint32_t lo[8], hi[8];
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        lo[2 * k] = hsub2_u32((xs[k] & 0x000f000fu) | 0x64006400u, 0x64086408u);
-                        lo[2 * k + 1] = hsub2_u32(((xs[k] >> 8) & 0x000f000fu) | 0x64006400u, 0x64086408u);
-                        hi[2 * k] = hsub2_u32(((xs[k] >> 4) & 0x000f000fu) | 0x64006400u, 0x64086408u);
-                        hi[2 * k + 1] = hsub2_u32(((xs[k] >> 12) & 0x000f000fu) | 0x64006400u, 0x64086408u);
+                        lo[2 * k] = hfma2_u32(hsub2_u32((xs[k] & 0x000f000fu) | 0x64006400u, 0x64086408u), s2, 0u);
+                        lo[2 * k + 1] = hfma2_u32(hsub2_u32(((xs[k] >> 8) & 0x000f000fu) | 0x64006400u, 0x64086408u), s2, 0u);
+                        hi[2 * k] = hfma2_u32(hsub2_u32(((xs[k] >> 4) & 0x000f000fu) | 0x64006400u, 0x64086408u), s2, 0u);
+                        hi[2 * k + 1] = hfma2_u32(hsub2_u32(((xs[k] >> 12) & 0x000f000fu) | 0x64006400u, 0x64086408u), s2, 0u);
                     }
                     uint8_t* atom = vp + (blk >> 1) * 16384;
                     const int ch = 4 * (blk & 1);
@@ -836,7 +840,12 @@ __global__ void __launch_bounds__(kThr, 1)
                 wait_or_flag(&bars[B_VF + buf], ph);
                 float vsf[X::VG];
                 int e_row = 0;
-                {
+                if constexpr (VQ) {
+                    // the q4 block scales are folded into V' by the converters
+#pragma unroll
+                    for (int g = 0; g < X::VG; ++g) vsf[g] = 1.0f;
+                    e_row = 15;   // the fp16 exponent field of 1.0
+                } else {
                     const uint8_t* vsr = sm + X::OFF_VSC + (buf * kTP + jpage) * X::VSC_B + (r & 15) * X::VSROW;
 #pragma unroll
                     for (int g = 0; g < X::VG; ++g) {
@@ -968,16 +977,16 @@ __global__ void __launch_bounds__(kThr, 1)
             const long long seg = (long long)pc.b * p.NH + pc.hg;
             float* mine = p.part1 + (size_t)(c + seg) * p.slot_floats;
             if constexpr (VQ) {
-                // q4 V (M = 128, lane = O row 16 g + j): warp w holds groups 2w (lanes 0-15) and
-                // 2w + 1 (lanes 16-31). The rotated output goes per head to shared memory (the P'
-                // area is free), the inverse rotation (FWHT-256 x 1/16, its own inverse) runs there,
-                // then the output or the partial slot is written. The rotation is linear, so the
-                // merge of partial slots commutes with it.
+                // q4 V: O in the int8 layout (warp g: lanes h and 8 + h hold the hi and lo rows of
+                // head h; P' is the same in every group, so warp g takes the dims of group g). The
+                // rotated output goes per head to shared memory (the P' area is free), the inverse
+                // rotation (FWHT-256 x 1/16, its own inverse) runs there, then the output or the
+                // partial slot is written. The rotation is linear, so the merge of partial slots
+                // commutes with it.
                 float* ox = reinterpret_cast<float*>(sm + X::OFF_PP);   // [8 heads][D]
                 {
-                    const int h = lane & 7, grp = lane >> 4;
                     const float e_inv = (E == 1000) ? 0.0f : exp2i(-E);
-                    const float Lh = h < G ? sML[8 + (h < G ? h : 0)] : 0.0f;
+                    const float Lh = lane < G ? sML[8 + (lane < G ? lane : 0)] : 0.0f;
                     const float inv = npieces == 1 ? (Lh > 0.0f ? e_inv / Lh : 0.0f) : e_inv;
 #pragma unroll 1
                     for (int c4 = 0; c4 < 4; ++c4) {
@@ -985,10 +994,10 @@ __global__ void __launch_bounds__(kThr, 1)
                         tmem_ld16(tmem + lb + X::OCOL + 64 * warp + 16 * c4, v);
 #pragma unroll
                         for (int j = 0; j < 16; ++j) v[j] += __shfl_xor_sync(0xffffffffu, v[j], 8);
-                        if ((lane & 8) == 0 && (c4 >> 1) == grp && h < G) {
+                        if (lane < G) {
                             const int d0 = 64 * warp + 16 * c4;
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) ox[h * D + d0 + perm4(j)] = v[j] * inv;
+                            for (int j = 0; j < 16; ++j) ox[lane * D + d0 + perm4(j)] = v[j] * inv;
                         }
                     }
                 }
