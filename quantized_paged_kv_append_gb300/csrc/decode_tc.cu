@@ -33,6 +33,11 @@
 //     sums), run a lazy online softmax (the frame max moves only when a score
 //     exceeds it by 2^8; all four warps agree on it once per tile), and write P'
 //     = p * V-scale * 2^E as fp16 hi + lo parts;
+//   * the other formats reuse the same roles: k8v4 converts its q4_0 V into
+//     fp16((q - 8) * d) (the block scale folded into V', so P' carries none)
+//     and rotates each piece's O back by the FWHT-256; ISO turns code pairs into
+//     fp16 level pairs through a per-lane table, takes the query rotated by the
+//     pool quaternion as fp16 hi + lo tiles, and rotates O back per 4-D group;
 //   * pieces that do not cover a whole sequence write a partial slot (m, l, O) to
 //     the caller's workspace; a second kernel (decode_tc_combine), launched with
 //     programmatic stream serialization, merges them.

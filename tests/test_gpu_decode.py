@@ -173,14 +173,17 @@ def test_decode_bad_page_entry_flags_without_fault(env, orc):
     assert qkv.device_error() & 1
 
 
-@pytest.mark.parametrize("fmt,d,hkv,hq", [("int8", 256, 2, 16), ("k8v4", 256, 2, 16), ("iso3", 128, 4, 16),
-                                          ("iso4", 128, 4, 16), ("int8", 256, 2, 32), ("iso4", 256, 2, 4)])
-def test_decode_fused_quantize_on_write(env, orc, fmt, d, hkv, hq):
+@pytest.mark.parametrize("fmt,d,hkv,hq,lens", [
+    ("int8", 256, 2, 16, [1, 37, 300, 16, 1000]), ("k8v4", 256, 2, 16, [1, 37, 300, 16, 1000]),
+    ("iso3", 128, 4, 16, [1, 37, 300, 16, 1000]), ("iso4", 128, 4, 16, [1, 37, 300, 16, 1000]),
+    ("int8", 256, 2, 32, [1, 37, 300, 16, 1000]), ("iso4", 256, 2, 4, [1, 37, 300, 16, 1000]),
+    ("int8", 256, 2, 16, [131072]),   # the benchmark step: quantize-on-write + decode at 128K
+])
+def test_decode_fused_quantize_on_write(env, orc, fmt, d, hkv, hq, lens):
     """kv_decode_attn with k_new/v_new: the newest token (position L - 1) is
     quantized inside the decode launch. The pool bytes must equal the oracle's
     append of all tokens, and the output the oracle's decode over them."""
     torch, qkv = env
-    lens = [1, 37, 300, 16, 1000]
     w = Workload(fmt, lens, hkv, hq, d, seed=31)
     full = w.oracle_pool(orc)
     ref = full.decode(w.q, w.table, w.lens, w.scale)
