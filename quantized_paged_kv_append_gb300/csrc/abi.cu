@@ -101,10 +101,11 @@ const Levels& levels() {
 // per-device set-up (constant tables, SM count), done once per device with that
 // device current
 // ---------------------------------------------------------------------------
-constexpr int kMaxDevices = 64;
 std::mutex g_dev_mu;
 bool g_dev_ready[kMaxDevices];
 int g_dev_sms[kMaxDevices];
+
+std::mutex g_attr_mu;
 
 int device_setup(int* dev_out) {
     int dev = 0;
@@ -256,6 +257,20 @@ int extend_layout(const qkv_cache_desc* d, int batch, int max_q_len, int max_pag
 }
 
 }  // namespace
+
+cudaError_t qkv::smem_attr_once(const void* fn, int bytes, bool (&done)[kMaxDevices]) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    if (!done[dev]) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e != cudaSuccess) return e;
+        done[dev] = true;
+    }
+    return cudaSuccess;
+}
 
 extern "C" {
 

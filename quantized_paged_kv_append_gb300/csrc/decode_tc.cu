@@ -126,7 +126,8 @@ enum {
     B_PFL = 18,  // P' written (4 softmax warps)
     B_QRD = 19,  // query tile of a piece written (1)
     B_PAT = 20,  // [kind] producer: the newest token's page landed (1 + tx)
-    B_N = 22
+    B_DRN = 22,  // every MMA of the CTA complete (commit), before TMEM is released
+    B_N = 23
 };
 static_assert(B_N <= 32, "barrier area holds 32 barriers");
 
@@ -256,6 +257,7 @@ __global__ void __launch_bounds__(kThr, 1)
         mbar_init(&bars[B_QRD], 1);
         mbar_init(&bars[B_PAT], 1);
         mbar_init(&bars[B_PAT + 1], 1);
+        mbar_init(&bars[B_DRN], 1);
         fence_mbar_init();
         *s_abort = 0;
     }
@@ -418,7 +420,8 @@ __global__ void __launch_bounds__(kThr, 1)
                         }
                         bulk_load(ss + jp * scb, scl + (size_t)row * scrow, scb, pb);
                     }
-                    wait_or_flag(pb, pat_phase);
+                    // after an abort elsewhere, still let this copy land before the row is patched
+                    if (!wait_or_flag(pb, pat_phase)) mbar_wait_bounded(pb, pat_phase);
                     pat_phase ^= 1;
                     uint8_t* rowbuf = sm + X::OFF_ROW + kind * 512;
                     const uint16_t* src = newsrc + ((size_t)pc.b * p.Hkv + kvh) * D;
@@ -454,8 +457,10 @@ __global__ void __launch_bounds__(kThr, 1)
                 if (lane == 0) mbar_arrive(full);
             }
         }
-        // every copy issued above has landed before the CTA exits
-        for (uint32_t t = (T >= 2 ? T - 2 : 0); t < T; ++t) wait_or_flag(fullb + (t & 1), (t >> 1) & 1);
+        // every copy issued above has landed before the CTA exits (bounded waits that do not
+        // stop at the abort flag: the copies of an aborted launch still land in this CTA's memory)
+        for (uint32_t t = (T >= 2 ? T - 2 : 0); t < T; ++t)
+            if (!mbar_wait_bounded(fullb + (t & 1), (t >> 1) & 1)) atomicOr(&g_err_dtc, kErrWait);
     } else if (warp == kWMma) {
         // =============================== MMA issue ===============================
         if (lane == 0) {
@@ -544,6 +549,12 @@ __global__ void __launch_bounds__(kThr, 1)
             if (hq || hv) {
                 atomicOr(&g_err_dtc, kErrWait);
                 *s_abort = 1;
+            }
+            // every MMA issued above completes before TMEM is released (after an abort the
+            // loop ends with MMAs possibly still in flight)
+            if (Tq > 0 || Tv > 0) {
+                umma_commit(&bars[B_DRN]);
+                if (!mbar_wait_bounded(&bars[B_DRN], 0)) atomicOr(&g_err_dtc, kErrWait);
             }
         }
         __syncwarp();
@@ -1247,11 +1258,10 @@ static cudaError_t launch_tc(int grid, const CUtensorMap& tk, const CUtensorMap&
     p.rec_by_seg = (long long)p.B * p.NH <= grid;
     using X = TG<D, FMT>;
     auto fn = decode_tc_kernel<D, G, FMT>;
-    static bool configured = false;   // per instantiation; the attribute is per device context
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, X::SMEM + 1024);
+    static bool configured[kMaxDevices];   // this instantiation's attribute, per device
+    {
+        cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(fn), X::SMEM + 1024, configured);
         if (e != cudaSuccess) return e;
-        configured = true;
     }
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -64,7 +64,7 @@ struct XGeo {
     static constexpr int OFF_KS = OFF_P + 128 * 128;     // 2 buffers
     static constexpr int OFF_RED = OFF_KS + 2 * KS_BYTES;   // [2 tiles][kXSplit parts][128 rows] row-max / row-sum exchange
     static constexpr int OFF_BAR = OFF_RED + 2 * kXSplit * 128 * 4;
-    static constexpr int OFF_TMEM = OFF_BAR + 16 * 8;
+    static constexpr int OFF_TMEM = OFF_BAR + 24 * 8;
     static constexpr int OFF_QR = (OFF_TMEM + 16 + 1023) / 1024 * 1024;   // ISO: [hi, lo] x Q_BYTES
     static constexpr int SMEM = ISO ? OFF_QR + 2 * Q_BYTES : OFF_TMEM + 16;
     static constexpr int S_COLS = NA * 64;               // TMEM columns of the group scores
@@ -82,7 +82,8 @@ enum {
     B_VE = 7,     // [2] PV of the tile complete: V slot free (commit)
     B_SFULL = 9, B_SFREE = 10, B_PFULL = 11, B_PVDONE = 12,
     B_RMX = 13,   // [2] row maxima of every key part written (all softmax threads)
-    B_RSUM = 15   // row sums of every part written
+    B_RSUM = 15,  // row sums of every part written
+    B_DRAIN = 16  // every MMA of the CTA complete (commit), before TMEM is released
 };
 
 __device__ __forceinline__ uint32_t bf16x2_to_h2(uint32_t w) {
@@ -380,6 +381,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
         mbar_init(&bars[B_RMX], kXSoft);
         mbar_init(&bars[B_RMX + 1], kXSoft);
         mbar_init(&bars[B_RSUM], kXSoft);
+        mbar_init(&bars[B_DRAIN], 1);
         fence_mbar_init();
     }
     tc_fence_before();
@@ -470,6 +472,12 @@ __global__ void __launch_bounds__(kXThreads, 1)
                     umma_f16(tmem_O, sw128_desc(ps + 32 * u), sw128_desc(vs + 32 * u), IDPV, (j > 0 || u > 0));
                 umma_commit(&bars[B_VE + (j & 1)]);
                 umma_commit(&bars[B_PVDONE]);
+            }
+            // A wait that ran out ends the loop early, possibly with MMAs still in flight:
+            // every MMA issued above completes before the CTA releases TMEM and exits.
+            if (NT > 0) {
+                umma_commit(&bars[B_DRAIN]);
+                if (!mbar_wait_bounded(&bars[B_DRAIN], 0)) atomicOr(&g_err_extend, kErrWait);
             }
         }
         __syncwarp();
@@ -692,11 +700,10 @@ static cudaError_t xlaunch(dim3 grid, const CUtensorMap& tk, const CUtensorMap& 
                            cudaStream_t st) {
     auto fn = extend_kernel<D, G, ISO>;
     constexpr int smem = XGeo<D, ISO>::SMEM + 1024;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    static bool configured[kMaxDevices];   // this instantiation's attribute, per device
+    {
+        cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(fn), smem, configured);
         if (e != cudaSuccess) return e;
-        configured = true;
     }
     fn<<<grid, kXThreads, smem, st>>>(tk, tv, p);
     return cudaGetLastError();

@@ -91,6 +91,15 @@ struct VerifyParams {
     int32_t* lens_rep;          // workspace: [total_q], the query's own length
 };
 
+// Devices the library keeps per-device state for (device ordinals 0 .. kMaxDevices - 1).
+constexpr int kMaxDevices = 64;
+
+// Raises kernel `fn`'s dynamic shared-memory limit to `bytes` on the current
+// device the first time it is asked there. The attribute belongs to the device's
+// context, so `done` (one flag per device, owned by the caller: one array per
+// kernel) records where it has been set; a process-wide mutex guards the flags.
+cudaError_t smem_attr_once(const void* fn, int bytes, bool (&done)[kMaxDevices]);
+
 cudaError_t append_upload_levels(const float* lv3, const float* lv4);
 cudaError_t append_read_error(unsigned* out, bool clear);
 cudaError_t append_launch(int fmt, int D, const AppendParams& p, cudaStream_t st);
