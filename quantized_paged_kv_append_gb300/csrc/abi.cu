@@ -215,7 +215,7 @@ struct DecodeLayout {
     int S;          // segments
     int Cmax;       // CTA upper bound
     int slot_floats;
-    size_t off_rec, bytes;
+    size_t bytes;
 };
 
 int decode_layout(const qkv_cache_desc* d, int batch, int num_q_heads, int sms, DecodeLayout* L) {
@@ -227,11 +227,10 @@ int decode_layout(const qkv_cache_desc* d, int batch, int num_q_heads, int sms, 
     L->S = batch * L->NH;
     L->Cmax = sms;
     L->slot_floats = 16 + 8 * d->head_dim;
-    // partial slots (m, l, O) of the pieces, then the merge records (per CTA or per segment)
+    // partial slots (m, l, O) of the pieces: piece (CTA c, segment s) uses slot c + s
     const size_t slots = (size_t)L->Cmax + L->S;
     auto al = [](size_t x) { return (x + 255) / 256 * 256; };
-    L->off_rec = al(slots * L->slot_floats * sizeof(float));
-    L->bytes = L->off_rec + al((size_t)L->Cmax * 8 * sizeof(int));   // records: per segment only when S <= grid
+    L->bytes = al(slots * L->slot_floats * sizeof(float));
     return QKV_OK;
 }
 
@@ -390,7 +389,6 @@ int kv_decode_attn(const qkv_cache_desc* cache, const void* q, const void* k_new
     for (int i = 0; i < 4; ++i) p.quat[i] = cache->quat[i];
     uint8_t* ws = (uint8_t*)workspace;
     p.part1 = (float*)ws;
-    p.rec = (int*)(ws + L.off_rec);
     p.slot_floats = L.slot_floats;
     p.k_new = (const uint16_t*)k_new;
     p.v_new = (const uint16_t*)v_new;

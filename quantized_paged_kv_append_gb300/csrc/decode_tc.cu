@@ -162,6 +162,15 @@ __device__ __forceinline__ float warp_reduce8(const float (&v)[8], int lane) {
 __device__ __forceinline__ int seq_len_clamped(const DecodeParams& p, int b) {
     return max(0, min(p.seq_lens[b], p.max_pages * kPage));
 }
+// The same from an L2-only load (ld.global.cg: nothing is kept in L1), for the
+// speculative read before the dependency wait.
+__device__ __forceinline__ int seq_len_clamped_cg(const DecodeParams& p, int b) {
+    return max(0, min(__ldcg(p.seq_lens + b), p.max_pages * kPage));
+}
+__device__ __forceinline__ void prefetch_l1(const void* a) { asm volatile("prefetch.global.L1 [%0];" ::"l"(a)); }
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* m) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
 
 struct Piece {
     int b, hg, p0, p1, L;
@@ -172,9 +181,10 @@ struct Piece {
 struct Walker {
     int b;
     long long pref, x, end;
+    template <bool CG = false>
     __device__ bool next(const DecodeParams& p, Piece& pc) {
         while (x < end && b < p.B) {
-            const int L = seq_len_clamped(p, b);
+            const int L = CG ? seq_len_clamped_cg(p, b) : seq_len_clamped(p, b);
             const long long np = (L + kPage - 1) / kPage;
             const long long seg0 = pref * p.NH;
             if (np == 0 || x >= seg0 + np * p.NH) {
@@ -284,22 +294,18 @@ __global__ void __launch_bounds__(kThr, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    // inputs may come from the previous kernel in the stream (programmatic dependent launch)
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;");
-    if (tid == 0 && !p.rec_by_seg) p.rec[c * 8] = 0;   // this CTA closes no multi-piece segment (yet)
     // Every warp derives this CTA's share of the (sequence, head group, page) units from
     // seq_lens on its own, so no block-wide barrier follows the dependency wait and the
     // producers reach the page table one global load later.
-    int b0 = p.B;
-    long long pref0 = 0, Tunits;
-    {
+    auto compute_share = [&](auto len_of, bool flag_errors, int& b0, long long& pref0, long long& Tunits) {
+        b0 = p.B;
+        pref0 = 0;
         const int per = (p.B + 31) / 32;
         const int b_lo = min(p.B, lane * per), b_hi = min(p.B, b_lo + per);
         long long local = 0;
         for (int b = b_lo; b < b_hi; ++b) {
-            const int Lr = p.seq_lens[b];
-            if (warp == 0 && (Lr < 0 || Lr > p.max_pages * kPage)) atomicOr(&g_err_dtc, kErrPos);
+            const int Lr = len_of(b);
+            if (flag_errors && warp == 0 && (Lr < 0 || Lr > p.max_pages * kPage)) atomicOr(&g_err_dtc, kErrPos);
             local += (max(0, min(Lr, p.max_pages * kPage)) + kPage - 1) / kPage;
         }
         long long incl = local;
@@ -313,7 +319,7 @@ __global__ void __launch_bounds__(kThr, 1)
         long long pref = incl - local, fpref = 0;
         int fb = -1;
         for (int b = b_lo; b < b_hi; ++b) {
-            const long long np = (seq_len_clamped(p, b) + kPage - 1) / kPage;
+            const long long np = (max(0, min(len_of(b), p.max_pages * kPage)) + kPage - 1) / kPage;
             if (np > 0 && pref * p.NH <= beg && beg < (pref + np) * p.NH) {
                 fb = b;
                 fpref = pref;
@@ -326,7 +332,42 @@ __global__ void __launch_bounds__(kThr, 1)
             b0 = __shfl_sync(0xffffffffu, fb, src);
             pref0 = __shfl_sync(0xffffffffu, fpref, src);
         }
+    };
+    // Before the dependency wait: the share as seq_lens reads now (L2-only loads; the previous
+    // kernel may still change it), used for nothing but the addresses of the lines the first
+    // piece reads first, which are prefetched into L1 right after the wait (page-table row,
+    // query rows). Every value the kernel uses is loaded after the wait.
+    {
+        int b0s;
+        long long pref0s, Tus;
+        compute_share([&](int b) { return __ldcg(p.seq_lens + b); }, false, b0s, pref0s, Tus);
+        Piece spc;
+        bool shas = false;
+        if (warp == kWProd || warp == kWProdV || warp < kSoftW) {
+            Walker ws{b0s, pref0s, Tus * c / C, Tus * (c + 1) / C};
+            shas = ws.template next<true>(p, spc);
+        }
+        if (warp == kWProd && lane == 0) prefetch_tensormap(&tmK);
+        if (warp == kWProdV && lane == 0) prefetch_tensormap(&tmV);
+        // inputs may come from the previous kernel in the stream (programmatic dependent launch)
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        asm volatile("griddepcontrol.launch_dependents;");
+        if (shas) {
+            if ((warp == kWProd || warp == kWProdV) && lane < 4) {
+                const int32_t* row = p.page_table + (size_t)spc.b * p.max_pages;
+                const int pi = spc.p0 + min(spc.p1 - spc.p0 - 1, 31 * (lane & 1) + 32 * (lane >> 1));
+                prefetch_l1(row + pi);
+            } else if (warp < kSoftW) {
+                const int kvh = spc.hg / (p.Gtot / G), hgi = spc.hg % (p.Gtot / G);
+                const int hq0 = kvh * p.Gtot + hgi * G;
+                if (tid < G * D * 2 / 128)
+                    prefetch_l1(reinterpret_cast<const uint8_t*>(p.q + ((size_t)spc.b * p.Hq + hq0) * D) + 128 * tid);
+            }
+        }
     }
+    int b0;
+    long long pref0, Tunits;
+    compute_share([&](int b) { return p.seq_lens[b]; }, true, b0, pref0, Tunits);
     const long long beg = Tunits * c / C, end = Tunits * (c + 1) / C;
     auto cta_of = [&](long long x) -> long long { return ((x + 1) * C + Tunits - 1) / Tunits - 1; };
 
@@ -338,7 +379,6 @@ __global__ void __launch_bounds__(kThr, 1)
             const int kvh = hg / (p.Gtot / G), hgi = hg % (p.Gtot / G);
             const int hq0 = kvh * p.Gtot + hgi * G;
             for (int i = tid; i < G * D; i += kThr) write_out<D, G>(p, b, hq0, i, 0.0f);
-            if (tid == 0 && p.rec_by_seg) p.rec[s * 8] = 0;
         }
     }
     Walker walker{b0, pref0, beg, end};
@@ -525,10 +565,13 @@ __global__ void __launch_bounds__(kThr, 1)
                                                     qd0 + (uint64_t)((pass * NA * 2048 + (2 * gk + (u >> 2)) * 2048 + 32 * (u & 3)) >> 4),
                                                     IDQK, pass > 0 || u > 0);
                         } else {
+                            // k-step outer, scale group inner: consecutive MMAs write different
+                            // accumulators, so the tensor pipe overlaps them instead of waiting on
+                            // each accumulator's previous k-step
 #pragma unroll
-                            for (int g = 0; g < NA; ++g)
+                            for (int u = 0; u < 4; ++u)
 #pragma unroll
-                                for (int u = 0; u < 4; ++u)
+                                for (int g = 0; g < NA; ++g)
                                     umma_f16_ta(sd + 16 * g, tk + 8 * (4 * g + u), qd0 + (uint64_t)((g * 2048 + 32 * u) >> 4),
                                                 IDQK, u > 0);
                         }
@@ -1105,22 +1148,10 @@ __global__ void __launch_bounds__(kThr, 1)
                 }
             }
             tc_fence_before();
-            if (npieces == 1) {
-                if (r == 0 && p.rec_by_seg) p.rec[seg * 8] = 0;
-            } else {
-                // partial slot of this piece; the combine kernel merges the segment's slots
-                if (r < G) {
-                    mine[r] = sML[r];
-                    mine[8 + r] = sML[8 + r];
-                }
-                if (r == 0 && c == chi) {
-                    int* rc = p.rec + (p.rec_by_seg ? seg : (long long)c) * 8;
-                    rc[1] = (int)clo;
-                    rc[2] = (int)seg;
-                    rc[3] = pc.b;
-                    rc[4] = hq0;
-                    rc[0] = npieces;
-                }
+            if (npieces > 1 && r < G) {
+                // the partial slot's frame and row sum; the combine kernel merges the segment's slots
+                mine[r] = sML[r];
+                mine[8 + r] = sML[8 + r];
             }
             soft_sync();
             ++piece;
@@ -1137,25 +1168,103 @@ __global__ void __launch_bounds__(kThr, 1)
 // ---------------------------------------------------------------------------
 // combine: merge the partial slots of every segment split across CTAs.
 // Grid (G * D / 64, R): block (s, y) merges output floats [64 s, 64 s + 64) of
-// the segment in record y (records are per segment when there are no more
-// segments than decode CTAs, else per closing CTA), with the partial-softmax rule
-// M = max m_j, O = sum 2^(m_j - M) O_j / sum 2^(m_j - M) l_j (base-2 scores).
+// one segment -- segment y when there are no more segments than decode CTAs,
+// else the multi-piece segment that decode CTA y closes (if any) -- with the
+// partial-softmax rule M = max m_j, O = sum 2^(m_j - M) O_j / sum 2^(m_j - M) l_j
+// (base-2 scores). Which CTAs hold the segment's pieces follows from seq_lens
+// alone (the decode grid's split is a pure function of it), so it is worked
+// out before the dependency wait and the merge needs one round of loads after it.
 // ---------------------------------------------------------------------------
 constexpr int kCombThr = 128;
 constexpr int kMaxGrid = 256;   // decode CTAs (pieces of one segment) the combine step can merge
+constexpr int kMaxBatchDec = 1024;
 
 template <int D, int G>
 __global__ void __launch_bounds__(kCombThr) decode_tc_combine(const DecodeParams p) {
     __shared__ float s_w[kMaxGrid], s_l[kMaxGrid];
     __shared__ float4 s_acc[8][16];
     __shared__ float s_red[8];
+    __shared__ long long s_pref[kMaxBatchDec + 1];   // pages of the sequences before b
+    __shared__ long long s_wsum[kCombThr / 32];
+    __shared__ int s_info[5];
+    const int t = threadIdx.x;
+    // ---- before the dependency wait: the segment and its pieces, from seq_lens (an input
+    // of the decode grid that it does not write) ----
+    {
+        const int per = (p.B + kCombThr - 1) / kCombThr;
+        const int b_lo = min(p.B, t * per), b_hi = min(p.B, b_lo + per);
+        long long loc = 0;
+        for (int b = b_lo; b < b_hi; ++b) loc += (seq_len_clamped(p, b) + kPage - 1) / kPage;
+        long long incl = loc;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const long long v = __shfl_up_sync(0xffffffffu, incl, off);
+            if ((t & 31) >= off) incl += v;
+        }
+        if ((t & 31) == 31) s_wsum[t >> 5] = incl;
+        __syncthreads();
+        long long pref = incl - loc, total = 0;
+        for (int w = 0; w < kCombThr / 32; ++w) {
+            if (w < (t >> 5)) pref += s_wsum[w];
+            total += s_wsum[w];
+        }
+        for (int b = b_lo; b < b_hi; ++b) {
+            s_pref[b] = pref;
+            pref += (seq_len_clamped(p, b) + kPage - 1) / kPage;
+        }
+        if (t == 0) s_pref[p.B] = total;
+        __syncthreads();
+        if (t == 0) {
+            const long long Tunits = total * p.NH, C = p.ctas;
+            auto cta_of = [&](long long x) -> long long { return ((x + 1) * C + Tunits - 1) / Tunits - 1; };
+            int n = 0, clo = 0, seg = 0, hg = 0, b = 0;
+            if (p.rec_by_seg) {
+                seg = blockIdx.y;
+                b = seg / p.NH;
+                hg = seg % p.NH;
+                const long long np = s_pref[b + 1] - s_pref[b];
+                if (np > 0) {
+                    const long long soff = s_pref[b] * p.NH + hg * np;
+                    clo = (int)cta_of(soff);
+                    n = (int)(cta_of(soff + np - 1) - clo + 1);
+                }
+            } else if (Tunits > 0) {
+                // the segment holding this CTA's first unit, if it started in an earlier CTA and
+                // ends in this one (a CTA closes at most one multi-piece segment)
+                const long long c = blockIdx.y, beg = Tunits * c / C, end = Tunits * (c + 1) / C;
+                if (beg < end) {
+                    int lo = 0, hi = p.B - 1;   // first b with s_pref[b + 1] * NH > beg
+                    while (lo < hi) {
+                        const int mid = (lo + hi) >> 1;
+                        if (s_pref[mid + 1] * p.NH > beg) hi = mid;
+                        else lo = mid + 1;
+                    }
+                    b = lo;
+                    const long long np = s_pref[b + 1] - s_pref[b];
+                    hg = (int)((beg - s_pref[b] * p.NH) / np);
+                    const long long soff = s_pref[b] * p.NH + (long long)hg * np;
+                    if (soff < beg && soff + np <= end) {
+                        clo = (int)cta_of(soff);
+                        n = (int)(c - clo + 1);
+                        seg = b * p.NH + hg;
+                    }
+                }
+            }
+            const int kvh = hg / (p.Gtot / G), hgi = hg % (p.Gtot / G);
+            s_info[0] = n;
+            s_info[1] = clo;
+            s_info[2] = seg;
+            s_info[3] = b;
+            s_info[4] = kvh * p.Gtot + hgi * G;
+        }
+        __syncthreads();
+    }
     asm volatile("griddepcontrol.wait;" ::: "memory");   // the decode grid has completed
     asm volatile("griddepcontrol.launch_dependents;");
-    const int* rc = p.rec + blockIdx.y * 8;
-    const int n = rc[0];
+    const int n = s_info[0];
     if (n < 2) return;
-    const int clo = rc[1], seg = rc[2], b = rc[3], hq0 = rc[4];
-    const int t = threadIdx.x, s = blockIdx.x;
+    const int clo = s_info[1], seg = s_info[2], b = s_info[3], hq0 = s_info[4];
+    const int s = blockIdx.x;
     const int f0 = 64 * s, h = f0 / D;
     auto slot = [&](int j) { return p.part1 + (size_t)(clo + j + seg) * p.slot_floats; };
     // O loads first (independent of the weights): thread -> float4 e, slots j = sg, sg + 8, ...
@@ -1239,7 +1348,7 @@ cudaError_t decode_tc_upload_levels(const float* lv3, const float* lv4) {
 }
 
 int decode_heads_per_cta(int Gtot) { return Gtot >= 8 ? 8 : Gtot; }
-int decode_max_batch() { return 1024; }
+int decode_max_batch() { return kMaxBatchDec; }
 
 cudaError_t decode_tc_read_error(unsigned* out, bool clear) {
     cudaError_t e = cudaMemcpyFromSymbol(out, g_err_dtc, sizeof(unsigned));
@@ -1256,6 +1365,7 @@ static cudaError_t launch_tc(int grid, const CUtensorMap& tk, const CUtensorMap&
                              cudaStream_t st) {
     DecodeParams p = p_in;
     p.rec_by_seg = (long long)p.B * p.NH <= grid;
+    p.ctas = grid;
     using X = TG<D, FMT>;
     auto fn = decode_tc_kernel<D, G, FMT>;
     static bool configured[kMaxDevices];   // this instantiation's attribute, per device

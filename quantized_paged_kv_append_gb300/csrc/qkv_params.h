@@ -37,8 +37,8 @@ struct DecodeParams {
     float quat[4];
     float* part1;        // (C + S) partial slots: m[8], l[8], O[8][D] per piece
     int slot_floats;     // 16 + 8 * D
-    int* rec;            // [max(C, S)][8]: multi-piece segment records for the merge
-    int rec_by_seg;      // records indexed by segment (when segments <= CTAs), else by the closing CTA
+    int rec_by_seg;      // merge blocks indexed by segment (when segments <= CTAs), else by the closing CTA
+    int ctas;            // CTAs of the decode grid (the split of the units follows from it and seq_lens)
     const uint16_t* k_new;   // optional bf16 [B][Hkv][D]: quantize-on-write of position seq_lens[b] - 1
     const uint16_t* v_new;
 };
