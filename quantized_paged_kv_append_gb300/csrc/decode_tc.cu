@@ -168,6 +168,10 @@ __device__ __forceinline__ int seq_len_clamped_cg(const DecodeParams& p, int b) 
     return max(0, min(__ldcg(p.seq_lens + b), p.max_pages * kPage));
 }
 __device__ __forceinline__ void prefetch_l1(const void* a) { asm volatile("prefetch.global.L1 [%0];" ::"l"(a)); }
+// bytes (a multiple of 16) at a 16-byte aligned global address into L2; no data is returned
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
@@ -334,35 +338,54 @@ __global__ void __launch_bounds__(kThr, 1)
         }
     };
     // Before the dependency wait: the share as seq_lens reads now (L2-only loads; the previous
-    // kernel may still change it), used for nothing but the addresses of the lines the first
-    // piece reads first, which are prefetched into L1 right after the wait (page-table row,
-    // query rows). Every value the kernel uses is loaded after the wait.
+    // kernel may still change it). It serves addresses only: the producers prefetch the first
+    // two tiles' pages into L2 (a prefetch returns no data, so a later write by the previous
+    // kernel is still what the copies after the wait read) and, after the wait, load the page
+    // ids of the first piece at once; those are kept only if the piece that the share read
+    // after the wait gives is the same. Every value the kernel uses is loaded after the wait.
+    Piece spc;
+    spc.b = -1;
+    int spid_cur = 0, spid_nxt = 0;
     {
         int b0s;
         long long pref0s, Tus;
         compute_share([&](int b) { return __ldcg(p.seq_lens + b); }, false, b0s, pref0s, Tus);
-        Piece spc;
         bool shas = false;
         if (warp == kWProd || warp == kWProdV || warp < kSoftW) {
             Walker ws{b0s, pref0s, Tus * c / C, Tus * (c + 1) / C};
             shas = ws.template next<true>(p, spc);
         }
-        if (warp == kWProd && lane == 0) prefetch_tensormap(&tmK);
-        if (warp == kWProdV && lane == 0) prefetch_tensormap(&tmV);
+        if (shas && (warp == kWProd || warp == kWProdV)) {
+            const int kind = warp == kWProdV ? 1 : 0;
+            if (lane == 0) prefetch_tensormap(kind ? &tmV : &tmK);
+            const int npf = min(2 * kTP, spc.p1 - spc.p0);
+            if (lane < npf) {
+                const int pid = __ldcg(p.page_table + (size_t)spc.b * p.max_pages + spc.p0 + lane);
+                if (pid >= 0 && pid < p.num_pages) {
+                    const int rowb = kind ? X::VROW : X::KROW, scrow = kind ? X::VSROW : X::KSROW;
+                    const long long prow = ((long long)pid * p.Hkv + spc.hg / (p.Gtot / G)) * kPage;
+                    bulk_prefetch_l2((kind ? p.vc : p.kc) + prow * rowb, kPage * rowb);
+                    bulk_prefetch_l2((kind ? p.vs : p.ks) + prow * scrow, kPage * scrow);
+                }
+            }
+        }
         // inputs may come from the previous kernel in the stream (programmatic dependent launch)
         asm volatile("griddepcontrol.wait;" ::: "memory");
         asm volatile("griddepcontrol.launch_dependents;");
         if (shas) {
-            if ((warp == kWProd || warp == kWProdV) && lane < 4) {
-                const int32_t* row = p.page_table + (size_t)spc.b * p.max_pages;
-                const int pi = spc.p0 + min(spc.p1 - spc.p0 - 1, 31 * (lane & 1) + 32 * (lane >> 1));
-                prefetch_l1(row + pi);
+            if (warp == kWProd || warp == kWProdV) {
+                const int32_t* row = p.page_table + (size_t)spc.b * p.max_pages + spc.p0;
+                const int npc = spc.p1 - spc.p0;
+                spid_cur = lane < npc ? row[lane] : 0;
+                spid_nxt = 32 + lane < npc ? row[32 + lane] : 0;
             } else if (warp < kSoftW) {
                 const int kvh = spc.hg / (p.Gtot / G), hgi = spc.hg % (p.Gtot / G);
                 const int hq0 = kvh * p.Gtot + hgi * G;
                 if (tid < G * D * 2 / 128)
                     prefetch_l1(reinterpret_cast<const uint8_t*>(p.q + ((size_t)spc.b * p.Hq + hq0) * D) + 128 * tid);
             }
+        } else {
+            spc.b = -1;
         }
     }
     int b0;
@@ -402,14 +425,23 @@ __global__ void __launch_bounds__(kThr, 1)
         const uint8_t* codes = kind ? p.vc : p.kc;
         uint32_t T = 0, pat_phase = 0;
         Piece pc;
+        bool first = true;
         while (walker.next(p, pc)) {
             const int kvh = pc.hg / (p.Gtot / G);
             const int32_t* ptrow = p.page_table + (size_t)pc.b * p.max_pages;
             const int last_page = (pc.L - 1) / kPage;
             const int npc = pc.p1 - pc.p0;
             int bc = 0;
-            int pid_cur = lane < npc ? ptrow[pc.p0 + lane] : 0;
-            int pid_nxt = 32 + lane < npc ? ptrow[pc.p0 + 32 + lane] : 0;
+            int pid_cur, pid_nxt;
+            if (first && pc.b == spc.b && pc.p0 == spc.p0 && pc.p1 == spc.p1) {
+                // the same addresses as the page ids loaded right after the wait
+                pid_cur = spid_cur;
+                pid_nxt = spid_nxt;
+            } else {
+                pid_cur = lane < npc ? ptrow[pc.p0 + lane] : 0;
+                pid_nxt = 32 + lane < npc ? ptrow[pc.p0 + 32 + lane] : 0;
+            }
+            first = false;
             for (int pg0 = pc.p0; pg0 < pc.p1; pg0 += kTP, ++T) {
                 const int npg = min(kTP, pc.p1 - pg0);
                 const int buf = T & 1;
@@ -1188,6 +1220,9 @@ __global__ void __launch_bounds__(kCombThr) decode_tc_combine(const DecodeParams
     __shared__ long long s_wsum[kCombThr / 32];
     __shared__ int s_info[5];
     const int t = threadIdx.x;
+    // The next kernel in the stream may be scheduled now: it does its own set-up while this
+    // grid waits, and waits for this grid to complete before it reads anything.
+    asm volatile("griddepcontrol.launch_dependents;");
     // ---- before the dependency wait: the segment and its pieces, from seq_lens (an input
     // of the decode grid that it does not write) ----
     {
@@ -1260,7 +1295,6 @@ __global__ void __launch_bounds__(kCombThr) decode_tc_combine(const DecodeParams
         __syncthreads();
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");   // the decode grid has completed
-    asm volatile("griddepcontrol.launch_dependents;");
     const int n = s_info[0];
     if (n < 2) return;
     const int clo = s_info[1], seg = s_info[2], b = s_info[3], hq0 = s_info[4];
