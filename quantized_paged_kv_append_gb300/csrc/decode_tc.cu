@@ -85,7 +85,9 @@ struct TG {
     static constexpr int VBOX = VPAGE_B / 2048;   // 128-byte TMA boxes per V page (int8, q4)
     static constexpr int SC_B = kPage * KSROW;    // staged K scales of one page
     static constexpr int VSC_B = kPage * VSROW;   // staged V scales of one page
-    static constexpr int QT = ISO ? 2 : 1;        // query tiles: the rotated query needs fp16 hi + lo
+    static constexpr int QT = 1;                  // query tile (ISO: the rotated query as fp16 hi rows 0..7, lo rows 8..15)
+    static constexpr int SACC = ISO ? 2 : 1;      // score accumulators per K scale group (ISO: even / odd k-steps)
+    static constexpr int SBUF = NKG * SACC * 16;  // TMEM columns of one score buffer
     static constexpr int LUT_N = FMT == 2 ? 64 : FMT == 3 ? 256 : 0;   // code pair -> fp16 level pair
     static constexpr int OFF_KST = 0;                               // [2][8][PAGE_B]
     static constexpr int OFF_VST = OFF_KST + 2 * kTP * PAGE_B;      // [2][8][VPAGE_B]
@@ -102,8 +104,8 @@ struct TG {
     static constexpr int OFF_MISC = OFF_BAR + 32 * 8;
     static constexpr int SMEM = OFF_MISC + 64;
     static constexpr int KCOL = 0;                     // K' columns: D / 2 (fp16 pairs)
-    static constexpr int SCOL = D / 2;                 // two score buffers of NKG x 16 columns
-    static constexpr int OCOL = SCOL + 2 * NKG * 16;   // O (M = 64 rows in lanes 32 (r / 16) + r % 16, N = D)
+    static constexpr int SCOL = D / 2;                 // two score buffers of SBUF columns
+    static constexpr int OCOL = SCOL + 2 * SBUF;       // O (M = 64 rows in lanes 32 (r / 16) + r % 16, N = D)
     static constexpr int TCOLS = (OCOL + D) <= 256 ? 256 : 512;
     static_assert(OCOL + D <= 512, "TMEM budget");
     static_assert(SMEM + 1024 <= 232448 - 1024, "shared memory budget");
@@ -583,19 +585,18 @@ __global__ void __launch_bounds__(kThr, 1)
                     if (ready && first) ready = mbar_test_wait(&bars[B_QRD], pieceq & 1);
                     if (ready) {
                         tc_fence_after();
-                        const uint32_t sd = tmem + X::SCOL + (Tq & 1) * X::NKG * 16;
+                        const uint32_t sd = tmem + X::SCOL + (Tq & 1) * X::SBUF;
                         if constexpr (X::ISO) {
-                            // per 128-dim block: 8 k-steps with the rotated query's fp16 hi part,
-                            // then 8 with its lo part, into the block's one accumulator
+                            // per 128-dim block: 8 k-steps against the query tile whose N columns hold
+                            // the rotated query's fp16 hi (0..7) and lo (8..15) parts; even and odd
+                            // k-steps go to two accumulators, so consecutive MMAs are independent
 #pragma unroll
-                            for (int gk = 0; gk < X::NKG; ++gk)
+                            for (int u = 0; u < 8; ++u)
 #pragma unroll
-                                for (int pass = 0; pass < 2; ++pass)
-#pragma unroll
-                                    for (int u = 0; u < 8; ++u)
-                                        umma_f16_ta(sd + 16 * gk, tk + 8 * (8 * gk + u),
-                                                    qd0 + (uint64_t)((pass * NA * 2048 + (2 * gk + (u >> 2)) * 2048 + 32 * (u & 3)) >> 4),
-                                                    IDQK, pass > 0 || u > 0);
+                                for (int gk = 0; gk < X::NKG; ++gk)
+                                    umma_f16_ta(sd + 32 * gk + 16 * (u & 1), tk + 8 * (8 * gk + u),
+                                                qd0 + (uint64_t)(((2 * gk + (u >> 2)) * 2048 + 32 * (u & 3)) >> 4),
+                                                IDQK, u > 1);
                         } else {
                             // k-step outer, scale group inner: consecutive MMAs write different
                             // accumulators, so the tensor pipe overlaps them instead of waiting on
@@ -817,9 +818,11 @@ __global__ void __launch_bounds__(kThr, 1)
             // ---- query tile (B operand, K-major, dims in converter order) and the offset sums ----
             {
                 uint8_t* qsm = sm + X::OFF_Q;
-                for (int idx = r; idx < 16 * NA * 8; idx += 128) {
+                // ISO: rows n < 8 take the rotated query's fp16 hi part, rows 8 + n its lo part
+                constexpr int QROWS = X::ISO ? 8 : 16;
+                for (int idx = r; idx < QROWS * NA * 8; idx += 128) {
                     const int n = idx / (NA * 8), rem = idx % (NA * 8), a = rem >> 3, cc = rem & 7;
-                    uint32_t w[4] = {0u, 0u, 0u, 0u};
+                    uint32_t w[4] = {0u, 0u, 0u, 0u}, wl[4] = {0u, 0u, 0u, 0u};
                     if (n < G) {
                         const uint16_t* qrow = p.q + ((size_t)pc.b * p.Hq + hq0 + n) * D + 64 * a + 8 * cc;
                         const uint4 raw = *reinterpret_cast<const uint4*>(qrow);
@@ -848,19 +851,17 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll
                         for (int k = 0; k < 4; ++k) w[k] = f32x2_to_h2(v[2 * k], v[2 * k + 1]);
                         if constexpr (X::ISO) {
-                            // the fp16 remainder of the rotated query: a second (lo) tile
-                            uint32_t wl[4];
+                            // the fp16 remainder of the rotated query
 #pragma unroll
                             for (int k = 0; k < 4; ++k) {
                                 const float2 f = h2_to_f32x2(w[k]);
                                 wl[k] = f32x2_to_h2(v[2 * k] - f.x, v[2 * k + 1] - f.y);
                             }
-                            *reinterpret_cast<uint4*>(qsm + (NA + a) * 2048 + sw_off(n, cc)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
                         }
-                    } else if constexpr (X::ISO) {
-                        *reinterpret_cast<uint4*>(qsm + (NA + a) * 2048 + sw_off(n, cc)) = make_uint4(0u, 0u, 0u, 0u);
                     }
                     *reinterpret_cast<uint4*>(qsm + a * 2048 + sw_off(n, cc)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    if constexpr (X::ISO)
+                        *reinterpret_cast<uint4*>(qsm + a * 2048 + sw_off(8 + n, cc)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
                 }
                 // 1152 * (sum of the fp16 query over each 64-dim group): thread -> (head, D / 16 dims)
                 constexpr int DPT = D / 16, TPG = 64 / DPT;
@@ -918,9 +919,17 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll
                 for (int g = 0; g < X::NKG; ++g) {
                     float v[16];
-                    tmem_ld16(tmem + lb + X::SCOL + buf * X::NKG * 16 + 16 * g, v);
+                    tmem_ld16(tmem + lb + X::SCOL + buf * X::SBUF + 16 * X::SACC * g, v);
+                    if constexpr (X::ISO) {
+                        // hi + lo columns of the even k-steps, then of the odd ones
+                        float v2[16];
+                        tmem_ld16(tmem + lb + X::SCOL + buf * X::SBUF + 16 * X::SACC * g + 16, v2);
 #pragma unroll
-                    for (int h = 0; h < G; ++h) s[h] += X::ISO ? ks[g] * v[h] : ks[g] * (v[h] - bias[g][h]);
+                        for (int h = 0; h < G; ++h) s[h] += ks[g] * ((v[h] + v[8 + h]) + (v2[h] + v2[8 + h]));
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < G; ++h) s[h] += ks[g] * (v[h] - bias[g][h]);
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();
