@@ -672,6 +672,9 @@ EXTEND_CONFIGS = {
     "extend_k8v4": ("k8v4", 16, 2, 256),
     "extend_iso3": ("iso3", 16, 4, 128),
     "extend_iso4": ("iso4", 16, 4, 128),
+    # ISO at head_dim 256 (two 128-value blocks per head), the int8 decode shape
+    "extend_iso3_d256": ("iso3", 16, 2, 256),
+    "extend_iso4_d256": ("iso4", 16, 2, 256),
 }
 
 

@@ -178,9 +178,8 @@ QKV_API int kv_decode_attn(const qkv_cache_desc* cache, const void* q, const voi
  * keys and values into it (fp16 planes, read by the attention kernel with TMA);
  * calls sharing a workspace must not overlap in time. A chunk longer than
  * max_q_len sets the position bit of qkv_device_error and is cut at max_q_len.
- * Formats: int8 (head_dim 128 or 256), k8v4 (256), ISO3 / ISO4 (128; head_dim
- * 256 returns QKV_ERR_UNSUPPORTED), with num_q_heads / num_kv_heads in {1, 2,
- * 4} or a multiple of 8. V is dequantized into the original domain first (k8v4
+ * Formats: int8 (head_dim 128 or 256), k8v4 (256), ISO3 / ISO4 (128 or 256),
+ * with num_q_heads / num_kv_heads in {1, 2, 4} or a multiple of 8. V is dequantized into the original domain first (k8v4
  * rotated back by the FWHT-256, ISO by the conjugate quaternion), so the output
  * needs no transform; ISO keys stay as their levels and the prefix tiles take
  * the query rotated by the pool quaternion.

@@ -420,8 +420,6 @@ int kv_extend_attn(const qkv_cache_desc* cache, const void* q, const void* k_new
     if (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads) return QKV_ERR_GQA;
     const int Gtot = num_q_heads / cache->num_kv_heads;
     if (!(Gtot == 1 || Gtot == 2 || Gtot == 4 || Gtot % 8 == 0)) return QKV_ERR_GQA;
-    // ISO prefixes take the rotated query as two extra fp16 tiles, which fit in shared memory at head_dim 128
-    if ((cache->format == QKV_ISO3 || cache->format == QKV_ISO4) && cache->head_dim != 128) return QKV_ERR_UNSUPPORTED;
     ExtendLayout XL;
     if ((rc = extend_layout(cache, batch, max_q_len, max_pages_per_seq, &XL))) return rc;
     if (!workspace || workspace_bytes < XL.bytes || ((uintptr_t)workspace & 255u)) return QKV_ERR_WORKSPACE;

@@ -48,25 +48,29 @@ constexpr int kXSoft = 128 * kXSplit;      // softmax warps: row r = lane + 32 (
 constexpr int kXThreads = kXSoft + 96;     // + 2 producer warps (K, V) + 1 MMA warp
 constexpr int kXProd = kXSoft / 32, kXMma = kXProd + 2;
 
-// shared-memory map (bytes from a 1 KB aligned base). ISO adds the rotated query of
-// the prefix tiles as two fp16 tiles (hi, and the fp16 remainder lo) after the rest.
+// shared-memory map (bytes from a 1 KB aligned base). ISO prefix tiles take the rotated
+// query as two fp16 tiles: hi in the query region (which holds the plain query once the
+// prefix is done) and the fp16 remainder lo in one more tile after the rest.
 template <int D, bool ISO = false>
 struct XGeo {
     static constexpr int NA = D / 64;                    // 64-dim atoms (= K scale groups)
     static constexpr int OFF_Q = 0;                      // NA atoms x 128 rows x 128 B
     static constexpr int Q_BYTES = NA * 128 * 128;
-    static constexpr int OFF_K = OFF_Q + Q_BYTES;        // 2 buffers x NA atoms x 64 rows x 128 B
+    // K and V staging depth: two tiles, one for ISO at head_dim 256 (where the rotated query's
+    // lo tile takes the room of the second K and V buffers)
+    static constexpr int NB = (ISO && D == 256) ? 1 : 2;
+    static constexpr int OFF_K = OFF_Q + Q_BYTES;        // NB buffers x NA atoms x 64 rows x 128 B
     static constexpr int K_BYTES = NA * 64 * 128;
-    static constexpr int OFF_V = OFF_K + 2 * K_BYTES;    // 2 buffers x D rows x 128 B
+    static constexpr int OFF_V = OFF_K + NB * K_BYTES;   // NB buffers x D rows x 128 B
     static constexpr int V_BYTES = D * 128;
-    static constexpr int OFF_P = OFF_V + 2 * V_BYTES;    // 128 rows x 128 B
+    static constexpr int OFF_P = OFF_V + NB * V_BYTES;   // 128 rows x 128 B
     static constexpr int KS_BYTES = kXT * NA * 4;        // fp32 K scales x softmax scale of a tile [64][NA]
-    static constexpr int OFF_KS = OFF_P + 128 * 128;     // 2 buffers
-    static constexpr int OFF_RED = OFF_KS + 2 * KS_BYTES;   // [2 tiles][kXSplit parts][128 rows] row-max / row-sum exchange
+    static constexpr int OFF_KS = OFF_P + 128 * 128;     // NB buffers
+    static constexpr int OFF_RED = OFF_KS + NB * KS_BYTES;   // [2 tiles][kXSplit parts][128 rows] row-max / row-sum exchange
     static constexpr int OFF_BAR = OFF_RED + 2 * kXSplit * 128 * 4;
     static constexpr int OFF_TMEM = OFF_BAR + 24 * 8;
-    static constexpr int OFF_QR = (OFF_TMEM + 16 + 1023) / 1024 * 1024;   // ISO: [hi, lo] x Q_BYTES
-    static constexpr int SMEM = ISO ? OFF_QR + 2 * Q_BYTES : OFF_TMEM + 16;
+    static constexpr int OFF_QR = (OFF_TMEM + 16 + 1023) / 1024 * 1024;   // ISO: the lo tile (Q_BYTES)
+    static constexpr int SMEM = ISO ? OFF_QR + Q_BYTES : OFF_TMEM + 16;
     static constexpr int S_COLS = NA * 64;               // TMEM columns of the group scores
     static constexpr int TMEM_COLS = 512;
     static_assert(S_COLS + D <= TMEM_COLS, "TMEM budget");
@@ -83,7 +87,8 @@ enum {
     B_SFULL = 9, B_SFREE = 10, B_PFULL = 11, B_PVDONE = 12,
     B_RMX = 13,   // [2] row maxima of every key part written (all softmax threads)
     B_RSUM = 15,  // row sums of every part written
-    B_DRAIN = 16  // every MMA of the CTA complete (commit), before TMEM is released
+    B_DRAIN = 16, // every MMA of the CTA complete (commit), before TMEM is released
+    B_QPLAIN = 17 // ISO: the plain query replaced the rotated hi tile (all softmax threads)
 };
 
 __device__ __forceinline__ uint32_t bf16x2_to_h2(uint32_t w) {
@@ -103,7 +108,7 @@ __device__ __forceinline__ uint32_t bf16x2_to_h2(uint32_t w) {
 //   1 k8v4 : K as int8. V: the q4_0 values (q - 8) * d of the FWHT-rotated row,
 //            rotated back with the same transform (H / 16 is its own inverse) in
 //            fp32 across the four threads of the row, then rounded to fp16 once.
-//   2, 3 ISO3 / ISO4 (head_dim 128): K' = the Lloyd-Max levels c (exact in
+//   2, 3 ISO3 / ISO4 (head_dim 128 or 256): K' = the Lloyd-Max levels c (exact in
 //            fp16) with the block's fp16 norm as the key scale of both its
 //            64-dim groups; the attention kernel rotates the query for these
 //            tiles. V: each 4-D group rotated back, u = conj(q) (x) c in fp32,
@@ -337,7 +342,6 @@ template <int D, int G, bool ISO>
 __global__ void __launch_bounds__(kXThreads, 1)
     extend_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const ExtendParams p) {
     using X = XGeo<D, ISO>;
-    static_assert(!ISO || D == 128, "the rotated query tiles fit in shared memory at head_dim 128");
     constexpr int NA = X::NA;
     constexpr int TPT = 128 / G;   // tokens per tile
     extern __shared__ __align__(1024) uint8_t xsmem_raw[];
@@ -382,6 +386,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
         mbar_init(&bars[B_RMX + 1], kXSoft);
         mbar_init(&bars[B_RSUM], kXSoft);
         mbar_init(&bars[B_DRAIN], 1);
+        mbar_init(&bars[B_QPLAIN], kXSoft);
         fence_mbar_init();
     }
     tc_fence_before();
@@ -407,8 +412,8 @@ __global__ void __launch_bounds__(kXThreads, 1)
             const int full0 = isk ? B_KF : B_VF, empty0 = isk ? B_KE : B_VE;
             int j = 0;
             for (; j < NT && ok; ++j) {
-                const int buf = j & 1;
-                if (j >= 2) wait(empty0 + buf, ((j - 2) >> 1) & 1);
+                const int buf = j % X::NB;
+                if (j >= X::NB) wait(empty0 + buf, ((j - X::NB) / X::NB) & 1);
                 uint64_t* bar = &bars[full0 + buf];
                 const int krow0 = hrow * p.Lmax + kXT * j;
                 if (isk) {
@@ -423,7 +428,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
                 }
             }
             // every copy issued above has landed before the CTA exits
-            for (int t = (j >= 2 ? j - 2 : 0); t < j; ++t) wait(full0 + (t & 1), (t >> 1) & 1);
+            for (int t = (j >= X::NB ? j - X::NB : 0); t < j; ++t) wait(full0 + t % X::NB, (t / X::NB) & 1);
         }
         __syncwarp();
     } else if (warp == kXMma) {
@@ -432,13 +437,13 @@ __global__ void __launch_bounds__(kXThreads, 1)
             const uint32_t qs = smem_addr(sm + X::OFF_Q);
             constexpr uint32_t IDQK = idesc_f16(128, 64), IDPV = idesc_f16(128, D);
             auto issue_qk = [&](int j) {
-                const int buf = j & 1;
-                wait(B_KF + buf, (j >> 1) & 1);
+                const int buf = j % X::NB;
+                wait(B_KF + buf, (j / X::NB) & 1);
                 if (j >= 1) wait(B_SFREE, (j - 1) & 1);
                 tc_fence_after();
                 const uint32_t ks = smem_addr(sm + X::OFF_K + buf * X::K_BYTES);
                 if (ISO && j < NTP) {
-                    // prefix tile: rotated query, hi then lo into the same accumulator
+                    // prefix tile: rotated query, hi (query region) then lo into the same accumulator
                     const uint32_t qr = smem_addr(sm + X::OFF_QR);
 #pragma unroll
                     for (int g = 0; g < NA; ++g)
@@ -446,9 +451,14 @@ __global__ void __launch_bounds__(kXThreads, 1)
                         for (int hl = 0; hl < 2; ++hl)
 #pragma unroll
                             for (int u = 0; u < 4; ++u)
-                                umma_f16(tmem_S + 64 * g, sw128_desc(qr + hl * X::Q_BYTES + g * 16384 + 32 * u),
+                                umma_f16(tmem_S + 64 * g, sw128_desc((hl ? qr : qs) + g * 16384 + 32 * u),
                                          sw128_desc(ks + g * 8192 + 32 * u), IDQK, (hl | u) > 0);
                 } else {
+                    // ISO: the first chunk tile needs the plain query back in the query region
+                    if (ISO && j == NTP && NTP > 0) {
+                        wait(B_QPLAIN, 0);
+                        tc_fence_after();
+                    }
 #pragma unroll
                     for (int g = 0; g < NA; ++g)
 #pragma unroll
@@ -463,14 +473,14 @@ __global__ void __launch_bounds__(kXThreads, 1)
             for (int j = 0; j < NT && ok; ++j) {
                 if (j + 1 < NT) issue_qk(j + 1);
                 wait(B_PFULL, j & 1);
-                wait(B_VF + (j & 1), (j >> 1) & 1);
+                wait(B_VF + j % X::NB, (j / X::NB) & 1);
                 tc_fence_after();
                 const uint32_t ps = smem_addr(sm + X::OFF_P);
-                const uint32_t vs = smem_addr(sm + X::OFF_V + (j & 1) * X::V_BYTES);
+                const uint32_t vs = smem_addr(sm + X::OFF_V + (j % X::NB) * X::V_BYTES);
 #pragma unroll
                 for (int u = 0; u < kXT / 16; ++u)
                     umma_f16(tmem_O, sw128_desc(ps + 32 * u), sw128_desc(vs + 32 * u), IDPV, (j > 0 || u > 0));
-                umma_commit(&bars[B_VE + (j & 1)]);
+                umma_commit(&bars[B_VE + j % X::NB]);
                 umma_commit(&bars[B_PVDONE]);
             }
             // A wait that ran out ends the loop early, possibly with MMAs still in flight:
@@ -491,18 +501,20 @@ __global__ void __launch_bounds__(kXThreads, 1)
         const int tokc = min(tok, T - 1);
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         float* red = reinterpret_cast<float*>(sm + X::OFF_RED);   // [2][128]
-        {
-            // Q tile row r = (token r / G, head r % G), bf16 -> fp16; this thread: a part of the dims
-            const uint16_t* qrow = p.q + ((size_t)(cu0 + tokc) * p.Hq + hq) * D;
+        // Q tile row r = (token r / G, head r % G), bf16 -> fp16; this thread: a part of the dims.
+        // ISO with a prefix: the rotated query's fp16 hi part goes to the query region and its lo
+        // part to the extra tile; the plain query replaces hi once the prefix tiles are done.
+        const uint16_t* qrow = p.q + ((size_t)(cu0 + tokc) * p.Hq + hq) * D;
+        auto write_query = [&](bool rotated) {
             uint8_t* qs = sm + X::OFF_Q;
 #pragma unroll 4
             for (int c = part * (D / 8 / kXSplit); c < (part + 1) * (D / 8 / kXSplit); ++c) {
                 uint4 o = make_uint4(0, 0, 0, 0);
-                uint4 ohi = o, olo = o;
+                uint4 olo = o;
                 if (rvalid) {
                     const uint4 w = *reinterpret_cast<const uint4*>(qrow + 8 * c);
                     o = make_uint4(bf16x2_to_h2(w.x), bf16x2_to_h2(w.y), bf16x2_to_h2(w.z), bf16x2_to_h2(w.w));
-                    if constexpr (ISO) {
+                    if (ISO && rotated) {
                         // R q_h per 4-D group (left Hamilton product by the pool quaternion) in fp32,
                         // then hi = fp16(v), lo = fp16(v - hi)
                         const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
@@ -525,26 +537,24 @@ __global__ void __launch_bounds__(kXThreads, 1)
                             const float2 f = h2_to_f32x2(hi[k]);
                             lo[k] = f32x2_to_h2(y[2 * k] - f.x, y[2 * k + 1] - f.y);
                         }
-                        ohi = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                        o = make_uint4(hi[0], hi[1], hi[2], hi[3]);
                         olo = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                     }
                 }
                 *reinterpret_cast<uint4*>(qs + (c >> 3) * 16384 + sw_off(r, c & 7)) = o;
-                if constexpr (ISO) {
-                    uint8_t* qr = sm + X::OFF_QR;
-                    *reinterpret_cast<uint4*>(qr + (c >> 3) * 16384 + sw_off(r, c & 7)) = ohi;
-                    *reinterpret_cast<uint4*>(qr + X::Q_BYTES + (c >> 3) * 16384 + sw_off(r, c & 7)) = olo;
-                }
+                if (ISO && rotated)
+                    *reinterpret_cast<uint4*>(sm + X::OFF_QR + (c >> 3) * 16384 + sw_off(r, c & 7)) = olo;
             }
             fence_proxy_async();
-            mbar_arrive(&bars[B_Q]);
-        }
+        };
+        write_query(ISO && NTP > 0);
+        mbar_arrive(&bars[B_Q]);
         float m_used = -INFINITY, l = 0.0f;
         uint8_t* psm = sm + X::OFF_P;
         for (int j = 0; j < NT && ok; ++j) {
-            const int buf = j & 1;
-            const float* ksc = reinterpret_cast<const float*>(sm + X::OFF_KS + buf * X::KS_BYTES);   // [64][NA]
-            wait(B_KF + buf, (j >> 1) & 1);   // this tile's key scales
+            const int kb = j % X::NB, buf = j & 1;   // K staging slot; row-exchange buffer
+            const float* ksc = reinterpret_cast<const float*>(sm + X::OFF_KS + kb * X::KS_BYTES);   // [64][NA]
+            wait(B_KF + kb, (j / X::NB) & 1);   // this tile's key scales
             wait(B_SFULL, j & 1);
             tc_fence_after();
             // ---- my KP keys: s = sum_g (K scale x softmax scale)_g * S_g, base 2 ----
@@ -558,6 +568,11 @@ __global__ void __launch_bounds__(kXThreads, 1)
                 else tmem_ld16x4(a0, a0 + 64, a0, a0 + 64, raw);
                 tc_fence_before();
                 mbar_arrive(&bars[B_SFREE]);   // S(j) is in registers: QK(j + 1) may overwrite it
+                if (ISO && j == NTP - 1) {
+                    // Q K^T of the last prefix tile has completed: the plain query for the chunk tiles
+                    write_query(false);
+                    mbar_arrive(&bars[B_QPLAIN]);
+                }
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     float acc;
@@ -574,7 +589,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
                     s[e] = acc;
                 }
             }
-            mbar_arrive(&bars[B_KE + buf]);   // the key scales are read: K(j + 2) may land
+            mbar_arrive(&bars[B_KE + kb]);   // the key scales are read: K(j + NB) may land
             // ---- masking (only tiles that reach past the prefix, the chunk or the causal edge) ----
             const int kbase = j < NTP ? kXT * j : kXT * (j - NTP);
             const int klim = j < NTP ? L0 : (p.causal ? min(T, tokc + 1) : T);   // keys < klim are visible
@@ -722,8 +737,7 @@ cudaError_t extend_upload_levels(const float* lv3, const float* lv4) {
 // kernel reads them.
 cudaError_t extend_launch(int fmt, int D, int G, int max_q_len, int NH, int B, const CUtensorMap& tk,
                           const CUtensorMap& tv, const ExtendParams& p, cudaStream_t st) {
-    if (fmt < 0 || fmt > 3 || (D != 128 && D != 256) || (fmt == 1 && D != 256) || (fmt >= 2 && D != 128) ||
-        !(G == 1 || G == 2 || G == 4 || G == 8))
+    if (fmt < 0 || fmt > 3 || (D != 128 && D != 256) || (fmt == 1 && D != 256) || !(G == 1 || G == 2 || G == 4 || G == 8))
         return cudaErrorInvalidValue;
     const dim3 pgrid((unsigned)(p.Lmax / kXT), (unsigned)p.Hkv, (unsigned)B);
     switch (fmt * 1000 + D) {
@@ -732,17 +746,26 @@ cudaError_t extend_launch(int fmt, int D, int G, int max_q_len, int NH, int B, c
         case 1256: extend_prep_kernel<256, 1><<<pgrid, 256, 0, st>>>(p); break;
         case 2128: extend_prep_kernel<128, 2><<<pgrid, 256, 0, st>>>(p); break;
         case 3128: extend_prep_kernel<128, 3><<<pgrid, 256, 0, st>>>(p); break;
+        case 2256: extend_prep_kernel<256, 2><<<pgrid, 256, 0, st>>>(p); break;
+        case 3256: extend_prep_kernel<256, 3><<<pgrid, 256, 0, st>>>(p); break;
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int tpt = 128 / G;
     dim3 grid((unsigned)((max_q_len + tpt - 1) / tpt), (unsigned)NH, (unsigned)B);
-    if (fmt >= 2) {
+    if (fmt >= 2 && D == 128) {
         switch (G) {
             case 1: return xlaunch<128, 1, true>(grid, tk, tv, p, st);
             case 2: return xlaunch<128, 2, true>(grid, tk, tv, p, st);
             case 4: return xlaunch<128, 4, true>(grid, tk, tv, p, st);
             case 8: return xlaunch<128, 8, true>(grid, tk, tv, p, st);
+        }
+    } else if (fmt >= 2) {
+        switch (G) {
+            case 1: return xlaunch<256, 1, true>(grid, tk, tv, p, st);
+            case 2: return xlaunch<256, 2, true>(grid, tk, tv, p, st);
+            case 4: return xlaunch<256, 4, true>(grid, tk, tv, p, st);
+            case 8: return xlaunch<256, 8, true>(grid, tk, tv, p, st);
         }
     } else if (D == 256) {
         switch (G) {

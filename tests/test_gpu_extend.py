@@ -164,14 +164,38 @@ def test_extend_rejects_unsupported_gqa(env):
     assert e.value.code == -3
 
 
-def test_extend_iso_head_dim_256_unsupported(env):
-    """ISO extend runs at head_dim 128 (the rotated query tiles need the shared
-    memory); head_dim 256 returns QKV_ERR_UNSUPPORTED and launches nothing."""
+@pytest.mark.parametrize("fmt,prefix,chunk,hkv,hq", [
+    ("iso3", [100], [37], 2, 16),
+    ("iso4", [0, 150, 64], [17, 40, 64], 2, 16),
+    ("iso3", [0], [45], 2, 16),
+    ("iso4", [77], [19], 1, 8),
+    ("iso3", [130], [50], 2, 4),
+])
+def test_extend_iso_head_dim_256(env, orc, fmt, prefix, chunk, hkv, hq):
+    """ISO extend at head_dim 256 (two 128-value blocks per head, as in the pages'
+    model): the rotated query's hi tile shares the query region with the plain
+    query, which replaces it once the prefix tiles are done."""
     torch, qkv = env
-    c = qkv.PagedKVCache("iso3", 4, 2, 256, quat=[0.5, 0.5, 0.5, 0.5])
-    z = torch.zeros((4, 16, 256), dtype=torch.bfloat16, device="cuda")
-    zk = torch.zeros((4, 2, 256), dtype=torch.bfloat16, device="cuda")
-    i32 = lambda a: torch.tensor(a, dtype=torch.int32, device="cuda")
-    with pytest.raises(qkv.QkvError) as e:
-        qkv.extend(c, z, zk, zk, i32([0, 4]), i32([0]), i32([[0, 1, 2, 3]]), 4)
-    assert e.value.code == -8
+    w, pool, table, q, kn, vn, cu, pre = _case(orc, prefix, chunk, hkv, hq, 256, seed=46, fmt=fmt)
+    scale = float(np.float32(1.0 / 16))
+    ref = pool.extend(q, kn, vn, cu, pre, table, scale, causal=True)
+    got = _run(torch, qkv, w, pool, table, q, kn, vn, cu, pre, scale=scale)
+    r = compare_attention(got, ref)
+    assert r["ok"], r
+
+
+@pytest.mark.parametrize("fmt", ["iso3", "iso4"])
+def test_extend_iso_head_dim_256_long_prefix_sampled(env, orc, fmt):
+    """A 256-token chunk over an 8192-token ISO prefix at head_dim 256 (Hq 16 / Hkv 2),
+    sampled rows against the oracle, fp32 and bf16 output."""
+    torch, qkv = env
+    w, pool, table, q, kn, vn, cu, pre = _case(orc, [8192], [256], 2, 16, 256, seed=47, fmt=fmt)
+    scale = float(np.float32(1.0 / 16))
+    got = _run(torch, qkv, w, pool, table, q, kn, vn, cu, pre, scale=scale)
+    rows = np.array([0, 1, 63, 64, 200, 255], np.int32)
+    ref = pool.extend(q, kn, vn, cu, pre, table, scale, causal=True, rows=rows)
+    r = compare_attention(got[rows], ref)
+    assert r["ok"], r
+    gotb = _run(torch, qkv, w, pool, table, q, kn, vn, cu, pre, scale=scale, out_dtype=torch.bfloat16)
+    rb = compare_attention(gotb[rows], ref, bf16=True)
+    assert rb["ok"], rb
