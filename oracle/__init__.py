@@ -22,6 +22,7 @@ _OUT_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_OUT_DIR, "libqkv_oracle.so")
 
 FMT_INT8, FMT_K8V4, FMT_ISO3, FMT_ISO4 = 0, 1, 2, 3
+FMT_Q4, FMT_K8, FMT_V8 = 4, 5, 6   # q4_0 both stores (rotated); int8 K + bf16 V; bf16 K + int8 V
 
 _lib = None
 

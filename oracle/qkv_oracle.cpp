@@ -16,6 +16,9 @@
 //         sections "What it does" and "Not in this PR".
 //   [K4]  "--kv k8v4: hybrid KV cache -- INT8 K + Hadamard-rotated Q4_0 V (816 B/cell)",
 //         sections "What", "How" and "Tests".
+// The format list follows [S8 "What it does"] (int8 for both stores, or for one store
+// with the other unquantized) and [S8 "Not in this PR"] / [K4 "What"] (q4_0 for both
+// stores, K and V rotated by the FWHT-256, 576 B per cell at head_dim 256).
 // Where the pages leave a step open, the reading taken is stated at the step.
 
 #include <cmath>
@@ -71,6 +74,16 @@ float float_from_bf16(uint16_t b) {
     return f;
 }
 
+// fp32 -> bfloat16, round to nearest, ties to even (the top 16 bits of the
+// binary32 encoding after rounding away the low 16); NaN stays a quiet NaN.
+uint16_t bf16_from_float(float f) {
+    uint32_t u;
+    std::memcpy(&u, &f, 4);
+    if ((u & 0x7fffffffu) > 0x7f800000u) return (uint16_t)((u >> 16) | 0x40);
+    const uint32_t lsb = (u >> 16) & 1u;
+    return (uint16_t)((u + 0x7fffu + lsb) >> 16);
+}
+
 // ---------------------------------------------------------------------------
 // Format geometry. [S8 "What it does"]: int8 codes + one fp16 scale per 64
 // values. [K4 "What"]: q4_0 V in 32-value blocks, fp16 d + 16 B of nibbles.
@@ -79,10 +92,15 @@ float float_from_bf16(uint16_t b) {
 // scales in another, each indexed [page][kv_head][slot][row bytes]. The ISO4
 // block's two bytes beyond code nibbles + fp16 norm are a reserved fp16 written
 // as zero, stored after the norm in the scale plane.
+// The unquantized store of the one-store formats [S8 "What it does": "k8v32 /
+// k32v8 quantize one store only"] keeps the input values as they arrive: the
+// pages' engine holds FP32 activations and keeps that store in FP32; here K and V
+// arrive as bf16, so the store holds the bf16 values unchanged (2 bytes per value,
+// no scale row). Reading the store back gives exactly the input.
 // ---------------------------------------------------------------------------
 
-enum { FMT_INT8 = 0, FMT_K8V4 = 1, FMT_ISO3 = 2, FMT_ISO4 = 3 };
-enum { ENC_INT8 = 0, ENC_Q4 = 1, ENC_ISO3 = 2, ENC_ISO4 = 3 };
+enum { FMT_INT8 = 0, FMT_K8V4 = 1, FMT_ISO3 = 2, FMT_ISO4 = 3, FMT_Q4 = 4, FMT_K8 = 5, FMT_V8 = 6 };
+enum { ENC_INT8 = 0, ENC_Q4 = 1, ENC_ISO3 = 2, ENC_ISO4 = 3, ENC_BF16 = 4 };
 
 int store_encoding(int fmt, int store /*0 = K, 1 = V*/) {
     switch (fmt) {
@@ -90,6 +108,9 @@ int store_encoding(int fmt, int store /*0 = K, 1 = V*/) {
         case FMT_K8V4: return store == 0 ? ENC_INT8 : ENC_Q4;
         case FMT_ISO3: return ENC_ISO3;
         case FMT_ISO4: return ENC_ISO4;
+        case FMT_Q4: return ENC_Q4;                              // K and V rotated, q4_0
+        case FMT_K8: return store == 0 ? ENC_INT8 : ENC_BF16;    // int8 K, V unquantized
+        case FMT_V8: return store == 0 ? ENC_BF16 : ENC_INT8;    // K unquantized, int8 V
     }
     return -1;
 }
@@ -101,6 +122,7 @@ void row_bytes(int enc, int D, int* code_b, int* scale_b) {
         case ENC_Q4:   *code_b = D / 2;        *scale_b = (D / 32) * 2;  break;
         case ENC_ISO3: *code_b = (D / 128) * 48; *scale_b = (D / 128) * 2; break;
         case ENC_ISO4: *code_b = (D / 128) * 64; *scale_b = (D / 128) * 4; break;
+        case ENC_BF16: *code_b = 2 * D;        *scale_b = 0;             break;
         default: *code_b = *scale_b = 0;
     }
 }
@@ -321,7 +343,13 @@ void unpack_iso(int bits, const uint8_t* in, int* codes) {
 // Dequantized values are returned in the original (unrotated) domain, in double.
 // ---------------------------------------------------------------------------
 void quant_vector(int enc, int D, const float* x, const float* quat, uint8_t* code, uint8_t* scale) {
-    if (enc == ENC_INT8) {
+    if (enc == ENC_BF16) {
+        // unquantized store: the bf16 value itself (x holds bf16 inputs, so this is exact)
+        for (int i = 0; i < D; ++i) {
+            uint16_t b = bf16_from_float(x[i]);
+            std::memcpy(code + 2 * i, &b, 2);
+        }
+    } else if (enc == ENC_INT8) {
         for (int g = 0; g < D / 64; ++g) {
             uint16_t h;
             quant_int8_group(x + 64 * g, (int8_t*)code + 64 * g, &h);
@@ -356,7 +384,13 @@ void quant_vector(int enc, int D, const float* x, const float* quat, uint8_t* co
 }
 
 void dequant_vector(int enc, int D, const uint8_t* code, const uint8_t* scale, const float* quat, double* out) {
-    if (enc == ENC_INT8) {
+    if (enc == ENC_BF16) {
+        for (int i = 0; i < D; ++i) {
+            uint16_t b;
+            std::memcpy(&b, code + 2 * i, 2);
+            out[i] = (double)float_from_bf16(b);
+        }
+    } else if (enc == ENC_INT8) {
         for (int g = 0; g < D / 64; ++g) {
             uint16_t h;
             std::memcpy(&h, scale + 2 * g, 2);

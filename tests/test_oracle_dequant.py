@@ -83,14 +83,17 @@ def test_q4_dequant_hand_packed_nibble_order(orc):
     assert np.max(np.abs(other - want)) > 0.1 * np.max(np.abs(want)), "the test sees the nibble order"
 
 
-def test_q4_reconstruction_within_half_step(orc):
+@pytest.mark.parametrize("fmt,store", [(1, 1), (4, 0), (4, 1)])
+def test_q4_reconstruction_within_half_step(orc, fmt, store):
+    """k8v4 V and both stores of the q4_0 format (K rotated like V: "rotate K after RoPE
+    and V", qwen35/q36 page, "Not in this PR")."""
     scipy_linalg = pytest.importorskip("scipy.linalg")
     H = scipy_linalg.hadamard(256).astype(np.float64)
     x = _bf16_inputs(12, 256 * 20, 1.0).reshape(20, 256)
     x[:, [3, 77]] *= 20.0
     for v in x:
-        code, scale = orc.quant_vector(orc.FMT_K8V4, 1, v)
-        deq = orc.dequant_vector(orc.FMT_K8V4, 1, 256, code, scale)
+        code, scale = orc.quant_vector(fmt, store, v)
+        deq = orc.dequant_vector(fmt, store, 256, code, scale)
         ds = _f16(scale.view(np.uint16))
         d = np.abs(ds)
         # the error, seen in the rotated domain (H/16 is orthonormal), is at most half a
@@ -197,3 +200,17 @@ def test_pool_gather_reads_the_hand_packed_planes(orc):
             wk = kc[pg, h, sl].astype(np.float64) * np.repeat(_f16(ks[pg, h, sl]), 64)
             wv = vc[pg, h, sl].astype(np.float64) * np.repeat(_f16(vs[pg, h, sl]), 64)
             assert np.array_equal(k[t, h], wk) and np.array_equal(v[t, h], wv)
+
+
+@pytest.mark.parametrize("fmt,store", [(5, 1), (6, 0)])
+def test_unquantized_store_returns_the_bf16_input(orc, fmt, store):
+    """The one-store formats keep the other store as the bf16 input bits: two bytes
+    per value, little-endian bf16, no scale row; reading it back is exact."""
+    x = _bf16_inputs(14, 128 * 8, 30.0)
+    x[:4] = [0.0, -0.0, 2.0 ** -130, -(2.0 ** 100)]
+    for v in x.reshape(8, 128):
+        code, scale = orc.quant_vector(fmt, store, v)
+        assert code.size == 256 and scale.size == 0
+        assert np.array_equal(code.view(np.uint16), synth.bf16_bits(v))
+        deq = orc.dequant_vector(fmt, store, 128, code, scale)
+        assert np.array_equal(deq, v.astype(np.float64))

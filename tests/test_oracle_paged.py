@@ -11,8 +11,8 @@ import pytest
 from quantized_paged_kv_append_gb300 import synth
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
-FMTS = [0, 1, 2, 3]
-DIMS = {0: 256, 1: 256, 2: 128, 3: 128}
+FMTS = [0, 1, 2, 3, 4, 5, 6]
+DIMS = {0: 256, 1: 256, 2: 128, 3: 128, 4: 256, 5: 128, 6: 256}
 
 
 def _pool(orc, fmt, L, hkv, d, seed=0, shuffle=True, outliers=True, B=1):
@@ -203,8 +203,13 @@ def test_byte_accounting_matches_pages(orc):
     assert q4_v == g["q4_v_bytes_per_head_cell"]["value"]
     assert orc.row_bytes(0, 1, 256)[0] == g["int8_v_bytes_per_head_cell"]["value"]
     assert 2 * 2 * 256 * 4 == g["fp32_cell_bytes_head_dim_256"]["value"] * 2
-    # q4_0 for both stores: 18 B per 32 values
-    assert 2 * 2 * q4_v == g["q4_0_pair_cell_bytes"]["value"]
+    # q4_0 for both stores (the q4_0 format): 18 B per 32 values, K and V
+    q4_k4, q4_v4 = sum(orc.row_bytes(orc.FMT_Q4, 0, 256)), sum(orc.row_bytes(orc.FMT_Q4, 1, 256))
+    assert 2 * 2 * q4_v == g["q4_0_pair_cell_bytes"]["value"] == 2 * (q4_k4 + q4_v4)
+    # one store quantized: int8 on one side, the bf16 input values (no scale row) on the other
+    assert orc.row_bytes(orc.FMT_K8, 0, 256) == orc.row_bytes(0, 0, 256)
+    assert orc.row_bytes(orc.FMT_K8, 1, 256) == (512, 0) == orc.row_bytes(orc.FMT_V8, 0, 256)
+    assert orc.row_bytes(orc.FMT_V8, 1, 256) == orc.row_bytes(0, 1, 256)
     iso3 = sum(orc.row_bytes(2, 0, 128))
     iso4 = sum(orc.row_bytes(3, 0, 128))
     assert iso3 == g["iso3_block_bytes"]["value"] and iso4 == g["iso4_block_bytes"]["value"]
