@@ -437,6 +437,10 @@ DECODE_CONFIGS = {
     "k8v4_119k": dict(fmt="k8v4", HQ=16, HKV=2, D=256, L=118750),
     "iso3_82k": dict(fmt="iso3", HQ=16, HKV=4, D=128, L=81920),
     "iso4_82k": dict(fmt="iso4", HQ=16, HKV=4, D=128, L=81920),
+    # the other formats at the 128K int8 shape
+    "q4_128k": dict(fmt="q4", HQ=16, HKV=2, D=256, L=131072),
+    "k8vbf16_128k": dict(fmt="k8vbf16", HQ=16, HKV=2, D=256, L=131072),
+    "kbf16v8_128k": dict(fmt="kbf16v8", HQ=16, HKV=2, D=256, L=131072),
 }
 
 
@@ -447,6 +451,10 @@ def kv_bytes_per_token(fmt, hkv, d):
         return 2 * hkv * (d + 2 * d // 64)
     if fmt == "k8v4":
         return hkv * ((d + 2 * d // 64) + (d // 2 + 2 * d // 32))
+    if fmt == "q4":
+        return 2 * hkv * (d // 2 + 2 * d // 32)
+    if fmt in ("k8vbf16", "kbf16v8"):
+        return hkv * ((d + 2 * d // 64) + 2 * d)
     per_block = 50 if fmt == "iso3" else 66
     return 2 * hkv * (d // 128) * per_block
 
@@ -675,6 +683,9 @@ EXTEND_CONFIGS = {
     # ISO at head_dim 256 (two 128-value blocks per head), the int8 decode shape
     "extend_iso3_d256": ("iso3", 16, 2, 256),
     "extend_iso4_d256": ("iso4", 16, 2, 256),
+    "extend_q4": ("q4", 16, 2, 256),
+    "extend_k8vbf16": ("k8vbf16", 16, 2, 256),
+    "extend_kbf16v8": ("kbf16v8", 16, 2, 256),
 }
 
 

@@ -52,12 +52,16 @@
 extern "C" {
 #endif
 
-/* KV formats [S8 "What it does"; K4 "What"; FT "What"]. */
+/* KV formats [S8 "What it does", "Not in this PR"; K4 "What"; FT "What"]. */
 typedef enum {
-    QKV_INT8 = 0, /* K and V: int8 codes + fp16 scale (group absmax/127) per 64 values     */
-    QKV_K8V4 = 1, /* K as QKV_INT8; V: FWHT-256 (x1/16) then q4_0 per 32 values; D = 256   */
-    QKV_ISO3 = 2, /* K and V: per 128 values, 3-bit Lloyd-Max codes (48 B) + fp16 norm    */
-    QKV_ISO4 = 3  /* K and V: per 128 values, 4-bit codes (64 B) + fp16 norm + 2 B reserved */
+    QKV_INT8 = 0,     /* K and V: int8 codes + fp16 scale (group absmax/127) per 64 values     */
+    QKV_K8V4 = 1,     /* K as QKV_INT8; V: FWHT-256 (x1/16) then q4_0 per 32 values; D = 256   */
+    QKV_ISO3 = 2,     /* K and V: per 128 values, 3-bit Lloyd-Max codes (48 B) + fp16 norm    */
+    QKV_ISO4 = 3,     /* K and V: per 128 values, 4-bit codes (64 B) + fp16 norm + 2 B reserved */
+    QKV_Q4 = 4,       /* K and V as the V of QKV_K8V4 (FWHT-256 then q4_0; 576 B per cell at
+                         2 KV heads); D = 256. The query is rotated in the kernels            */
+    QKV_K8_VBF16 = 5, /* K as QKV_INT8; V unquantized: the bf16 input values, no scales       */
+    QKV_KBF16_V8 = 6  /* K unquantized (bf16 input values, no scales); V as QKV_INT8          */
 } qkv_format;
 
 typedef enum { QKV_OUT_BF16 = 0, QKV_OUT_F32 = 1 } qkv_out_dtype;
@@ -88,6 +92,9 @@ enum {
  *   iso4 codes : per block 64 bytes, value i at byte i/2 (low nibble if i even);
  *                scales: per block fp16 corrected norm followed by a reserved
  *                fp16 written as 0 (68 B per block in total).
+ *   bf16 codes : the unquantized store of QKV_K8_VBF16 / QKV_KBF16_V8: the bf16
+ *                input values, two bytes each; that store has no scale plane
+ *                (0 scale bytes per row; its scale pointer may be NULL).
  * `quat` is the fixed unit quaternion (w, x, y, z) of the ISO formats; it is
  * ignored by the other formats. Buffers must be 16-byte aligned.
  */
@@ -96,7 +103,7 @@ typedef struct {
     int32_t num_pages;    /* physical pages in the pool                  */
     int32_t page_size;    /* must be 16                                  */
     int32_t num_kv_heads;
-    int32_t head_dim;     /* int8: 128 or 256; k8v4: 256; iso: 128 or 256 */
+    int32_t head_dim;     /* k8v4, q4: 256; the other formats: 128 or 256 */
     int32_t reserved0;
     void* k_codes;
     void* k_scales;

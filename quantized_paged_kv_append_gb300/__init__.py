@@ -13,7 +13,8 @@ import ctypes as C
 import math
 
 from . import _lib
-from ._lib import FORMATS, QKV_INT8, QKV_K8V4, QKV_ISO3, QKV_ISO4, QkvError  # noqa: F401
+from ._lib import (FORMATS, QKV_INT8, QKV_K8V4, QKV_ISO3, QKV_ISO4, QKV_Q4, QKV_K8_VBF16, QKV_KBF16_V8,  # noqa: F401
+                   QkvError)
 
 __all__ = ["PagedKVCache", "append", "decode", "decode_workspace", "extend", "extend_workspace", "row_bytes", "iso_levels",
            "device_error"]

@@ -14,7 +14,9 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libqkv.so")
 
 QKV_INT8, QKV_K8V4, QKV_ISO3, QKV_ISO4 = 0, 1, 2, 3
-FORMATS = {"int8": QKV_INT8, "k8v4": QKV_K8V4, "iso3": QKV_ISO3, "iso4": QKV_ISO4}
+QKV_Q4, QKV_K8_VBF16, QKV_KBF16_V8 = 4, 5, 6
+FORMATS = {"int8": QKV_INT8, "k8v4": QKV_K8V4, "iso3": QKV_ISO3, "iso4": QKV_ISO4, "q4": QKV_Q4,
+           "k8vbf16": QKV_K8_VBF16, "kbf16v8": QKV_KBF16_V8}
 QKV_OUT_BF16, QKV_OUT_F32 = 0, 1
 ERRORS = {0: "QKV_OK", -1: "QKV_ERR_ARG", -2: "QKV_ERR_HEAD_DIM", -3: "QKV_ERR_GQA", -4: "QKV_ERR_WORKSPACE",
           -5: "QKV_ERR_FORMAT", -6: "QKV_ERR_CUDA", -7: "QKV_ERR_DEVICE", -8: "QKV_ERR_UNSUPPORTED"}

@@ -185,15 +185,17 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 int check_desc(const qkv_cache_desc* d) {
     if (!d) return QKV_ERR_ARG;
-    if (d->format < QKV_INT8 || d->format > QKV_ISO4) return QKV_ERR_FORMAT;
+    if (d->format < QKV_INT8 || d->format > QKV_KBF16_V8) return QKV_ERR_FORMAT;
     if (d->page_size != kPage || d->num_pages <= 0 || d->num_kv_heads <= 0) return QKV_ERR_ARG;
     const int D = d->head_dim;
     switch (d->format) {
-        case QKV_INT8: if (D != 128 && D != 256) return QKV_ERR_HEAD_DIM; break;
-        case QKV_K8V4: if (D != 256) return QKV_ERR_HEAD_DIM; break;
+        case QKV_K8V4:
+        case QKV_Q4: if (D != 256) return QKV_ERR_HEAD_DIM; break;
         default: if (D != 128 && D != 256) return QKV_ERR_HEAD_DIM; break;
     }
-    if (!d->k_codes || !d->k_scales || !d->v_codes || !d->v_scales) return QKV_ERR_ARG;
+    // the unquantized (bf16) store has no scale plane: its scale pointer may be null
+    const bool ks_none = d->format == QKV_KBF16_V8, vs_none = d->format == QKV_K8_VBF16;
+    if (!d->k_codes || !d->v_codes || (!d->k_scales && !ks_none) || (!d->v_scales && !vs_none)) return QKV_ERR_ARG;
     if (!aligned16(d->k_codes) || !aligned16(d->k_scales) || !aligned16(d->v_codes) || !aligned16(d->v_scales))
         return QKV_ERR_ARG;
     return QKV_OK;
@@ -205,6 +207,9 @@ int enc_of(int fmt, int store) {
         case QKV_K8V4: return store == 0 ? ENC_INT8 : ENC_Q4;
         case QKV_ISO3: return ENC_ISO3;
         case QKV_ISO4: return ENC_ISO4;
+        case QKV_Q4: return ENC_Q4;
+        case QKV_K8_VBF16: return store == 0 ? ENC_INT8 : ENC_BF16;
+        case QKV_KBF16_V8: return store == 0 ? ENC_BF16 : ENC_INT8;
     }
     return -1;
 }
@@ -249,9 +254,11 @@ int extend_layout(const qkv_cache_desc* d, int batch, int max_q_len, int max_pag
     if (L->Lmax > (1LL << 30)) return QKV_ERR_ARG;
     const size_t heads = (size_t)batch * d->num_kv_heads;
     const size_t plane = al(heads * (size_t)L->Lmax * d->head_dim * 2);
-    L->off_v = plane;
-    L->off_s = 2 * plane;
-    L->bytes = 2 * plane + al(heads * (size_t)L->Lmax * (d->head_dim / 64) * 4);
+    // K' rows (hi plane; the q4 format adds the lo plane right after it), V^T rows, key scales
+    const size_t kplanes = d->format == QKV_Q4 ? 2 : 1;
+    L->off_v = kplanes * plane;
+    L->off_s = L->off_v + plane;
+    L->bytes = L->off_s + al(heads * (size_t)L->Lmax * (d->head_dim / 64) * 4);
     return QKV_OK;
 }
 
@@ -274,7 +281,7 @@ cudaError_t qkv::smem_attr_once(const void* fn, int bytes, bool (&done)[kMaxDevi
 extern "C" {
 
 int qkv_row_bytes(int format, int store, int head_dim, int* code_bytes, int* scale_bytes) {
-    if (format < QKV_INT8 || format > QKV_ISO4) return QKV_ERR_FORMAT;
+    if (format < QKV_INT8 || format > QKV_KBF16_V8) return QKV_ERR_FORMAT;
     if ((store != 0 && store != 1) || head_dim <= 0 || !code_bytes || !scale_bytes) return QKV_ERR_ARG;
     const int enc = enc_of(format, store);
     if (head_dim % group_size(enc) || (enc == ENC_Q4 && head_dim != 256)) return QKV_ERR_HEAD_DIM;
@@ -359,9 +366,10 @@ int kv_decode_attn(const qkv_cache_desc* cache, const void* q, const void* k_new
     std::memset(&tk, 0, sizeof(tk));
     std::memset(&tv, 0, sizeof(tv));
     const int kenc = enc_of(cache->format, 0), venc = enc_of(cache->format, 1);
-    if (kenc == ENC_INT8 && (rc = make_code_map(&tk, cache->k_codes, rows, code_row_bytes(kenc, D)))) return rc;
-    if ((venc == ENC_INT8 || venc == ENC_Q4) && (rc = make_code_map(&tv, cache->v_codes, rows, code_row_bytes(venc, D))))
-        return rc;
+    // tensor maps for the planes staged by 128-byte TMA boxes (int8, q4 and bf16 rows; ISO rows go by bulk copies)
+    auto tma_plane = [](int enc) { return enc == ENC_INT8 || enc == ENC_Q4 || enc == ENC_BF16; };
+    if (tma_plane(kenc) && (rc = make_code_map(&tk, cache->k_codes, rows, code_row_bytes(kenc, D)))) return rc;
+    if (tma_plane(venc) && (rc = make_code_map(&tv, cache->v_codes, rows, code_row_bytes(venc, D)))) return rc;
 
     // grid: at most one CTA per SM, and about 8 pages (one per warp) or more per CTA
     const long long max_pages_hint = ((long long)std::min(max_seq_len, max_pages_per_seq * kPage) + kPage - 1) / kPage;
@@ -432,7 +440,8 @@ int kv_extend_attn(const qkv_cache_desc* cache, const void* q, const void* k_new
     CUtensorMap tk, tv;
     std::memset(&tk, 0, sizeof(tk));
     std::memset(&tv, 0, sizeof(tv));
-    if ((rc = make_f16_map(&tk, ws, heads * XL.Lmax, D, 64))) return rc;
+    const long long kplanes = cache->format == QKV_Q4 ? 2 : 1;
+    if ((rc = make_f16_map(&tk, ws, kplanes * heads * XL.Lmax, D, 64))) return rc;
     if ((rc = make_f16_map(&tv, ws + XL.off_v, heads * D, XL.Lmax, D))) return rc;
     ExtendParams p;
     p.kc = (const uint8_t*)cache->k_codes;
@@ -458,6 +467,7 @@ int kv_extend_attn(const qkv_cache_desc* cache, const void* q, const void* k_new
     p.Lmax = (int)XL.Lmax;
     p.xk = (uint16_t*)ws;
     p.xv = (uint16_t*)(ws + XL.off_v);
+    p.xklo = (uint16_t*)ws + (size_t)heads * XL.Lmax * D;
     p.xs = (float*)(ws + XL.off_s);
     for (int i = 0; i < 4; ++i) p.quat[i] = cache->quat[i];
     const int NH = cache->num_kv_heads * (Gtot / G);

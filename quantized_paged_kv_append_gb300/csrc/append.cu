@@ -66,7 +66,7 @@ cudaError_t append_read_error(unsigned* out, bool clear) {
     return cudaMemcpyToSymbol(g_err_append, &z, sizeof(unsigned));
 }
 
-// fmt: 0 int8, 1 k8v4, 2 iso3, 3 iso4
+// fmt: 0 int8, 1 k8v4, 2 iso3, 3 iso4, 4 q4 (both stores), 5 int8 K + bf16 V, 6 bf16 K + int8 V
 cudaError_t append_launch(int fmt, int D, const AppendParams& p, cudaStream_t st) {
     long long warps = (long long)p.n_tokens * p.Hkv * 2;
     if (warps == 0) return cudaSuccess;
@@ -79,6 +79,11 @@ cudaError_t append_launch(int fmt, int D, const AppendParams& p, cudaStream_t st
     else if (fmt == 2 && D == 256) QKV_APPEND(ENC_ISO3, ENC_ISO3, 256);
     else if (fmt == 3 && D == 128) QKV_APPEND(ENC_ISO4, ENC_ISO4, 128);
     else if (fmt == 3 && D == 256) QKV_APPEND(ENC_ISO4, ENC_ISO4, 256);
+    else if (fmt == 4 && D == 256) QKV_APPEND(ENC_Q4, ENC_Q4, 256);
+    else if (fmt == 5 && D == 128) QKV_APPEND(ENC_INT8, ENC_BF16, 128);
+    else if (fmt == 5 && D == 256) QKV_APPEND(ENC_INT8, ENC_BF16, 256);
+    else if (fmt == 6 && D == 128) QKV_APPEND(ENC_BF16, ENC_INT8, 128);
+    else if (fmt == 6 && D == 256) QKV_APPEND(ENC_BF16, ENC_INT8, 256);
     else return cudaErrorInvalidValue;
 #undef QKV_APPEND
     return cudaGetLastError();

@@ -65,54 +65,69 @@ constexpr int kThr = (kWProdV + 1) * 32;    // 480 threads
 
 // Formats (the ABI's qkv_format): 0 int8 K and V; 1 k8v4 (int8 K, q4_0 codes of the
 // FWHT-rotated V); 2 / 3 ISO3 / ISO4 (K and V: Lloyd-Max codes of the rotated unit
-// vector per 128 values, one fp16 norm scale per block).
+// vector per 128 values, one fp16 norm scale per block); 4 q4_0 for both stores (K
+// rotated like V; the query is rotated by the same FWHT); 5 int8 K with the bf16 V
+// unquantized; 6 the bf16 K unquantized with int8 V.
 template <int D, int FMT>
 struct TG {
-    static constexpr bool VQ = FMT == 1, ISO = FMT >= 2;
+    static constexpr bool ISO = FMT == 2 || FMT == 3;
+    static constexpr bool KQ = FMT == 4;                 // K: q4_0 of the rotated row
+    static constexpr bool VQ = FMT == 1 || FMT == 4;     // V: q4_0 of the rotated row (output rotated back)
+    static constexpr bool KB = FMT == 6, VB = FMT == 5;  // the unquantized bf16 K / V
+    static constexpr bool QHL = ISO || KQ;               // transformed query: fp16 hi (rows 0..7) + lo (8..15)
     static constexpr int ISO_RB = FMT == 2 ? 48 : 64;             // ISO code bytes per 128 values
     static constexpr int ISO_SB = FMT == 2 ? 2 : 4;               // ISO scale bytes per 128 values
     static constexpr int NA = D / 64;             // 64-dim atoms (Q tile, K' and V' tiles)
-    static constexpr int NKG = ISO ? D / 128 : D / 64;            // K scale groups = score accumulators
-    static constexpr int KROW = ISO ? ISO_RB * D / 128 : D;       // K code bytes of one row
-    static constexpr int KSROW = ISO ? ISO_SB * D / 128 : 2 * NA; // K scale bytes of one row
-    static constexpr int VROW = ISO ? KROW : (VQ ? D / 2 : D);
-    static constexpr int VSROW = ISO ? KSROW : (VQ ? 2 * (D / 32) : 2 * NA);
-    static constexpr int VG = ISO ? D / 128 : (VQ ? D / 32 : D / 64);   // V scale groups
+    static constexpr int NKG = ISO ? D / 128 : KQ ? D / 32 : D / 64;   // K scale groups = score accumulators
+    static constexpr int KROW = ISO ? ISO_RB * D / 128 : KQ ? D / 2 : KB ? 2 * D : D;   // K code bytes of one row
+    static constexpr int KSROW = ISO ? ISO_SB * D / 128 : KQ ? 2 * (D / 32) : KB ? 0 : 2 * NA;   // K scale bytes
+    static constexpr int VROW = ISO ? KROW : VQ ? D / 2 : VB ? 2 * D : D;
+    static constexpr int VSROW = ISO ? KSROW : VQ ? 2 * (D / 32) : VB ? 0 : 2 * NA;
+    static constexpr int VG = ISO ? D / 128 : (VQ ? D / 32 : D / 64);   // V scale groups (q4, bf16: scale 1)
     static constexpr int PG = 4;                  // P' column groups of 16 (8 heads hi + lo)
     static constexpr int PM = 16 * PG;            // M of the PV MMA: 64
     static constexpr int PAGE_B = KROW * kPage;   // staged K codes of one page
     static constexpr int VPAGE_B = VROW * kPage;  // staged V codes of one page
-    static constexpr int VBOX = VPAGE_B / 2048;   // 128-byte TMA boxes per V page (int8, q4)
+    static constexpr int KBOX = KB ? 2 * D / 128 : KQ ? 1 : D / 128;   // 128-byte TMA boxes per K page (not ISO)
+    static constexpr int VBOX = VPAGE_B / 2048;   // 128-byte TMA boxes per V page (not ISO)
     static constexpr int SC_B = kPage * KSROW;    // staged K scales of one page
     static constexpr int VSC_B = kPage * VSROW;   // staged V scales of one page
-    static constexpr int QT = 1;                  // query tile (ISO: the rotated query as fp16 hi rows 0..7, lo rows 8..15)
+    static constexpr int KSTB = KB ? 1 : 2;       // K staging tiles (bf16 K: one, for shared-memory room)
+    static constexpr int VSTB = VB ? 0 : 2;       // V staging tiles (bf16 V lands in V' itself)
+    static constexpr int VPB = VB ? 2 : 1;        // V' tiles
+    static constexpr int NSB = KQ ? 1 : 2;        // TMEM score buffers (q4 K: 8 accumulators, one buffer)
+    static constexpr int QT = 1;                  // query tile (QHL: hi rows 0..7, lo rows 8..15)
     static constexpr int SACC = ISO ? 2 : 1;      // score accumulators per K scale group (ISO: even / odd k-steps)
     static constexpr int SBUF = NKG * SACC * 16;  // TMEM columns of one score buffer
     static constexpr int LUT_N = FMT == 2 ? 64 : FMT == 3 ? 256 : 0;   // code pair -> fp16 level pair
-    static constexpr int OFF_KST = 0;                               // [2][8][PAGE_B]
-    static constexpr int OFF_VST = OFF_KST + 2 * kTP * PAGE_B;      // [2][8][VPAGE_B]
-    static constexpr int OFF_VP = OFF_VST + 2 * kTP * VPAGE_B;      // V' [NA][128 rows][128 B]
-    static constexpr int OFF_PP = OFF_VP + NA * 16384;              // P' [PM / 64][128 rows][128 B]
+    static constexpr int KE_N = kConvW + (KB ? 0 : kSoftW);   // arrivals that free a K slot
+    static constexpr int VE_N = VB ? 1 : kConvW + kSoftW;     // arrivals that free a V slot (bf16 V: the PV commit)
+    static constexpr int OFF_KST = 0;                               // [KSTB][8][PAGE_B]
+    static constexpr int OFF_VST = OFF_KST + KSTB * kTP * PAGE_B;   // [VSTB][8][VPAGE_B]
+    static constexpr int OFF_VP = OFF_VST + VSTB * kTP * VPAGE_B;   // V' [VPB][NA][128 rows][128 B]
+    static constexpr int OFF_PP = OFF_VP + VPB * NA * 16384;        // P' [PM / 64][128 rows][128 B]
     static constexpr int OFF_Q = OFF_PP + (PM / 64) * 16384;        // Q [QT][NA][16 rows][128 B]
     static constexpr int OFF_LUT = OFF_Q + QT * NA * 2048;          // per-lane level pairs [LUT_N][32]
-    static constexpr int OFF_KSC = OFF_LUT + LUT_N * 32 * 4;        // [2][8][SC_B]
-    static constexpr int OFF_VSC = OFF_KSC + 2 * kTP * SC_B;        // [2][8][VSC_B]
+    static constexpr int OFF_KSC = OFF_LUT + LUT_N * 32 * 4;        // [KSTB][8][SC_B]
+    static constexpr int OFF_VSC = OFF_KSC + KSTB * kTP * SC_B;     // [2][8][VSC_B]
     static constexpr int OFF_BIAS = OFF_VSC + 2 * kTP * VSC_B;      // float [NA][8]
     static constexpr int OFF_RED = OFF_BIAS + 256;                  // softmax-warp reductions
     static constexpr int OFF_ROW = OFF_RED + 512;                   // quantize-on-write rows [2][512]
     static constexpr int OFF_BAR = OFF_ROW + 1024;
     static constexpr int OFF_MISC = OFF_BAR + 32 * 8;
     static constexpr int SMEM = OFF_MISC + 64;
-    static constexpr int KCOL = 0;                     // K' columns: D / 2 (fp16 pairs)
-    static constexpr int SCOL = D / 2;                 // two score buffers of SBUF columns
-    static constexpr int OCOL = SCOL + 2 * SBUF;       // O (M = 64 rows in lanes 32 (r / 16) + r % 16, N = D)
+    static constexpr int KCOL = 0;                     // K' columns: D / 2 (16-bit pairs)
+    static constexpr int SCOL = D / 2;                 // NSB score buffers of SBUF columns
+    static constexpr int OCOL = SCOL + NSB * SBUF;     // O (M = 64 rows in lanes 32 (r / 16) + r % 16, N = D)
     static constexpr int TCOLS = (OCOL + D) <= 256 ? 256 : 512;
     static_assert(OCOL + D <= 512, "TMEM budget");
     static_assert(SMEM + 1024 <= 232448 - 1024, "shared memory budget");
     static_assert(2 * kTP * SC_B <= 4096 && 2 * kTP * VSC_B <= 4096, "scale staging");
     static_assert(!VQ || D == 256, "q4 V is FWHT-256 rotated");
+    static_assert(!KQ || D == 256, "q4 K is FWHT-256 rotated");
     static_assert(OFF_VP % 1024 == 0 && OFF_PP % 1024 == 0 && OFF_Q % 1024 == 0, "UMMA operand alignment");
     static_assert(PAGE_B % 16 == 0 && VPAGE_B % 16 == 0 && SC_B % 16 == 0 && VSC_B % 16 == 0, "bulk copies");
+    static_assert(KROW * kPage <= 2048 * 4 && VROW * kPage <= 2048 * 4, "TMA boxes per page");
 };
 
 enum {
@@ -261,8 +276,8 @@ __global__ void __launch_bounds__(kThr, 1)
         mbar_init(&bars[B_VF], 2);
         mbar_init(&bars[B_VF + 1], 2);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&bars[B_KE + i], kConvW + kSoftW);
-            mbar_init(&bars[B_VE + i], kConvW + kSoftW);
+            mbar_init(&bars[B_KE + i], X::KE_N);
+            mbar_init(&bars[B_VE + i], X::VE_N);
             mbar_init(&bars[B_QKD + i], 1);
             mbar_init(&bars[B_PVD + i], 1);
             mbar_init(&bars[B_SF + i], kSoftW);
@@ -367,7 +382,7 @@ __global__ void __launch_bounds__(kThr, 1)
                     const int rowb = kind ? X::VROW : X::KROW, scrow = kind ? X::VSROW : X::KSROW;
                     const long long prow = ((long long)pid * p.Hkv + spc.hg / (p.Gtot / G)) * kPage;
                     bulk_prefetch_l2((kind ? p.vc : p.kc) + prow * rowb, kPage * rowb);
-                    bulk_prefetch_l2((kind ? p.vs : p.ks) + prow * scrow, kPage * scrow);
+                    if (scrow) bulk_prefetch_l2((kind ? p.vs : p.ks) + prow * scrow, kPage * scrow);
                 }
             }
         }
@@ -420,11 +435,20 @@ __global__ void __launch_bounds__(kThr, 1)
         const uint8_t* scl = kind ? p.vs : p.ks;
         const uint16_t* newsrc = kind ? p.v_new : p.k_new;
         // per-plane geometry: V pages of q4 codes are half as wide and carry twice the scales;
-        // ISO pages (48 or 64 code bytes per 128 values) are staged row-major by one bulk copy
+        // ISO pages (48 or 64 code bytes per 128 values) are staged row-major by one bulk copy;
+        // the unquantized bf16 V goes straight into the V' tile (its 64-dim boxes are the MN-major
+        // operand layout), bf16 K into one staging tile
         const int pageb = kind ? X::VPAGE_B : X::PAGE_B, scb = kind ? X::VSC_B : X::SC_B;
-        const int nbox = kind ? X::VBOX : D / 128, scrow = kind ? X::VSROW : X::KSROW;
+        const int nbox = kind ? X::VBOX : X::KBOX, scrow = kind ? X::VSROW : X::KSROW;
+        const int nslot = kind ? 2 : X::KSTB;   // staging slots of this plane
+        const bool to_vp = X::VB && kind;
         const int rowb = pageb / kPage;   // code bytes of one row
         const uint8_t* codes = kind ? p.vc : p.kc;
+        // where box bx of page j of a tile in slot buf lands
+        auto dst = [&](int buf, int j, int bx) -> uint8_t* {
+            if (to_vp) return sm + X::OFF_VP + buf * NA * 16384 + bx * 16384 + j * 2048;
+            return sm + (kind ? X::OFF_VST : X::OFF_KST) + (buf * kTP + j) * pageb + bx * 2048;
+        };
         uint32_t T = 0, pat_phase = 0;
         Piece pc;
         bool first = true;
@@ -446,8 +470,11 @@ __global__ void __launch_bounds__(kThr, 1)
             first = false;
             for (int pg0 = pc.p0; pg0 < pc.p1; pg0 += kTP, ++T) {
                 const int npg = min(kTP, pc.p1 - pg0);
-                const int buf = T & 1;
-                const int jp = (p.k_new != nullptr && last_page >= pg0 && last_page < pg0 + npg) ? last_page - pg0 : -1;
+                const int buf = nslot == 2 ? (int)(T & 1) : 0;
+                const uint32_t round = nslot == 2 ? T >> 1 : T;   // uses of this slot so far
+                // the page of the sequence's last token is patched after it lands: the newest row
+                // (quantize-on-write) and, for the bf16 V tile, zeros in the rows past the end
+                const int jp = ((p.k_new != nullptr || to_vp) && last_page >= pg0 && last_page < pg0 + npg) ? last_page - pg0 : -1;
                 const int pi = pg0 - pc.p0;   // page index inside the piece (a multiple of 8)
                 if ((pi >> 5) > bc) {
                     pid_cur = pid_nxt;
@@ -460,9 +487,8 @@ __global__ void __launch_bounds__(kThr, 1)
                     pid = 0;
                 }
                 const int pid_patch = __shfl_sync(0xffffffffu, pid, jp < 0 ? 0 : jp);
-                if (T >= 2) wait_or_flag(emptyb + buf, ((T >> 1) - 1) & 1);
+                if (round >= 1) wait_or_flag(emptyb + buf, (round - 1) & 1);
                 uint64_t* full = fullb + buf;
-                uint8_t* st = sm + (kind ? X::OFF_VST : X::OFF_KST) + buf * kTP * pageb;
                 uint8_t* ss = sm + (kind ? X::OFF_VSC : X::OFF_KSC) + buf * kTP * scb;
                 const int nload = npg - (jp >= 0 ? 1 : 0);
                 if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)nload * (pageb + scb));
@@ -472,12 +498,12 @@ __global__ void __launch_bounds__(kThr, 1)
                     const int row = (pid * p.Hkv + kvh) * kPage;
                     const uint64_t pol = l2_evict_first_policy();
                     if constexpr (X::ISO) {
-                        bulk_load_hint(st + lane * pageb, codes + (size_t)row * rowb, pageb, full, pol);
+                        bulk_load_hint(dst(buf, lane, 0), codes + (size_t)row * rowb, pageb, full, pol);
                     } else {
                         for (int bx = 0; bx < nbox; ++bx)
-                            tma_load_2d_hint(st + lane * pageb + bx * 2048, tm, full, bx * 128, row, pol);
+                            tma_load_2d_hint(dst(buf, lane, bx), tm, full, bx * 128, row, pol);
                     }
-                    bulk_load_hint(ss + lane * scb, scl + (size_t)row * scrow, scb, full, pol);
+                    if (scb) bulk_load_hint(ss + lane * scb, scl + (size_t)row * scrow, scb, full, pol);
                 }
                 if (jp >= 0) {
                     // the sequence's newest token: load its page, quantize the new row into the
@@ -487,24 +513,37 @@ __global__ void __launch_bounds__(kThr, 1)
                     if (lane == 0) {
                         mbar_arrive_expect_tx(pb, pageb + scb);
                         if constexpr (X::ISO) {
-                            bulk_load(st + jp * pageb, codes + (size_t)row * rowb, pageb, pb);
+                            bulk_load(dst(buf, jp, 0), codes + (size_t)row * rowb, pageb, pb);
                         } else {
-                            for (int bx = 0; bx < nbox; ++bx)
-                                tma_load_2d(st + jp * pageb + bx * 2048, tm, pb, bx * 128, row);
+                            for (int bx = 0; bx < nbox; ++bx) tma_load_2d(dst(buf, jp, bx), tm, pb, bx * 128, row);
                         }
-                        bulk_load(ss + jp * scb, scl + (size_t)row * scrow, scb, pb);
+                        if (scb) bulk_load(ss + jp * scb, scl + (size_t)row * scrow, scb, pb);
                     }
                     // after an abort elsewhere, still let this copy land before the row is patched
                     if (!wait_or_flag(pb, pat_phase)) mbar_wait_bounded(pb, pat_phase);
                     pat_phase ^= 1;
+                    if (to_vp && (pc.L % kPage) != 0) {
+                        // rows past the sequence end hold whatever the pool has there; P' is 0 for
+                        // them, but 0 x NaN is not, so they are zeroed
+                        const int r0 = pc.L % kPage;
+                        for (int e = lane; e < (kPage - r0) * NA * 8; e += 32) {
+                            const int rw = r0 + e / (NA * 8), at = (e / 8) % NA, u = e % 8;
+                            *reinterpret_cast<uint4*>(dst(buf, jp, at) + rw * 128 + 16 * u) = make_uint4(0u, 0u, 0u, 0u);
+                        }
+                    }
+                }
+                if (jp >= 0 && p.k_new != nullptr) {
+                    const int row = (pid_patch * p.Hkv + kvh) * kPage;
                     uint8_t* rowbuf = sm + X::OFF_ROW + kind * 512;
                     const uint16_t* src = newsrc + ((size_t)pc.b * p.Hkv + kvh) * D;
                     if constexpr (X::ISO) {
                         constexpr int TT = FMT == 3 ? 1 : 0;
                         quantize_row<FMT == 3 ? ENC_ISO4 : ENC_ISO3, D>(src, rowbuf, rowbuf + 256, lane, p.quat,
                                                                         c_tc_levels[TT], c_tc_mids[TT]);
-                    } else if (VQ && kind) {
+                    } else if (kind ? VQ : X::KQ) {
                         quantize_row<ENC_Q4, D>(src, rowbuf, rowbuf + 256, lane, nullptr, nullptr, nullptr);
+                    } else if (kind ? X::VB : X::KB) {
+                        quantize_row<ENC_BF16, D>(src, rowbuf, rowbuf + 256, lane, nullptr, nullptr, nullptr);
                     } else {
                         quantize_row<ENC_INT8, D>(src, rowbuf, rowbuf + 256, lane, nullptr, nullptr, nullptr);
                     }
@@ -513,19 +552,28 @@ __global__ void __launch_bounds__(kThr, 1)
                     const long long grow = (long long)row + rr;
                     uint8_t* gcode = const_cast<uint8_t*>(codes) + grow * rowb;
                     uint8_t* gscale = const_cast<uint8_t*>(scl) + grow * scrow;
-                    uint8_t* scode = st + jp * pageb;
                     if (lane < rowb / 16) {
                         const uint4 v = *reinterpret_cast<const uint4*>(rowbuf + 16 * lane);
                         *reinterpret_cast<uint4*>(gcode + 16 * lane) = v;
-                        if constexpr (X::ISO) *reinterpret_cast<uint4*>(scode + rr * rowb + 16 * lane) = v;
-                        else *reinterpret_cast<uint4*>(scode + (lane >> 3) * 2048 + sw_off(rr, lane & 7)) = v;
+                        if constexpr (X::ISO) *reinterpret_cast<uint4*>(dst(buf, jp, 0) + rr * rowb + 16 * lane) = v;
+                        else *reinterpret_cast<uint4*>(dst(buf, jp, lane >> 3) + sw_off(rr, lane & 7)) = v;
                     }
                     if (lane < scrow / 2) {
                         const uint16_t v = reinterpret_cast<const uint16_t*>(rowbuf + 256)[lane];
                         reinterpret_cast<uint16_t*>(gscale)[lane] = v;
                         reinterpret_cast<uint16_t*>(ss + jp * scb + rr * scrow)[lane] = v;
                     }
-                    fence_proxy_async();   // before later TMA refills of these bytes
+                    __syncwarp();
+                }
+                if (to_vp && npg < kTP) {
+                    // pages the tile does not load: zero V' rows (stale shared memory may hold NaN)
+                    for (int e = lane; e < (kTP - npg) * NA * 128; e += 32) {
+                        const int pg = npg + e / (NA * 128), at = (e / 128) % NA, u = e % 128;
+                        *reinterpret_cast<uint4*>(dst(buf, pg, at) + 16 * u) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+                if (jp >= 0 || (to_vp && npg < kTP)) {
+                    fence_proxy_async();   // generic writes before the tensor core (and later TMA refills)
                     __syncwarp();
                 }
                 if (lane == 0) mbar_arrive(full);
@@ -533,13 +581,14 @@ __global__ void __launch_bounds__(kThr, 1)
         }
         // every copy issued above has landed before the CTA exits (bounded waits that do not
         // stop at the abort flag: the copies of an aborted launch still land in this CTA's memory)
-        for (uint32_t t = (T >= 2 ? T - 2 : 0); t < T; ++t)
-            if (!mbar_wait_bounded(fullb + (t & 1), (t >> 1) & 1)) atomicOr(&g_err_dtc, kErrWait);
+        for (uint32_t t = (T >= (uint32_t)nslot ? T - nslot : 0); t < T; ++t)
+            if (!mbar_wait_bounded(fullb + (nslot == 2 ? (t & 1) : 0), (nslot == 2 ? t >> 1 : t) & 1))
+                atomicOr(&g_err_dtc, kErrWait);
     } else if (warp == kWMma) {
         // =============================== MMA issue ===============================
         if (lane == 0) {
-            constexpr uint32_t IDQK = idesc_f16(128, 16);
-            constexpr uint32_t IDPV = idesc_f16(X::PM, D, 1, 1);
+            constexpr uint32_t IDQK = idesc_f16(128, 16, 0, 0, X::KB ? 1 : 0);      // bf16 K: bf16 operands
+            constexpr uint32_t IDPV = idesc_f16(X::PM, D, 1, 1, X::VB ? 1 : 0);     // bf16 V: bf16 P' and V'
             // base descriptors; every MMA adds a compile-time offset (16-byte units) to them
             const uint64_t qd0 = sw128_desc(smem_addr(sm + X::OFF_Q));
             const uint64_t vd0 = sw128_desc_lbo(smem_addr(sm + X::OFF_VP), 16384, 1024);
@@ -559,15 +608,19 @@ __global__ void __launch_bounds__(kThr, 1)
                 bool progressed = false;
                 if (hv && Tv < Tq) {
                     bool ready = mbar_test_wait(&bars[B_PFL], Tv & 1);
-                    if (ready) ready = mbar_test_wait(&bars[B_VCV], Tv & 1);
+                    // V' of the tile: converted, or (bf16 V) landed in its own V' tile
+                    if (ready) ready = X::VB ? mbar_test_wait(&bars[B_VF + (Tv & 1)], (Tv >> 1) & 1)
+                                             : mbar_test_wait(&bars[B_VCV], Tv & 1);
                     if (ready) {
                         tc_fence_after();
+                        const uint64_t vdt = vd0 + (uint64_t)(X::VB ? ((Tv & 1) * NA * 16384) >> 4 : 0);
                         // O[64 P' columns][D] += P'^T (MN-major, token rows) x V' (MN-major, token rows)
 #pragma unroll
                         for (int u = 0; u < kTok / 16; ++u)
-                            umma_f16(to, pd0 + (uint64_t)((u * 2048) >> 4), vd0 + (uint64_t)((u * 2048) >> 4), IDPV,
+                            umma_f16(to, pd0 + (uint64_t)((u * 2048) >> 4), vdt + (uint64_t)((u * 2048) >> 4), IDPV,
                                      (tv > 0 || u > 0));
                         umma_commit(&bars[B_PVD + (Tv & 1)]);
+                        if constexpr (X::VB) umma_commit(&bars[B_VE + (Tv & 1)]);   // the V' tile is free
                         ++Tv;
                         if (pv.p0 + kTP * (tv + 1) < pv.p1) {
                             ++tv;
@@ -581,12 +634,22 @@ __global__ void __launch_bounds__(kThr, 1)
                 if (hq && (!hv || Tq <= Tv + 1)) {
                     const bool first = tq == 0;
                     bool ready = mbar_test_wait(&bars[B_KCV], Tq & 1);
-                    if (ready && Tq >= 2) ready = mbar_test_wait(&bars[B_SF + (Tq & 1)], ((Tq >> 1) - 1) & 1);
+                    if (ready && Tq >= (uint32_t)X::NSB)
+                        ready = mbar_test_wait(&bars[B_SF + Tq % X::NSB], ((Tq / X::NSB) - 1) & 1);
                     if (ready && first) ready = mbar_test_wait(&bars[B_QRD], pieceq & 1);
                     if (ready) {
                         tc_fence_after();
-                        const uint32_t sd = tmem + X::SCOL + (Tq & 1) * X::SBUF;
-                        if constexpr (X::ISO) {
+                        const uint32_t sd = tmem + X::SCOL + (Tq % X::NSB) * X::SBUF;
+                        if constexpr (X::KQ) {
+                            // q4 K: one accumulator per 32-dim block (its own scale); two k-steps a
+                            // block against the rotated query's hi (N columns 0..7) and lo (8..15)
+#pragma unroll
+                            for (int u = 0; u < 2; ++u)
+#pragma unroll
+                                for (int g = 0; g < X::NKG; ++g)
+                                    umma_f16_ta(sd + 16 * g, tk + 8 * (2 * g + u),
+                                                qd0 + (uint64_t)(((g >> 1) * 2048 + (g & 1) * 64 + 32 * u) >> 4), IDQK, u > 0);
+                        } else if constexpr (X::ISO) {
                             // per 128-dim block: 8 k-steps against the query tile whose N columns hold
                             // the rotated query's fp16 hi (0..7) and lo (8..15) parts; even and odd
                             // k-steps go to two accumulators, so consecutive MMAs are independent
@@ -669,7 +732,12 @@ __global__ void __launch_bounds__(kThr, 1)
                 }
             }
         };
+        int v_npg = 0, v_pos0 = 0, v_len = 0;   // extent of the tile whose V is converted next
         auto convert_v = [&](uint32_t Tc) {
+            if constexpr (X::VB) return;   // the bf16 V tile lands in V' itself
+            // rows past the sequence end (or of pages the tile did not load) may hold anything in
+            // shared memory; the q4 path multiplies by a staged scale, so those rows are zeroed
+            const bool vrow_ok = jpage < v_npg && v_pos0 + r < v_len;
             const int buf = Tc & 1;
             wait_or_flag(&bars[B_VF + buf], (Tc >> 1) & 1);
             // V' is free once PV of the tile before read it
@@ -701,7 +769,7 @@ __global__ void __launch_bounds__(kThr, 1)
                     const int blk = (D / 64) * hf + bi;
                     const uint4 x = *reinterpret_cast<const uint4*>(slot + sw_off(rr, blk));
                     const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
-                    const uint32_t sb = vsr[blk], s2 = sb | (sb << 16);
+                    const uint32_t sb = vrow_ok ? (uint32_t)vsr[blk] : 0u, s2 = sb | (sb << 16);
                     uint32_t lo[8], hi[8];
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
@@ -746,9 +814,10 @@ __global__ void __launch_bounds__(kThr, 1)
         Piece pc;
         while (walker.next(p, pc)) {
             for (int pg0 = pc.p0; pg0 < pc.p1; pg0 += kTP, ++T) {
-                const int buf = T & 1;
-                // ---- K of tile T: exact fp16 1152 + c, one token per TMEM lane ----
-                wait_or_flag(&bars[B_KF + buf], (T >> 1) & 1);
+                const int buf = X::KSTB == 2 ? (int)(T & 1) : 0;
+                // ---- K of tile T: exact fp16 1152 + c (int8), q - 8 (q4) or the bf16 values, one
+                // token per TMEM lane ----
+                wait_or_flag(&bars[B_KF + buf], (X::KSTB == 2 ? T >> 1 : T) & 1);
                 if (T >= 1) wait_or_flag(&bars[B_QKD + ((T - 1) & 1)], ((T - 1) >> 1) & 1);
                 tc_fence_after();
                 if constexpr (X::ISO) {
@@ -767,6 +836,48 @@ __global__ void __launch_bounds__(kThr, 1)
                             w[16 + i] = w1[i];
                         }
                         tmem_st32_nowait(tmem + lb + X::KCOL + p0, w);
+                    }
+                    tmem_wait_st();
+                } else if constexpr (X::KQ) {
+                    // q4_0 block b of the rotated row -> exact fp16 q - 8 into TMEM columns 16 b ..
+                    // 16 b + 15 (low-nibble pairs, then high-nibble pairs: position p of the block
+                    // holds element perm4(p), as in the int8 path)
+                    const uint8_t* slot = sm + X::OFF_KST + (buf * kTP + jpage) * X::PAGE_B;
+#pragma unroll
+                    for (int b2 = 0; b2 < 2; ++b2) {
+                        uint32_t w[32];
+#pragma unroll
+                        for (int bb = 0; bb < 2; ++bb) {
+                            const int blk = 4 * hf + 2 * b2 + bb;
+                            const uint4 x = *reinterpret_cast<const uint4*>(slot + sw_off(rr, blk));
+                            const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                w[16 * bb + 2 * k] = hsub2_u32((xs[k] & 0x000f000fu) | 0x64006400u, 0x64086408u);
+                                w[16 * bb + 2 * k + 1] = hsub2_u32(((xs[k] >> 8) & 0x000f000fu) | 0x64006400u, 0x64086408u);
+                                w[16 * bb + 8 + 2 * k] = hsub2_u32(((xs[k] >> 4) & 0x000f000fu) | 0x64006400u, 0x64086408u);
+                                w[16 * bb + 8 + 2 * k + 1] = hsub2_u32(((xs[k] >> 12) & 0x000f000fu) | 0x64006400u, 0x64086408u);
+                            }
+                        }
+                        tmem_st32_nowait(tmem + lb + X::KCOL + 16 * (4 * hf + 2 * b2), w);
+                    }
+                    tmem_wait_st();
+                } else if constexpr (X::KB) {
+                    // bf16 K: the staged values as they are, dims 2 c, 2 c + 1 in TMEM column c
+                    const uint8_t* slot = sm + X::OFF_KST + jpage * X::PAGE_B;
+#pragma unroll
+                    for (int i0 = 0; i0 < D / 16; i0 += 8) {
+                        uint32_t w[32];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int gc = hf * (D / 16) + i0 + i;   // 16-byte chunk = 8 dims
+                            const uint4 x = *reinterpret_cast<const uint4*>(slot + (gc >> 3) * 2048 + sw_off(rr, gc & 7));
+                            w[4 * i] = x.x;
+                            w[4 * i + 1] = x.y;
+                            w[4 * i + 2] = x.z;
+                            w[4 * i + 3] = x.w;
+                        }
+                        tmem_st32_nowait(tmem + lb + X::KCOL + 4 * (hf * (D / 16) + i0), w);
                     }
                     tmem_wait_st();
                 } else {
@@ -797,6 +908,9 @@ __global__ void __launch_bounds__(kThr, 1)
                 }
                 // ---- V of tile T - 1 ----
                 if (T >= 1) convert_v(T - 1);
+                v_npg = min(kTP, pc.p1 - pg0);
+                v_pos0 = pg0 * kPage;
+                v_len = pc.L;
             }
         }
         if (T >= 1) convert_v(T - 1);
@@ -818,8 +932,50 @@ __global__ void __launch_bounds__(kThr, 1)
             // ---- query tile (B operand, K-major, dims in converter order) and the offset sums ----
             {
                 uint8_t* qsm = sm + X::OFF_Q;
-                // ISO: rows n < 8 take the rotated query's fp16 hi part, rows 8 + n its lo part
-                constexpr int QROWS = X::ISO ? 8 : 16;
+                // q4 K: the query rotated by the FWHT-256 (x 1/16) in fp32 first, in the P' area
+                // (free between pieces): thread (head hh, slice q16) takes strides 16 .. 128 on
+                // dims q16 + 16 k, then strides 1 .. 8 on dims 16 q16 + i
+                float* qrot = reinterpret_cast<float*>(sm + X::OFF_PP);   // [8][D]
+                if constexpr (X::KQ) {
+                    const int hh = r >> 4, q16 = r & 15;
+                    if (hh < G) {
+                        const uint16_t* qrow = p.q + ((size_t)pc.b * p.Hq + hq0 + hh) * D;
+                        float x[16];
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) x[k] = bf16_bits_to_f32(qrow[q16 + 16 * k]);
+#pragma unroll
+                        for (int st = 1; st < 16; st <<= 1)
+#pragma unroll
+                            for (int k = 0; k < 16; ++k)
+                                if ((k & st) == 0) {
+                                    const float a0 = x[k], a1 = x[k + st];
+                                    x[k] = a0 + a1;
+                                    x[k + st] = a0 - a1;
+                                }
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) qrot[hh * D + q16 + 16 * k] = x[k];
+                    }
+                    soft_sync();
+                    if (hh < G) {
+                        float y[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) y[i] = qrot[hh * D + 16 * q16 + i];
+#pragma unroll
+                        for (int st = 1; st < 16; st <<= 1)
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                if ((i & st) == 0) {
+                                    const float a0 = y[i], a1 = y[i + st];
+                                    y[i] = a0 + a1;
+                                    y[i + st] = a0 - a1;
+                                }
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) qrot[hh * D + 16 * q16 + i] = y[i] * 0.0625f;
+                    }
+                    soft_sync();
+                }
+                // ISO and q4 K: rows n < 8 take the transformed query's fp16 hi part, rows 8 + n its lo part
+                constexpr int QROWS = X::QHL ? 8 : 16;
                 for (int idx = r; idx < QROWS * NA * 8; idx += 128) {
                     const int n = idx / (NA * 8), rem = idx % (NA * 8), a = rem >> 3, cc = rem & 7;
                     uint32_t w[4] = {0u, 0u, 0u, 0u}, wl[4] = {0u, 0u, 0u, 0u};
@@ -828,7 +984,11 @@ __global__ void __launch_bounds__(kThr, 1)
                         const uint4 raw = *reinterpret_cast<const uint4*>(qrow);
                         const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
                         float v[8];
-                        if constexpr (X::ISO) {
+                        if constexpr (X::KQ) {
+                            // positions in the q4 K' order (perm4 inside each group of four)
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) v[e] = qrot[n * D + 64 * a + 8 * cc + perm4(e)];
+                        } else if constexpr (X::ISO) {
                             // natural dim order; each 4-D group rotated: <q, conj(R) c> = <R q, c>
 #pragma unroll
                             for (int e = 0; e < 8; ++e) v[e] = bf16_bits_to_f32((rw[e >> 1] >> (16 * (e & 1))) & 0xffffu);
@@ -849,9 +1009,9 @@ __global__ void __launch_bounds__(kThr, 1)
                             }
                         }
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) w[k] = f32x2_to_h2(v[2 * k], v[2 * k + 1]);
-                        if constexpr (X::ISO) {
-                            // the fp16 remainder of the rotated query
+                        for (int k = 0; k < 4; ++k) w[k] = X::KB ? rw[k] : f32x2_to_h2(v[2 * k], v[2 * k + 1]);   // bf16 K: bf16 query as it is
+                        if constexpr (X::QHL) {
+                            // the fp16 remainder of the transformed query
 #pragma unroll
                             for (int k = 0; k < 4; ++k) {
                                 const float2 f = h2_to_f32x2(w[k]);
@@ -860,7 +1020,7 @@ __global__ void __launch_bounds__(kThr, 1)
                         }
                     }
                     *reinterpret_cast<uint4*>(qsm + a * 2048 + sw_off(n, cc)) = make_uint4(w[0], w[1], w[2], w[3]);
-                    if constexpr (X::ISO)
+                    if constexpr (X::QHL)
                         *reinterpret_cast<uint4*>(qsm + a * 2048 + sw_off(8 + n, cc)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
                 }
                 // 1152 * (sum of the fp16 query over each 64-dim group): thread -> (head, D / 16 dims)
@@ -874,7 +1034,9 @@ __global__ void __launch_bounds__(kThr, 1)
                 }
 #pragma unroll
                 for (int off = 1; off < TPG; off <<= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-                if (h < G && (r & 15) % TPG == 0) bias_s[(s0 / 64) * 8 + h] = X::ISO ? 0.0f : 1152.0f * part;
+                // only the int8 K' carries the 1152 offset
+                constexpr bool KI8 = !X::ISO && !X::KQ && !X::KB;
+                if (h < G && (r & 15) % TPG == 0) bias_s[(s0 / 64) * 8 + h] = KI8 ? 1152.0f * part : 0.0f;
             }
             fence_proxy_async();
             soft_sync();
@@ -900,30 +1062,39 @@ __global__ void __launch_bounds__(kThr, 1)
                 const int pos = (pg0 + jpage) * kPage + (r & 15);
                 const bool valid = jpage < npg && pos < pc.L;
                 // ---- scores ----
-                wait_or_flag(&bars[B_KF + buf], ph);
                 float ks[X::NKG];
-                {
+                if constexpr (X::KB) {
+#pragma unroll
+                    for (int g = 0; g < X::NKG; ++g) ks[g] = 1.0f;   // the bf16 K carries no scale
+                } else {
+                    const int kb = X::KSTB == 2 ? buf : 0;
+                    wait_or_flag(&bars[B_KF + kb], (X::KSTB == 2 ? T >> 1 : T) & 1);
                     // one fp16 scale per group (ISO4 rows carry 2 reserved bytes after each)
-                    const uint16_t* ksr = reinterpret_cast<const uint16_t*>(sm + X::OFF_KSC + (buf * kTP + jpage) * X::SC_B +
+                    const uint16_t* ksr = reinterpret_cast<const uint16_t*>(sm + X::OFF_KSC + (kb * kTP + jpage) * X::SC_B +
                                                                             (r & 15) * X::KSROW);
 #pragma unroll
                     for (int g = 0; g < X::NKG; ++g) ks[g] = f16_bits_to_f32(ksr[g * (X::ISO ? X::ISO_SB / 2 : 1)]);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars[B_KE + kb]);
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[B_KE + buf]);
                 wait_or_flag(&bars[B_QKD + buf], ph);
                 tc_fence_after();
                 float s[G];
 #pragma unroll
                 for (int h = 0; h < G; ++h) s[h] = 0.0f;
+                const uint32_t sbuf = tmem + lb + X::SCOL + (T % X::NSB) * X::SBUF;
 #pragma unroll
                 for (int g = 0; g < X::NKG; ++g) {
                     float v[16];
-                    tmem_ld16(tmem + lb + X::SCOL + buf * X::SBUF + 16 * X::SACC * g, v);
-                    if constexpr (X::ISO) {
+                    tmem_ld16(sbuf + 16 * X::SACC * g, v);
+                    if constexpr (X::KQ) {
+                        // hi + lo columns of the rotated query; exact codes q - 8, the block's scale
+#pragma unroll
+                        for (int h = 0; h < G; ++h) s[h] += ks[g] * (v[h] + v[8 + h]);
+                    } else if constexpr (X::ISO) {
                         // hi + lo columns of the even k-steps, then of the odd ones
                         float v2[16];
-                        tmem_ld16(tmem + lb + X::SCOL + buf * X::SBUF + 16 * X::SACC * g + 16, v2);
+                        tmem_ld16(sbuf + 16 * X::SACC * g + 16, v2);
 #pragma unroll
                         for (int h = 0; h < G; ++h) s[h] += ks[g] * ((v[h] + v[8 + h]) + (v2[h] + v2[8 + h]));
                     } else {
@@ -933,15 +1104,15 @@ __global__ void __launch_bounds__(kThr, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[B_SF + buf]);
+                if (lane == 0) mbar_arrive(&bars[B_SF + T % X::NSB]);
 #pragma unroll
                 for (int h = 0; h < G; ++h) s[h] = valid ? s[h] * p.scale_log2 : -INFINITY;
                 // ---- V scales ----
-                wait_or_flag(&bars[B_VF + buf], ph);
                 float vsf[X::VG];
                 int e_row = 0;
-                if constexpr (VQ) {
-                    // the q4 block scales are folded into V' by the converters
+                if constexpr (!X::VB) wait_or_flag(&bars[B_VF + buf], ph);
+                if constexpr (VQ || X::VB) {
+                    // the q4 block scales are folded into V' by the converters; the bf16 V has none
 #pragma unroll
                     for (int g = 0; g < X::VG; ++g) vsf[g] = 1.0f;
                     e_row = 15;   // the fp16 exponent field of 1.0
@@ -954,8 +1125,10 @@ __global__ void __launch_bounds__(kThr, 1)
                         e_row = max(e_row, (int)((hb & 0x7fffu) >> 10));
                     }
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[B_VE + buf]);
+                if constexpr (!X::VB) {   // the bf16 V tile is released by the PV commit
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars[B_VE + buf]);
+                }
                 if (!valid) e_row = 0;
                 // ---- frame: all 128 threads agree on the max and the range exponent ----
                 bool need = false;
@@ -1037,9 +1210,18 @@ __global__ void __launch_bounds__(kThr, 1)
                             for (int h = 0; h < 8; ++h) P[h] = h < G ? pr[h < G ? h : 0] * sc : 0.0f;
 #pragma unroll
                             for (int k = 0; k < 4; ++k) {
-                                hw[k] = f32x2_to_h2(P[2 * k], P[2 * k + 1]);
-                                const float2 f = h2_to_f32x2(hw[k]);
-                                lw[k] = f32x2_to_h2(P[2 * k] - f.x, P[2 * k + 1] - f.y);
+                                if constexpr (X::VB) {
+                                    // bf16 V': P' in bf16 hi + lo (the operands of one MMA share a type)
+                                    __nv_bfloat162 hb = __floats2bfloat162_rn(P[2 * k], P[2 * k + 1]);
+                                    const float2 f = __bfloat1622float2(hb);
+                                    __nv_bfloat162 lb2 = __floats2bfloat162_rn(P[2 * k] - f.x, P[2 * k + 1] - f.y);
+                                    hw[k] = *reinterpret_cast<uint32_t*>(&hb);
+                                    lw[k] = *reinterpret_cast<uint32_t*>(&lb2);
+                                } else {
+                                    hw[k] = f32x2_to_h2(P[2 * k], P[2 * k + 1]);
+                                    const float2 f = h2_to_f32x2(hw[k]);
+                                    lw[k] = f32x2_to_h2(P[2 * k] - f.x, P[2 * k + 1] - f.y);
+                                }
                             }
                         }
                         uint8_t* pa = pp + (g >> 2) * 16384;   // 64 P' columns (4 groups) per atom
@@ -1173,6 +1355,10 @@ __global__ void __launch_bounds__(kThr, 1)
                                 o[4 * k + 2] = (q0 * c0 + q1 * dd - q2 * a0 - q3 * b0) * inv;
                                 o[4 * k + 3] = (q0 * dd - q1 * c0 + q2 * b0 - q3 * a0) * inv;
                             }
+                        } else if constexpr (X::VB) {
+                            // the bf16 V' holds dims in natural order
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) o[j] = v[j] * inv;
                         } else {
 #pragma unroll
                             for (int j = 0; j < 16; ++j) o[perm4(j)] = v[j] * inv;
@@ -1446,15 +1632,19 @@ static cudaError_t launch_tc_g(int G, int grid, const CUtensorMap& tk, const CUt
     return cudaErrorInvalidValue;
 }
 
-// fmt: 0 int8 (head_dim 128 or 256), 1 k8v4 (256), 2 ISO3 and 3 ISO4 (128 or 256); the
+// fmt: 0 int8 (head_dim 128 or 256), 1 k8v4 (256), 2 ISO3 and 3 ISO4 (128 or 256), 4 q4 (256),
+// 5 int8 K + bf16 V and 6 bf16 K + int8 V (128 or 256); the
 // tensor maps are used for int8 and q4 code planes only
 cudaError_t decode_tc_launch(int D, int G, int grid, int fmt, const CUtensorMap& tk, const CUtensorMap& tv,
                              const DecodeParams& p, cudaStream_t st) {
     grid = grid < kMaxGrid ? grid : kMaxGrid;
     if (fmt == 1) return D == 256 ? launch_tc_g<256, 1>(G, grid, tk, tv, p, st) : cudaErrorInvalidValue;
+    if (fmt == 4) return D == 256 ? launch_tc_g<256, 4>(G, grid, tk, tv, p, st) : cudaErrorInvalidValue;
     if (D != 128 && D != 256) return cudaErrorInvalidValue;
     switch (fmt) {
         case 0: return D == 256 ? launch_tc_g<256, 0>(G, grid, tk, tv, p, st) : launch_tc_g<128, 0>(G, grid, tk, tv, p, st);
+        case 5: return D == 256 ? launch_tc_g<256, 5>(G, grid, tk, tv, p, st) : launch_tc_g<128, 5>(G, grid, tk, tv, p, st);
+        case 6: return D == 256 ? launch_tc_g<256, 6>(G, grid, tk, tv, p, st) : launch_tc_g<128, 6>(G, grid, tk, tv, p, st);
         case 2: return D == 256 ? launch_tc_g<256, 2>(G, grid, tk, tv, p, st) : launch_tc_g<128, 2>(G, grid, tk, tv, p, st);
         case 3: return D == 256 ? launch_tc_g<256, 3>(G, grid, tk, tv, p, st) : launch_tc_g<128, 3>(G, grid, tk, tv, p, st);
     }

@@ -51,14 +51,19 @@ constexpr int kXProd = kXSoft / 32, kXMma = kXProd + 2;
 // shared-memory map (bytes from a 1 KB aligned base). ISO prefix tiles take the rotated
 // query as two fp16 tiles: hi in the query region (which holds the plain query once the
 // prefix is done) and the fp16 remainder lo in one more tile after the rest.
-template <int D, bool ISO = false>
+// XM: the kind of prefix tile. 0: plain keys; 1: ISO (raw levels against the rotated query,
+// fp16 hi + lo); 2: two key planes, fp16 hi + lo, against the plain query (q4 keys rotated
+// back to the original domain).
+template <int D, int XM = 0>
 struct XGeo {
+    static constexpr bool ISO = XM == 1;
     static constexpr int NA = D / 64;                    // 64-dim atoms (= K scale groups)
     static constexpr int OFF_Q = 0;                      // NA atoms x 128 rows x 128 B
     static constexpr int Q_BYTES = NA * 128 * 128;
-    // K and V staging depth: two tiles, one for ISO at head_dim 256 (where the rotated query's
-    // lo tile takes the room of the second K and V buffers)
-    static constexpr int NB = (ISO && D == 256) ? 1 : 2;
+    // K and V staging depth: two tiles, one at head_dim 256 when the prefix tiles need an extra
+    // tile (ISO: the rotated query's lo part; XM 2: the lo key plane), which takes the room of
+    // the second K and V buffers
+    static constexpr int NB = (XM != 0 && D == 256) ? 1 : 2;
     static constexpr int OFF_K = OFF_Q + Q_BYTES;        // NB buffers x NA atoms x 64 rows x 128 B
     static constexpr int K_BYTES = NA * 64 * 128;
     static constexpr int OFF_V = OFF_K + NB * K_BYTES;   // NB buffers x D rows x 128 B
@@ -69,8 +74,9 @@ struct XGeo {
     static constexpr int OFF_RED = OFF_KS + NB * KS_BYTES;   // [2 tiles][kXSplit parts][128 rows] row-max / row-sum exchange
     static constexpr int OFF_BAR = OFF_RED + 2 * kXSplit * 128 * 4;
     static constexpr int OFF_TMEM = OFF_BAR + 24 * 8;
-    static constexpr int OFF_QR = (OFF_TMEM + 16 + 1023) / 1024 * 1024;   // ISO: the lo tile (Q_BYTES)
-    static constexpr int SMEM = ISO ? OFF_QR + Q_BYTES : OFF_TMEM + 16;
+    static constexpr int OFF_QR = (OFF_TMEM + 16 + 1023) / 1024 * 1024;   // the extra tile: lo query (ISO) or lo keys
+    static constexpr int SMEM = XM ? OFF_QR + Q_BYTES : OFF_TMEM + 16;
+    static_assert(K_BYTES <= Q_BYTES, "a lo key tile fits the extra tile");
     static constexpr int S_COLS = NA * 64;               // TMEM columns of the group scores
     static constexpr int TMEM_COLS = 512;
     static_assert(S_COLS + D <= TMEM_COLS, "TMEM budget");
@@ -126,10 +132,58 @@ __device__ __forceinline__ void quat_conj_mul(const float* q, float a, float b, 
     u[3] = q[0] * d - q[1] * c + q[2] * b - q[3] * a;
 }
 
+// FWHT-256 x 1/16 of one row held by its four threads (64 values each, thread qd owns
+// dims [64 qd, 64 qd + 64)): butterflies at distances 1 .. 32 inside the thread, 64 and
+// 128 across the threads (lanes qd ^ 1, qd ^ 2). Every lane of the warp must call it.
+__device__ __forceinline__ void fwht256_rows4(float (&x)[64], int qd) {
+#pragma unroll
+    for (int h = 1; h < 64; h <<= 1) {
+#pragma unroll
+        for (int e = 0; e < 64; ++e) {
+            if (e & h) continue;
+            const float a = x[e], c = x[e + h];
+            x[e] = a + c;
+            x[e + h] = a - c;
+        }
+    }
+#pragma unroll
+    for (int m = 1; m <= 2; m <<= 1) {
+        const bool upper = (qd & m) != 0;
+#pragma unroll
+        for (int e = 0; e < 64; ++e) {
+            const float o = __shfl_xor_sync(0xffffffffu, x[e], m);
+            x[e] = upper ? o - x[e] : x[e] + o;
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 64; ++e) x[e] *= 0.0625f;
+}
+
+// the q4_0 values (q - 8) * d of blocks 2 qd and 2 qd + 1 of a rotated row (x: 64 values)
+__device__ __forceinline__ void q4_blocks2(const uint8_t* code_row, const uint8_t* scale_row, int qd, float (&x)[64]) {
+    const uint8_t* src = code_row + 32 * qd;
+    const uint16_t* sc = reinterpret_cast<const uint16_t*>(scale_row);
+#pragma unroll
+    for (int lb = 0; lb < 2; ++lb) {
+        const float d16 = f16_bits_to_f32(sc[2 * qd + lb]);
+        const uint4 v4 = *reinterpret_cast<const uint4*>(src + 16 * lb);
+        const uint32_t w4[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const uint32_t byte = (w4[j >> 2] >> (8 * (j & 3))) & 0xffu;
+            x[32 * lb + j] = (float)((int)(byte & 15u) - 8) * d16;
+            x[32 * lb + j + 16] = (float)((int)(byte >> 4) - 8) * d16;
+        }
+    }
+}
+
 template <int D, int FMT>
 __global__ void __launch_bounds__(256) extend_prep_kernel(const ExtendParams p) {
     constexpr int NA = D / 64, QD = D / 4;
-    constexpr bool ISO = FMT >= 2;
+    constexpr bool ISO = FMT == 2 || FMT == 3;
+    constexpr bool KI8 = FMT == 0 || FMT == 1 || FMT == 5, VI8 = FMT == 0 || FMT == 6;
+    constexpr bool KQ4 = FMT == 4, VQ4 = FMT == 1 || FMT == 4;
+    constexpr bool KB16 = FMT == 6, VB16 = FMT == 5;
     __shared__ __align__(16) uint16_t vt[D][kXT + 8];
     const int b = blockIdx.z, kvh = blockIdx.y, t = blockIdx.x;
     const int cu0 = p.cu[b], T = max(0, p.cu[b + 1] - cu0);
@@ -140,13 +194,17 @@ __global__ void __launch_bounds__(256) extend_prep_kernel(const ExtendParams p) 
     const int tid = threadIdx.x, i = tid >> 2, qd = tid & 3;
     const bool prefix = t < NTP;
     const size_t krow = ((size_t)b * p.Hkv + kvh) * p.Lmax + (size_t)kXT * t + i;
-    uint32_t kw[QD / 2], vw[QD / 2];
+    uint32_t kw[QD / 2], vw[QD / 2], kl[KQ4 ? QD / 2 : 1];
     float ksv[NA];
-    // k8v4: the thread's 64 rotated V values; zero for rows past the prefix, so that the
+    // q4 V (and K): the thread's 64 rotated values; zero for rows past the prefix, so that the
     // cross-thread butterflies below run on every lane of the warp
-    float xr[FMT == 1 ? 64 : 1];
+    float xr[VQ4 ? 64 : 1], xk[KQ4 ? 64 : 1];
 #pragma unroll
-    for (int e = 0; e < (FMT == 1 ? 64 : 1); ++e) xr[e] = 0.0f;
+    for (int e = 0; e < (VQ4 ? 64 : 1); ++e) xr[e] = 0.0f;
+#pragma unroll
+    for (int e = 0; e < (KQ4 ? 64 : 1); ++e) xk[e] = 0.0f;
+#pragma unroll
+    for (int k = 0; k < (KQ4 ? QD / 2 : 1); ++k) kl[k] = 0u;
 #pragma unroll
     for (int g = 0; g < NA; ++g) ksv[g] = 0.0f;
 #pragma unroll
@@ -163,7 +221,30 @@ __global__ void __launch_bounds__(256) extend_prep_kernel(const ExtendParams p) 
         }
         if (page >= 0) {
             const long long row = ((long long)page * p.Hkv + kvh) * kPage + (pos & 15);
-            if constexpr (!ISO) {
+            if constexpr (KB16) {
+                // the unquantized bf16 K: fp16 (exact in fp16's normal range), key scale 1
+                const uint4* ksrc = reinterpret_cast<const uint4*>(p.kc + row * 2 * D) + (QD * qd) / 8;
+#pragma unroll
+                for (int c = 0; c < QD / 8; ++c) {
+                    const uint4 kx = ksrc[c];
+                    kw[4 * c + 0] = bf16x2_to_h2(kx.x);
+                    kw[4 * c + 1] = bf16x2_to_h2(kx.y);
+                    kw[4 * c + 2] = bf16x2_to_h2(kx.z);
+                    kw[4 * c + 3] = bf16x2_to_h2(kx.w);
+                }
+                if (qd == 0) {
+#pragma unroll
+                    for (int g = 0; g < NA; ++g) ksv[g] = p.scale_log2;
+                }
+            } else if constexpr (KQ4) {
+                // q4 K: (q - 8) * d of the rotated row; rotated back and split into fp16 hi + lo
+                // below, where every lane of the warp takes part
+                q4_blocks2(p.kc + row * (D / 2), p.ks + row * (D / 16), qd, xk);
+                if (qd == 0) {
+#pragma unroll
+                    for (int g = 0; g < NA; ++g) ksv[g] = p.scale_log2;
+                }
+            } else if constexpr (KI8) {
                 // int8 K: exact codes, fp32 group scales
                 const uint8_t* ksrc = p.kc + row * D + QD * qd;
 #pragma unroll
@@ -183,7 +264,18 @@ __global__ void __launch_bounds__(256) extend_prep_kernel(const ExtendParams p) 
                         ksv[g] = f16_bits_to_f32(reinterpret_cast<const uint16_t*>(p.ks + row * NA * 2)[g]) * p.scale_log2;
                 }
             }
-            if constexpr (FMT == 0) {
+            if constexpr (VB16) {
+                // the unquantized bf16 V: fp16 (exact in fp16's normal range)
+                const uint4* vsrc = reinterpret_cast<const uint4*>(p.vc + row * 2 * D) + (QD * qd) / 8;
+#pragma unroll
+                for (int c = 0; c < QD / 8; ++c) {
+                    const uint4 vx = vsrc[c];
+                    vw[4 * c + 0] = bf16x2_to_h2(vx.x);
+                    vw[4 * c + 1] = bf16x2_to_h2(vx.y);
+                    vw[4 * c + 2] = bf16x2_to_h2(vx.z);
+                    vw[4 * c + 3] = bf16x2_to_h2(vx.w);
+                }
+            } else if constexpr (VI8) {
                 const uint8_t* vsrc = p.vc + row * D + QD * qd;
                 const uint32_t vsb = reinterpret_cast<const uint16_t*>(p.vs + row * NA * 2)[(QD * qd) / 64];
                 const uint32_t sv2 = vsb | (vsb << 16);
@@ -200,24 +292,10 @@ __global__ void __launch_bounds__(256) extend_prep_kernel(const ExtendParams p) 
                         vw[8 * c + 2 * u + 1] = hfma2_u32(c23, sv2, 0u);
                     }
                 }
-            } else if constexpr (FMT == 1) {
+            } else if constexpr (VQ4) {
                 // q4_0 V, blocks 2 qd and 2 qd + 1 of the rotated row (16 code bytes + one fp16 d each)
-                static_assert(D == 256, "k8v4 V is FWHT-256 rotated");
-                float (&x)[64] = xr;
-                const uint8_t* vsrc = p.vc + row * (D / 2) + 32 * qd;
-                const uint16_t* vsc = reinterpret_cast<const uint16_t*>(p.vs + row * (D / 16));
-#pragma unroll
-                for (int lb = 0; lb < 2; ++lb) {
-                    const float d16 = f16_bits_to_f32(vsc[2 * qd + lb]);
-                    const uint4 v4 = *reinterpret_cast<const uint4*>(vsrc + 16 * lb);
-                    const uint32_t w4[4] = {v4.x, v4.y, v4.z, v4.w};
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const uint32_t byte = (w4[j >> 2] >> (8 * (j & 3))) & 0xffu;
-                        x[32 * lb + j] = (float)((int)(byte & 15u) - 8) * d16;
-                        x[32 * lb + j + 16] = (float)((int)(byte >> 4) - 8) * d16;
-                    }
-                }
+                static_assert(D == 256, "q4 V is FWHT-256 rotated");
+                q4_blocks2(p.vc + row * (D / 2), p.vs + row * (D / 16), qd, xr);
                 // rotated back after this branch, where every lane of the warp takes part
             } else {
                 // ISO3 / ISO4: dims [QD qd, QD qd + QD) lie in block nb at offset j0
@@ -263,33 +341,24 @@ __global__ void __launch_bounds__(256) extend_prep_kernel(const ExtendParams p) 
                 }
             }
         }
-        if constexpr (FMT == 1) {
-            // k8v4 V back to the original domain: the FWHT-256 (x 1/16) is its own inverse.
-            // Butterflies at distances 1 .. 32 inside the thread's 64 values, then 64 and 128
-            // across the four threads of the row (lanes qd ^ 1, qd ^ 2). `prefix` is uniform
-            // over the block, so every lane of the warp reaches the shuffles; rows past the
-            // prefix carry zeros and stay zero.
+        if constexpr (VQ4) {
+            // q4 V back to the original domain: the FWHT-256 (x 1/16) is its own inverse.
+            // `prefix` is uniform over the block, so every lane of the warp reaches the shuffles;
+            // rows past the prefix carry zeros and stay zero.
+            fwht256_rows4(xr, qd);
 #pragma unroll
-            for (int h = 1; h < 64; h <<= 1) {
+            for (int k = 0; k < 32; ++k) vw[k] = f32x2_to_h2(xr[2 * k], xr[2 * k + 1]);
+        }
+        if constexpr (KQ4) {
+            // q4 K back to the original domain, as fp16 hi + the fp16 remainder lo (two key planes:
+            // one fp16 rounding of the rotated-back key would move scores by more than the bound)
+            fwht256_rows4(xk, qd);
 #pragma unroll
-                for (int e = 0; e < 64; ++e) {
-                    if (e & h) continue;
-                    const float a = xr[e], c = xr[e + h];
-                    xr[e] = a + c;
-                    xr[e + h] = a - c;
-                }
+            for (int k = 0; k < 32; ++k) {
+                kw[k] = f32x2_to_h2(xk[2 * k], xk[2 * k + 1]);
+                const float2 f = h2_to_f32x2(kw[k]);
+                kl[k] = f32x2_to_h2(xk[2 * k] - f.x, xk[2 * k + 1] - f.y);
             }
-#pragma unroll
-            for (int m = 1; m <= 2; m <<= 1) {
-                const bool upper = (qd & m) != 0;
-#pragma unroll
-                for (int e = 0; e < 64; ++e) {
-                    const float o = __shfl_xor_sync(0xffffffffu, xr[e], m);
-                    xr[e] = upper ? o - xr[e] : xr[e] + o;
-                }
-            }
-#pragma unroll
-            for (int k = 0; k < 32; ++k) vw[k] = f32x2_to_h2(xr[2 * k] * 0.0625f, xr[2 * k + 1] * 0.0625f);
         }
     } else {
         const int n = kXT * (t - NTP) + i;
@@ -316,6 +385,12 @@ __global__ void __launch_bounds__(256) extend_prep_kernel(const ExtendParams p) 
     uint4* kdst = reinterpret_cast<uint4*>(p.xk + krow * D + QD * qd);
 #pragma unroll
     for (int c = 0; c < QD / 8; ++c) kdst[c] = make_uint4(kw[4 * c], kw[4 * c + 1], kw[4 * c + 2], kw[4 * c + 3]);
+    if constexpr (KQ4) {
+        // the lo key plane (zero for the chunk's new tokens, which are exact in the hi plane)
+        uint4* ldst = reinterpret_cast<uint4*>(p.xklo + krow * D + QD * qd);
+#pragma unroll
+        for (int c = 0; c < QD / 8; ++c) ldst[c] = make_uint4(kl[4 * c], kl[4 * c + 1], kl[4 * c + 2], kl[4 * c + 3]);
+    }
     if (qd == 0) {
 #pragma unroll
         for (int g = 0; g < NA; ++g) p.xs[krow * NA + g] = ksv[g];
@@ -338,10 +413,12 @@ __global__ void __launch_bounds__(256) extend_prep_kernel(const ExtendParams p) 
 // key scale, and the prefix tiles take the query rotated per 4-D group (<q_h, conj(R) c>
 // = <R q_h, c>), held as fp16 hi + lo so that Q K^T sees the fp32 rotated query; the
 // bf16 new tokens take the plain query.
-template <int D, int G, bool ISO>
+template <int D, int G, int XM>
 __global__ void __launch_bounds__(kXThreads, 1)
     extend_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const ExtendParams p) {
-    using X = XGeo<D, ISO>;
+    using X = XGeo<D, XM>;
+    constexpr bool ISO = XM == 1, KLO = XM == 2;
+    static_assert(!KLO || D == 256, "two key planes: q4 keys, head_dim 256");
     constexpr int NA = X::NA;
     constexpr int TPT = 128 / G;   // tokens per tile
     extern __shared__ __align__(1024) uint8_t xsmem_raw[];
@@ -417,10 +494,17 @@ __global__ void __launch_bounds__(kXThreads, 1)
                 uint64_t* bar = &bars[full0 + buf];
                 const int krow0 = hrow * p.Lmax + kXT * j;
                 if (isk) {
-                    mbar_arrive_expect_tx(bar, X::K_BYTES + X::KS_BYTES);
+                    const bool lo = KLO && j < NTP;   // prefix tile with a lo key plane
+                    mbar_arrive_expect_tx(bar, X::K_BYTES * (lo ? 2 : 1) + X::KS_BYTES);
 #pragma unroll
                     for (int g = 0; g < NA; ++g)
                         tma_load_2d(sm + X::OFF_K + buf * X::K_BYTES + g * 8192, &tmK, bar, 64 * g, krow0);
+                    if (lo) {
+                        // the lo plane follows the hi plane in the workspace (rows + B Hkv Lmax)
+                        const int lrow0 = krow0 + p.B * p.Hkv * p.Lmax;
+#pragma unroll
+                        for (int g = 0; g < NA; ++g) tma_load_2d(sm + X::OFF_QR + g * 8192, &tmK, bar, 64 * g, lrow0);
+                    }
                     bulk_load(sm + X::OFF_KS + buf * X::KS_BYTES, p.xs + (size_t)krow0 * NA, X::KS_BYTES, bar);
                 } else {
                     mbar_arrive_expect_tx(bar, X::V_BYTES);
@@ -442,7 +526,18 @@ __global__ void __launch_bounds__(kXThreads, 1)
                 if (j >= 1) wait(B_SFREE, (j - 1) & 1);
                 tc_fence_after();
                 const uint32_t ks = smem_addr(sm + X::OFF_K + buf * X::K_BYTES);
-                if (ISO && j < NTP) {
+                if (KLO && j < NTP) {
+                    // prefix tile: the plain query against the hi and then the lo key plane
+                    const uint32_t kl = smem_addr(sm + X::OFF_QR);
+#pragma unroll
+                    for (int g = 0; g < NA; ++g)
+#pragma unroll
+                        for (int hl = 0; hl < 2; ++hl)
+#pragma unroll
+                            for (int u = 0; u < 4; ++u)
+                                umma_f16(tmem_S + 64 * g, sw128_desc(qs + g * 16384 + 32 * u),
+                                         sw128_desc((hl ? kl : ks) + g * 8192 + 32 * u), IDQK, (hl | u) > 0);
+                } else if (ISO && j < NTP) {
                     // prefix tile: rotated query, hi (query region) then lo into the same accumulator
                     const uint32_t qr = smem_addr(sm + X::OFF_QR);
 #pragma unroll
@@ -710,11 +805,11 @@ cudaError_t extend_read_error(unsigned* out, bool clear) {
     return cudaMemcpyToSymbol(g_err_extend, &z, sizeof(unsigned));
 }
 
-template <int D, int G, bool ISO>
+template <int D, int G, int XM>
 static cudaError_t xlaunch(dim3 grid, const CUtensorMap& tk, const CUtensorMap& tv, const ExtendParams& p,
                            cudaStream_t st) {
-    auto fn = extend_kernel<D, G, ISO>;
-    constexpr int smem = XGeo<D, ISO>::SMEM + 1024;
+    auto fn = extend_kernel<D, G, XM>;
+    constexpr int smem = XGeo<D, XM>::SMEM + 1024;
     static bool configured[kMaxDevices];   // this instantiation's attribute, per device
     {
         cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(fn), smem, configured);
@@ -737,7 +832,8 @@ cudaError_t extend_upload_levels(const float* lv3, const float* lv4) {
 // kernel reads them.
 cudaError_t extend_launch(int fmt, int D, int G, int max_q_len, int NH, int B, const CUtensorMap& tk,
                           const CUtensorMap& tv, const ExtendParams& p, cudaStream_t st) {
-    if (fmt < 0 || fmt > 3 || (D != 128 && D != 256) || (fmt == 1 && D != 256) || !(G == 1 || G == 2 || G == 4 || G == 8))
+    if (fmt < 0 || fmt > 6 || (D != 128 && D != 256) || ((fmt == 1 || fmt == 4) && D != 256) ||
+        !(G == 1 || G == 2 || G == 4 || G == 8))
         return cudaErrorInvalidValue;
     const dim3 pgrid((unsigned)(p.Lmax / kXT), (unsigned)p.Hkv, (unsigned)B);
     switch (fmt * 1000 + D) {
@@ -748,40 +844,31 @@ cudaError_t extend_launch(int fmt, int D, int G, int max_q_len, int NH, int B, c
         case 3128: extend_prep_kernel<128, 3><<<pgrid, 256, 0, st>>>(p); break;
         case 2256: extend_prep_kernel<256, 2><<<pgrid, 256, 0, st>>>(p); break;
         case 3256: extend_prep_kernel<256, 3><<<pgrid, 256, 0, st>>>(p); break;
+        case 4256: extend_prep_kernel<256, 4><<<pgrid, 256, 0, st>>>(p); break;
+        case 5128: extend_prep_kernel<128, 5><<<pgrid, 256, 0, st>>>(p); break;
+        case 5256: extend_prep_kernel<256, 5><<<pgrid, 256, 0, st>>>(p); break;
+        case 6128: extend_prep_kernel<128, 6><<<pgrid, 256, 0, st>>>(p); break;
+        case 6256: extend_prep_kernel<256, 6><<<pgrid, 256, 0, st>>>(p); break;
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int tpt = 128 / G;
     dim3 grid((unsigned)((max_q_len + tpt - 1) / tpt), (unsigned)NH, (unsigned)B);
-    if (fmt >= 2 && D == 128) {
-        switch (G) {
-            case 1: return xlaunch<128, 1, true>(grid, tk, tv, p, st);
-            case 2: return xlaunch<128, 2, true>(grid, tk, tv, p, st);
-            case 4: return xlaunch<128, 4, true>(grid, tk, tv, p, st);
-            case 8: return xlaunch<128, 8, true>(grid, tk, tv, p, st);
-        }
-    } else if (fmt >= 2) {
-        switch (G) {
-            case 1: return xlaunch<256, 1, true>(grid, tk, tv, p, st);
-            case 2: return xlaunch<256, 2, true>(grid, tk, tv, p, st);
-            case 4: return xlaunch<256, 4, true>(grid, tk, tv, p, st);
-            case 8: return xlaunch<256, 8, true>(grid, tk, tv, p, st);
-        }
-    } else if (D == 256) {
-        switch (G) {
-            case 1: return xlaunch<256, 1, false>(grid, tk, tv, p, st);
-            case 2: return xlaunch<256, 2, false>(grid, tk, tv, p, st);
-            case 4: return xlaunch<256, 4, false>(grid, tk, tv, p, st);
-            case 8: return xlaunch<256, 8, false>(grid, tk, tv, p, st);
-        }
-    } else {
-        switch (G) {
-            case 1: return xlaunch<128, 1, false>(grid, tk, tv, p, st);
-            case 2: return xlaunch<128, 2, false>(grid, tk, tv, p, st);
-            case 4: return xlaunch<128, 4, false>(grid, tk, tv, p, st);
-            case 8: return xlaunch<128, 8, false>(grid, tk, tv, p, st);
-        }
+    // prefix tile kind: ISO -> rotated query (1), q4 -> two key planes (2), else plain (0)
+    const int xm = (fmt == 2 || fmt == 3) ? 1 : fmt == 4 ? 2 : 0;
+#define QKV_XL(DD, XMM)                                                     \
+    switch (G) {                                                           \
+        case 1: return xlaunch<DD, 1, XMM>(grid, tk, tv, p, st);           \
+        case 2: return xlaunch<DD, 2, XMM>(grid, tk, tv, p, st);           \
+        case 4: return xlaunch<DD, 4, XMM>(grid, tk, tv, p, st);           \
+        case 8: return xlaunch<DD, 8, XMM>(grid, tk, tv, p, st);           \
     }
+    if (xm == 1 && D == 128) { QKV_XL(128, 1) }
+    else if (xm == 1) { QKV_XL(256, 1) }
+    else if (xm == 2) { QKV_XL(256, 2) }
+    else if (D == 256) { QKV_XL(256, 0) }
+    else { QKV_XL(128, 0) }
+#undef QKV_XL
     return cudaErrorInvalidValue;
 }
 

@@ -11,7 +11,8 @@
 //   q4_0 : (q - 8) * d16 per 32-value block, then the FWHT-256 x 1/16 over the
 //          row (butterflies at distances 1, 2, 4 inside a lane, 8 .. 128 by lane
 //          shuffles that every lane of the warp executes);
-//   ISO  : s16 * (conj(q) (x) c) per 4-D group of levels c.
+//   ISO  : s16 * (conj(q) (x) c) per 4-D group of levels c;
+//   bf16 : the unquantized store's values as they are.
 #include "qkv_device.cuh"
 #include "qkv_params.h"
 
@@ -25,7 +26,11 @@ __device__ __forceinline__ void dequant_row(const uint8_t* code, const uint8_t* 
                                             float (&x)[D / 32]) {
     constexpr int E = D / 32;   // values per lane: dims [E lane, E lane + E)
     const int d0 = E * lane;
-    if constexpr (ENC == ENC_INT8) {
+    if constexpr (ENC == ENC_BF16) {
+        (void)scale;
+#pragma unroll
+        for (int e = 0; e < E; ++e) x[e] = bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(code)[d0 + e]);
+    } else if constexpr (ENC == ENC_INT8) {
         const float d16 = f16_bits_to_f32(reinterpret_cast<const uint16_t*>(scale)[d0 / 64]);
 #pragma unroll
         for (int e = 0; e < E; ++e) x[e] = (float)(int8_t)code[d0 + e] * d16;
@@ -147,6 +152,11 @@ cudaError_t gather_launch(int fmt, int D, const GatherParams& p, cudaStream_t st
     else if (fmt == 2 && D == 256) QKV_GATHER(ENC_ISO3, ENC_ISO3, 256);
     else if (fmt == 3 && D == 128) QKV_GATHER(ENC_ISO4, ENC_ISO4, 128);
     else if (fmt == 3 && D == 256) QKV_GATHER(ENC_ISO4, ENC_ISO4, 256);
+    else if (fmt == 4 && D == 256) QKV_GATHER(ENC_Q4, ENC_Q4, 256);
+    else if (fmt == 5 && D == 128) QKV_GATHER(ENC_INT8, ENC_BF16, 128);
+    else if (fmt == 5 && D == 256) QKV_GATHER(ENC_INT8, ENC_BF16, 256);
+    else if (fmt == 6 && D == 128) QKV_GATHER(ENC_BF16, ENC_INT8, 128);
+    else if (fmt == 6 && D == 256) QKV_GATHER(ENC_BF16, ENC_INT8, 256);
     else return cudaErrorInvalidValue;
 #undef QKV_GATHER
     return cudaGetLastError();

@@ -12,18 +12,18 @@
 namespace qkv {
 
 // Store encodings (a format is one encoding for K and one for V).
-enum Enc : int { ENC_INT8 = 0, ENC_Q4 = 1, ENC_ISO3 = 2, ENC_ISO4 = 3 };
+enum Enc : int { ENC_INT8 = 0, ENC_Q4 = 1, ENC_ISO3 = 2, ENC_ISO4 = 3, ENC_BF16 = 4 };
 
 constexpr int kPage = 16;  // tokens per page
 
 __host__ __device__ constexpr int code_row_bytes(int enc, int D) {
-    return enc == ENC_INT8 ? D : enc == ENC_Q4 ? D / 2 : enc == ENC_ISO3 ? (D / 128) * 48 : (D / 128) * 64;
+    return enc == ENC_INT8 ? D : enc == ENC_Q4 ? D / 2 : enc == ENC_ISO3 ? (D / 128) * 48 : enc == ENC_ISO4 ? (D / 128) * 64 : 2 * D;
 }
 __host__ __device__ constexpr int scale_row_bytes(int enc, int D) {
-    return enc == ENC_INT8 ? (D / 64) * 2 : enc == ENC_Q4 ? (D / 32) * 2 : enc == ENC_ISO3 ? (D / 128) * 2 : (D / 128) * 4;
+    return enc == ENC_INT8 ? (D / 64) * 2 : enc == ENC_Q4 ? (D / 32) * 2 : enc == ENC_ISO3 ? (D / 128) * 2 : enc == ENC_ISO4 ? (D / 128) * 4 : 0;
 }
-// values sharing one scale
-__host__ __device__ constexpr int group_size(int enc) { return enc == ENC_INT8 ? 64 : enc == ENC_Q4 ? 32 : 128; }
+// values sharing one scale (the unquantized bf16 store: none; head_dim a multiple of 64 there)
+__host__ __device__ constexpr int group_size(int enc) { return enc == ENC_INT8 ? 64 : enc == ENC_Q4 ? 32 : enc == ENC_BF16 ? 64 : 128; }
 
 // Device error word bits (see qkv_device_error in qkv.h).
 constexpr unsigned kErrPage = 1u, kErrPos = 2u, kErrWait = 4u;

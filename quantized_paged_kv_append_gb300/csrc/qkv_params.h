@@ -64,6 +64,7 @@ struct ExtendParams {
     int out_f32;
     int Lmax;            // keys per (sequence, KV head) in the workspace planes (multiple of 64)
     uint16_t* xk;        // workspace: fp16 K' [B * Hkv][Lmax][D]
+    uint16_t* xklo;      // workspace (q4 format): the fp16 remainder of K', right after xk
     uint16_t* xv;        // workspace: fp16 V^T [B * Hkv][D][Lmax]
     float* xs;           // workspace: fp32 key scales x softmax scale [B * Hkv][Lmax][D / 64]
     float quat[4];       // ISO formats: the pool's unit quaternion (w, x, y, z)

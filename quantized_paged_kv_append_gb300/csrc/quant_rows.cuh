@@ -11,6 +11,8 @@
 //   q4_0   "--kv k8v4: hybrid KV cache", "What"/"How": V rotated by the 1/16-
 //          normalised FWHT-256, then q4_0 (d = signed absmax / -8,
 //          q = min(15, trunc(x/d + 8.5))).
+//   bf16   "qwen35/q36: --kv - int8 K/V caches", "What it does": the one-store
+//          formats leave the other store unquantized (here: the bf16 input).
 //   ISO    "feat(kvcache): add ISO3/ISO4 KV-cache quantization", "What": per 128
 //          values L2-normalise, rotate each 4-D group by a unit quaternion, code
 //          to the nearest Lloyd-Max level, store ||x|| / ||levels||.
@@ -222,7 +224,11 @@ __device__ void append_iso_block(const uint16_t* src, uint8_t* code, uint8_t* sc
 template <int ENC, int D>
 __device__ __forceinline__ void quantize_row(const uint16_t* src, uint8_t* code, uint8_t* scale, int lane,
                                              const float* quat, const float* levels, const float* mids) {
-    if constexpr (ENC == ENC_INT8) {
+    if constexpr (ENC == ENC_BF16) {
+        // the unquantized store: the bf16 input row as it is (D / 8 lanes move 16 bytes each)
+        (void)scale;
+        if (lane < D / 8) reinterpret_cast<uint4*>(code)[lane] = reinterpret_cast<const uint4*>(src)[lane];
+    } else if constexpr (ENC == ENC_INT8) {
         append_int8_row<D>(src, code, scale, lane);
     } else if constexpr (ENC == ENC_Q4) {
         append_q4_row(src, code, scale, lane);

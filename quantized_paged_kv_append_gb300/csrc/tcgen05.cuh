@@ -111,11 +111,11 @@ __device__ __forceinline__ uint64_t sw128_desc_lbo(uint32_t saddr, uint32_t lbo,
 // K-major, 128-byte swizzle, 8-row groups 1024 B apart.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) { return sw128_desc_lbo(saddr, 16, 1024); }
 
-// Instruction descriptor, kind::f16: fp16 A and B, fp32 accumulator, M x N;
-// a_mn / b_mn select MN-major A / B.
-__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_mn = 0, int b_mn = 0) {
-    return (1u << 4) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) |
-           ((uint32_t)(M >> 4) << 24);
+// Instruction descriptor, kind::f16: fp16 (bf16 = 0) or bf16 (bf16 = 1) A and B, fp32
+// accumulator, M x N; a_mn / b_mn select MN-major A / B.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_mn = 0, int b_mn = 0, int bf16 = 0) {
+    return (1u << 4) | ((uint32_t)bf16 << 7) | ((uint32_t)bf16 << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // byte offset of 16-byte chunk `c` (0..7) of row `r` in a 128-byte-swizzled tile

@@ -9,7 +9,7 @@ import numpy as np
 
 from quantized_paged_kv_append_gb300 import synth
 
-FMT = {"int8": 0, "k8v4": 1, "iso3": 2, "iso4": 3}
+FMT = {"int8": 0, "k8v4": 1, "iso3": 2, "iso4": 3, "q4": 4, "k8vbf16": 5, "kbf16v8": 6}
 
 
 class Workload:

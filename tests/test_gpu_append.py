@@ -45,6 +45,7 @@ def _assert_planes_equal(got, ref, label):
 CASES = [
     ("int8", 256, 2), ("int8", 128, 4), ("k8v4", 256, 2),
     ("iso3", 128, 4), ("iso4", 128, 4), ("iso3", 256, 2), ("iso4", 256, 2),
+    ("q4", 256, 2), ("k8vbf16", 256, 2), ("k8vbf16", 128, 4), ("kbf16v8", 256, 2), ("kbf16v8", 128, 4),
 ]
 
 
@@ -59,7 +60,8 @@ def test_append_bytes_small_ragged(env, orc, fmt, d, hkv):
 
 @pytest.mark.parametrize("fmt,d,hkv,L", [("int8", 256, 2, 2048), ("int8", 256, 2, 131072),
                                          ("k8v4", 256, 2, 118750), ("iso3", 128, 4, 81920),
-                                         ("iso4", 128, 4, 81920)])
+                                         ("iso4", 128, 4, 81920), ("q4", 256, 2, 131072),
+                                         ("k8vbf16", 256, 2, 65536), ("kbf16v8", 256, 2, 65536)])
 def test_append_bytes_full_size(env, orc, fmt, d, hkv, L):
     """The configurations the benchmark runs: every token of the pool."""
     torch, qkv = env

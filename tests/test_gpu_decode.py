@@ -44,6 +44,8 @@ SMALL = [
     ("int8", 256, 2, 32), ("k8v4", 256, 2, 16), ("k8v4", 256, 1, 4),
     ("iso3", 128, 4, 16), ("iso4", 128, 4, 16), ("iso3", 256, 2, 16), ("iso4", 256, 2, 4),
     ("iso4", 128, 2, 2),
+    ("q4", 256, 2, 16), ("q4", 256, 1, 4), ("k8vbf16", 256, 2, 16), ("k8vbf16", 128, 4, 16),
+    ("kbf16v8", 256, 2, 16), ("kbf16v8", 128, 2, 2),
 ]
 
 
@@ -64,6 +66,9 @@ def test_decode_small_ragged(env, orc, fmt, d, hkv, hq):
     ("k8v4", 256, 2, 16, 118750),
     ("iso3", 128, 4, 16, 81920),
     ("iso4", 128, 4, 16, 81920),
+    ("q4", 256, 2, 16, 131072),
+    ("k8vbf16", 256, 2, 16, 65536),
+    ("kbf16v8", 256, 2, 16, 65536),
 ])
 def test_decode_full_size(env, orc, fmt, d, hkv, hq, L):
     torch, qkv = env
@@ -178,6 +183,8 @@ def test_decode_bad_page_entry_flags_without_fault(env, orc):
     ("iso3", 128, 4, 16, [1, 37, 300, 16, 1000]), ("iso4", 128, 4, 16, [1, 37, 300, 16, 1000]),
     ("int8", 256, 2, 32, [1, 37, 300, 16, 1000]), ("iso4", 256, 2, 4, [1, 37, 300, 16, 1000]),
     ("int8", 256, 2, 16, [131072]),   # the benchmark step: quantize-on-write + decode at 128K
+    ("q4", 256, 2, 16, [1, 37, 300, 16, 1000]), ("k8vbf16", 256, 2, 16, [1, 37, 300, 16, 1000]),
+    ("kbf16v8", 256, 2, 16, [1, 37, 300, 16, 1000]), ("kbf16v8", 128, 4, 16, [1, 37, 300, 16, 1000]),
 ])
 def test_decode_fused_quantize_on_write(env, orc, fmt, d, hkv, hq, lens):
     """kv_decode_attn with k_new/v_new: the newest token (position L - 1) is

@@ -80,6 +80,12 @@ def test_extend_small(env, orc, prefix, chunk, hkv, hq, d):
     ("iso4", [130], [50], 2, 16, 128),
     ("iso3", [77], [19], 2, 32, 128),
     ("iso4", [60], [25], 4, 4, 128),
+    ("q4", [100], [37], 2, 16, 256),
+    ("q4", [0, 200, 33], [20, 70, 1], 2, 16, 256),
+    ("k8vbf16", [100], [37], 2, 16, 256),
+    ("k8vbf16", [90], [33], 4, 4, 128),
+    ("kbf16v8", [0, 150, 64], [17, 40, 64], 2, 16, 256),
+    ("kbf16v8", [77], [19], 2, 32, 128),
 ])
 def test_extend_formats(env, orc, fmt, prefix, chunk, hkv, hq, d):
     """k8v4 (V rotated back from the FWHT domain) and ISO3 / ISO4 (raw levels as
@@ -94,7 +100,8 @@ def test_extend_formats(env, orc, fmt, prefix, chunk, hkv, hq, d):
     assert r["ok"], r
 
 
-@pytest.mark.parametrize("fmt,hkv,d", [("k8v4", 2, 256), ("iso3", 4, 128), ("iso4", 4, 128)])
+@pytest.mark.parametrize("fmt,hkv,d", [("k8v4", 2, 256), ("iso3", 4, 128), ("iso4", 4, 128), ("q4", 2, 256),
+                                       ("k8vbf16", 2, 256), ("kbf16v8", 2, 256)])
 def test_extend_formats_long_prefix_sampled(env, orc, fmt, hkv, d):
     """A 256-token chunk over an 8192-token prefix (Hq 16); the oracle computes a
     sample of rows one by one."""

@@ -41,6 +41,9 @@ def _check(got, ref, exact):
     ("iso4", [61], 4, 128),
     ("iso3", [90], 2, 256),
     ("iso4", [45], 2, 256),
+    ("q4", [200, 17], 2, 256),
+    ("k8vbf16", [37, 300], 2, 256),
+    ("kbf16v8", [129], 4, 128),
 ])
 def test_gather_matches_oracle(env, orc, fmt, lens, hkv, d):
     torch, qkv = env
@@ -52,8 +55,8 @@ def test_gather_matches_oracle(env, orc, fmt, lens, hkv, d):
         k, v = qkv.gather_dequant(cache, table[b], L)
         torch.cuda.synchronize()
         kr, vr = pool.gather_dequant(w.table, b, L)
-        _check(k.cpu().numpy(), kr, exact=fmt in ("int8", "k8v4"))
-        _check(v.cpu().numpy(), vr, exact=fmt == "int8")
+        _check(k.cpu().numpy(), kr, exact=fmt in ("int8", "k8v4", "k8vbf16", "kbf16v8"))
+        _check(v.cpu().numpy(), vr, exact=fmt in ("int8", "k8vbf16", "kbf16v8"))
     assert qkv.device_error() == 0
 
 

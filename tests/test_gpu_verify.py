@@ -34,7 +34,8 @@ def _run(torch, qkv, w, pool, windows, out_dtype=None, seed=61):
 
 
 @pytest.mark.parametrize("fmt,d,hkv,hq", [("int8", 256, 2, 16), ("k8v4", 256, 2, 16), ("iso3", 128, 4, 16),
-                                          ("iso4", 128, 4, 16), ("int8", 128, 2, 4)])
+                                          ("iso4", 128, 4, 16), ("int8", 128, 2, 4), ("q4", 256, 2, 16),
+                                          ("k8vbf16", 256, 2, 16), ("kbf16v8", 128, 4, 16)])
 def test_verify_matches_oracle(env, orc, fmt, d, hkv, hq):
     torch, qkv = env
     w = Workload(fmt, [300, 45, 1000, 17], hkv, hq, d, seed=61)
