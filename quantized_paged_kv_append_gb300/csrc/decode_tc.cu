@@ -21,7 +21,9 @@
 //   * warps 4-11 (converters) turn int8 codes into exact fp16: K as 1152 + c
 //     straight into TMEM (the A operand of Q K^T, one token per TMEM lane), V
 //     as c into an MN-major shared-memory tile (the B operand of P'^T V'); K of
-//     tile T is converted before V of tile T - 1, so Q K^T runs a tile ahead;
+//     tile T is converted before V of tile T - 1, so Q K^T runs a tile ahead
+//     (the bf16 K of format 6 is copied in two k-step halves, each released by
+//     its own commit);
 //   * warp 13 (one thread) issues tcgen05.mma: S_g = K'_g Q_g^T per 64-dim
 //     scale group g (M = 128 tokens, N = 16 query columns; 16 MMAs per tile at
 //     D = 256) and O += P'^T V' (M = 64 P' columns: 16 per scale group = 8
@@ -135,7 +137,7 @@ enum {
     B_KE = 2,    // [2] K slot free (8 converter warps + 4 softmax warps)
     B_VF = 4,    // [2]
     B_VE = 6,    // [2]
-    B_KCV = 8,   // K' written to TMEM (8 converter warps)
+    B_KCV = 8,   // K' written to TMEM (8 converter warps; bf16 K: the 4 warps of k-step half 0)
     B_VCV = 9,   // V' written (8 converter warps)
     B_QKD = 10,  // [2] QK^T of a tile complete (commit)
     B_PVD = 12,  // [2] PV of a tile complete (commit)
@@ -144,7 +146,9 @@ enum {
     B_QRD = 19,  // query tile of a piece written (1)
     B_PAT = 20,  // [kind] producer: the newest token's page landed (1 + tx)
     B_DRN = 22,  // every MMA of the CTA complete (commit), before TMEM is released
-    B_N = 23
+    B_KCV1 = 23, // bf16 K: K' of k-step half 1 written (its 4 converter warps)
+    B_QKH = 24,  // [2] bf16 K: the Q K^T MMAs of k-step half 0 of a tile complete (commit)
+    B_N = 26
 };
 static_assert(B_N <= 32, "barrier area holds 32 barriers");
 
@@ -260,6 +264,7 @@ __global__ void __launch_bounds__(kThr, 1)
     using X = TG<D, FMT>;
     constexpr int NA = X::NA;
     constexpr bool VQ = X::VQ;
+    constexpr bool kSplitK = X::KB;   // Q K^T issued in two k-step halves (bf16 K)
     extern __shared__ __align__(1024) uint8_t dsm_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -279,10 +284,12 @@ __global__ void __launch_bounds__(kThr, 1)
             mbar_init(&bars[B_KE + i], X::KE_N);
             mbar_init(&bars[B_VE + i], X::VE_N);
             mbar_init(&bars[B_QKD + i], 1);
+            mbar_init(&bars[B_QKH + i], 1);
             mbar_init(&bars[B_PVD + i], 1);
             mbar_init(&bars[B_SF + i], kSoftW);
         }
-        mbar_init(&bars[B_KCV], kConvW);
+        mbar_init(&bars[B_KCV], kSplitK ? kConvW / 2 : kConvW);
+        mbar_init(&bars[B_KCV1], kConvW / 2);
         mbar_init(&bars[B_VCV], kConvW);
         mbar_init(&bars[B_PFL], kSoftW);
         mbar_init(&bars[B_QRD], 1);
@@ -602,6 +609,7 @@ __global__ void __launch_bounds__(kThr, 1)
             bool hq = wq.next(p, pq), hv = wv.next(p, pv);
             int tq = 0, tv = 0;           // tile index inside the current piece
             uint32_t Tq = 0, Tv = 0, pieceq = 0;
+            int qh = 0;                   // the next Q K^T half of tile Tq
             uint32_t idle = 0;
             while ((hq || hv) && idle < (1u << 22)) {
                 if ((idle & 63) == 63 && *s_abort) break;
@@ -631,7 +639,66 @@ __global__ void __launch_bounds__(kThr, 1)
                         progressed = true;
                     }
                 }
-                if (hq && (!hv || Tq <= Tv + 1)) {
+                // bf16 K: Q K^T of a tile in two halves, k-steps 0-1 and 2-3 of every 64-dim group
+                // (the four accumulators stay interleaved in each half). The converters of half h
+                // write the K' columns of those k-steps and wait only for the MMAs of half h of the
+                // tile before, so K' of the next tile is written while the other half's MMAs still
+                // run (53.6 -> 49.5 us at 131072 tokens). The other formats issue the tile at once:
+                // there an early half queues ahead of PV in the tensor pipe and PV, whose P' and V'
+                // tiles are single-buffered, finishes later (int8: 40.0 -> 42.6 us).
+                auto qk_half = [&](int h) {
+                    const uint32_t sd = tmem + X::SCOL + (Tq % X::NSB) * X::SBUF;
+                    if constexpr (X::KQ) {
+                        // q4 K: one accumulator per 32-dim block (its own scale); two k-steps a
+                        // block against the rotated query's hi (N columns 0..7) and lo (8..15)
+#pragma unroll
+                        for (int u = 0; u < 2; ++u)
+#pragma unroll
+                            for (int g = 0; g < X::NKG; ++g)
+                                umma_f16_ta(sd + 16 * g, tk + 8 * (2 * g + u),
+                                            qd0 + (uint64_t)(((g >> 1) * 2048 + (g & 1) * 64 + 32 * u) >> 4), IDQK, u > 0);
+                    } else if constexpr (X::ISO) {
+                        // per 128-dim block: 8 k-steps against the query tile whose N columns hold
+                        // the rotated query's fp16 hi (0..7) and lo (8..15) parts; even and odd
+                        // k-steps go to two accumulators, so consecutive MMAs are independent
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+#pragma unroll
+                            for (int gk = 0; gk < X::NKG; ++gk)
+                                umma_f16_ta(sd + 32 * gk + 16 * (u & 1), tk + 8 * (8 * gk + u),
+                                            qd0 + (uint64_t)(((2 * gk + (u >> 2)) * 2048 + 32 * (u & 3)) >> 4),
+                                            IDQK, u > 1);
+                    } else {
+                        // k-step outer, scale group inner: consecutive MMAs write different
+                        // accumulators, so the tensor pipe overlaps them instead of waiting on
+                        // each accumulator's previous k-step
+#pragma unroll
+                        for (int ui = 0; ui < (kSplitK ? 2 : 4); ++ui)
+#pragma unroll
+                            for (int g = 0; g < NA; ++g) {
+                                const int u = kSplitK ? 2 * h + ui : ui;
+                                umma_f16_ta(sd + 16 * g, tk + 8 * (4 * g + u), qd0 + (uint64_t)((g * 2048 + 32 * u) >> 4),
+                                            IDQK, u > 0);
+                            }
+                    }
+                };
+                if (hq && qh == 1) {
+                    if (mbar_test_wait(&bars[B_KCV1], Tq & 1)) {
+                        tc_fence_after();
+                        qk_half(1);
+                        umma_commit(&bars[B_QKD + (Tq & 1)]);
+                        ++Tq;
+                        qh = 0;
+                        if (pq.p0 + kTP * (tq + 1) < pq.p1) {
+                            ++tq;
+                        } else {
+                            tq = 0;
+                            ++pieceq;
+                            hq = wq.next(p, pq);
+                        }
+                        progressed = true;
+                    }
+                } else if (hq && (!hv || Tq <= Tv + 1)) {
                     const bool first = tq == 0;
                     bool ready = mbar_test_wait(&bars[B_KCV], Tq & 1);
                     if (ready && Tq >= (uint32_t)X::NSB)
@@ -639,46 +706,20 @@ __global__ void __launch_bounds__(kThr, 1)
                     if (ready && first) ready = mbar_test_wait(&bars[B_QRD], pieceq & 1);
                     if (ready) {
                         tc_fence_after();
-                        const uint32_t sd = tmem + X::SCOL + (Tq % X::NSB) * X::SBUF;
-                        if constexpr (X::KQ) {
-                            // q4 K: one accumulator per 32-dim block (its own scale); two k-steps a
-                            // block against the rotated query's hi (N columns 0..7) and lo (8..15)
-#pragma unroll
-                            for (int u = 0; u < 2; ++u)
-#pragma unroll
-                                for (int g = 0; g < X::NKG; ++g)
-                                    umma_f16_ta(sd + 16 * g, tk + 8 * (2 * g + u),
-                                                qd0 + (uint64_t)(((g >> 1) * 2048 + (g & 1) * 64 + 32 * u) >> 4), IDQK, u > 0);
-                        } else if constexpr (X::ISO) {
-                            // per 128-dim block: 8 k-steps against the query tile whose N columns hold
-                            // the rotated query's fp16 hi (0..7) and lo (8..15) parts; even and odd
-                            // k-steps go to two accumulators, so consecutive MMAs are independent
-#pragma unroll
-                            for (int u = 0; u < 8; ++u)
-#pragma unroll
-                                for (int gk = 0; gk < X::NKG; ++gk)
-                                    umma_f16_ta(sd + 32 * gk + 16 * (u & 1), tk + 8 * (8 * gk + u),
-                                                qd0 + (uint64_t)(((2 * gk + (u >> 2)) * 2048 + 32 * (u & 3)) >> 4),
-                                                IDQK, u > 1);
+                        qk_half(0);
+                        if constexpr (kSplitK) {
+                            umma_commit(&bars[B_QKH + (Tq & 1)]);
+                            qh = 1;
                         } else {
-                            // k-step outer, scale group inner: consecutive MMAs write different
-                            // accumulators, so the tensor pipe overlaps them instead of waiting on
-                            // each accumulator's previous k-step
-#pragma unroll
-                            for (int u = 0; u < 4; ++u)
-#pragma unroll
-                                for (int g = 0; g < NA; ++g)
-                                    umma_f16_ta(sd + 16 * g, tk + 8 * (4 * g + u), qd0 + (uint64_t)((g * 2048 + 32 * u) >> 4),
-                                                IDQK, u > 0);
-                        }
-                        umma_commit(&bars[B_QKD + (Tq & 1)]);
-                        ++Tq;
-                        if (pq.p0 + kTP * (tq + 1) < pq.p1) {
-                            ++tq;
-                        } else {
-                            tq = 0;
-                            ++pieceq;
-                            hq = wq.next(p, pq);
+                            umma_commit(&bars[B_QKD + (Tq & 1)]);
+                            ++Tq;
+                            if (pq.p0 + kTP * (tq + 1) < pq.p1) {
+                                ++tq;
+                            } else {
+                                tq = 0;
+                                ++pieceq;
+                                hq = wq.next(p, pq);
+                            }
                         }
                         progressed = true;
                     }
@@ -691,7 +732,7 @@ __global__ void __launch_bounds__(kThr, 1)
             }
             // every MMA issued above completes before TMEM is released (after an abort the
             // loop ends with MMAs possibly still in flight)
-            if (Tq > 0 || Tv > 0) {
+            if (Tq > 0 || Tv > 0 || qh) {
                 umma_commit(&bars[B_DRN]);
                 if (!mbar_wait_bounded(&bars[B_DRN], 0)) atomicOr(&g_err_dtc, kErrWait);
             }
@@ -818,7 +859,9 @@ __global__ void __launch_bounds__(kThr, 1)
                 // ---- K of tile T: exact fp16 1152 + c (int8), q - 8 (q4) or the bf16 values, one
                 // token per TMEM lane ----
                 wait_or_flag(&bars[B_KF + buf], (X::KSTB == 2 ? T >> 1 : T) & 1);
-                if (T >= 1) wait_or_flag(&bars[B_QKD + ((T - 1) & 1)], ((T - 1) >> 1) & 1);
+                // the K' columns of half hf are free once the MMAs of tile T - 1 that read them are done
+                if (T >= 1)
+                    wait_or_flag(&bars[(kSplitK && !hf ? B_QKH : B_QKD) + ((T - 1) & 1)], ((T - 1) >> 1) & 1);
                 tc_fence_after();
                 if constexpr (X::ISO) {
                     // level pairs of dims 2 p, 2 p + 1 into TMEM column p, one token per lane
@@ -863,21 +906,22 @@ __global__ void __launch_bounds__(kThr, 1)
                     }
                     tmem_wait_st();
                 } else if constexpr (X::KB) {
-                    // bf16 K: the staged values as they are, dims 2 c, 2 c + 1 in TMEM column c
+                    // bf16 K: the staged values as they are, dims 2 c, 2 c + 1 in TMEM column c; half
+                    // hf holds k-steps 2 hf, 2 hf + 1 of every 64-dim group (TMEM columns 32 g + 16 hf ..)
                     const uint8_t* slot = sm + X::OFF_KST + jpage * X::PAGE_B;
 #pragma unroll
-                    for (int i0 = 0; i0 < D / 16; i0 += 8) {
-                        uint32_t w[32];
+                    for (int g = 0; g < NA; ++g) {
+                        uint32_t w[16];
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const int gc = hf * (D / 16) + i0 + i;   // 16-byte chunk = 8 dims
+                        for (int i = 0; i < 4; ++i) {
+                            const int gc = 8 * g + 4 * hf + i;   // 16-byte chunk = 8 dims
                             const uint4 x = *reinterpret_cast<const uint4*>(slot + (gc >> 3) * 2048 + sw_off(rr, gc & 7));
                             w[4 * i] = x.x;
                             w[4 * i + 1] = x.y;
                             w[4 * i + 2] = x.z;
                             w[4 * i + 3] = x.w;
                         }
-                        tmem_st32_nowait(tmem + lb + X::KCOL + 4 * (hf * (D / 16) + i0), w);
+                        tmem_st16_nowait(tmem + lb + X::KCOL + 32 * g + 16 * hf, w);
                     }
                     tmem_wait_st();
                 } else {
@@ -903,7 +947,7 @@ __global__ void __launch_bounds__(kThr, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(&bars[B_KCV]);
+                    mbar_arrive(&bars[kSplitK && hf ? B_KCV1 : B_KCV]);
                     mbar_arrive(&bars[B_KE + buf]);
                 }
                 // ---- V of tile T - 1 ----
