@@ -785,28 +785,44 @@ def run_verify(args):
     ws = qkv.verify_workspace(caches[0], HQ, W, pages, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
-    def step(i):
+    wsf = qkv.verify_fixed_workspace(caches[0], 1, W, HQ, pages, device=dev)
+
+    def step_expanded(i):
         c = i % LAYERS
         qkv.verify(caches[c], q_d[c], cu, lens, tabs[c], L, scale=1.0 / math.sqrt(D), out=out, workspace=ws,
                    stream=stream)
+
+    def step(i):
+        # the window in one pass: its W x 8 queries per KV head as 16-column tile passes
+        c = i % LAYERS
+        qkv.verify_fixed(caches[c], q_d[c], lens, tabs[c], L, W, scale=1.0 / math.sqrt(D), out=out, workspace=wsf,
+                         stream=stream)
 
     with torch.cuda.stream(stream):
         for i in range(max(3, args.warmup)):
             step(i)
     torch.cuda.synchronize()
     assert qkv.device_error() == 0
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            step_expanded(i)
+    torch.cuda.synchronize()
+    assert qkv.device_error() == 0
     proc, cpath = _clock_sampler()
     per_ms, _ = _time_graph(torch, stream, step, args.steps, max(3, args.reps))
+    exp_ms, _ = _time_graph(torch, stream, step_expanded, args.steps, max(3, args.reps))
     clocks = _clock_summary(proc, cpath, 0)
     res = {"metric": "verify window call time, int8 128K, W = 4", "value": round(per_ms * 1e3, 2), "unit": "us",
            "n_gpus": 1, "steps": args.steps * max(3, args.reps), "warmup": max(3, args.warmup),
            "ms_per_step": round(per_ms, 5), "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
            "dtype": "int8", "data": "synthetic (seeded splitmix64 + Box-Muller, bf16)",
            "config": {"workload": f"verify window of {W} queries over one {L}-token int8 sequence, {HQ} q heads / "
-                                  f"{HKV} KV heads, head_dim {D}, page 16; expansion kernel + tensor-core decode over "
-                                  f"{W} rows", "layer_copies": LAYERS,
+                                  f"{HKV} KV heads, head_dim {D}, page 16; kv_verify_attn_fixed: the window's "
+                                  f"{W * HQ // HKV} queries per KV head as 16-column passes of the tensor-core "
+                                  f"decode", "layer_copies": LAYERS,
                       "l2": f"inputs larger than L2: {LAYERS} caches cycled"},
            "packed_gbs_per_query": round(DECODE_BYTES * W / (per_ms / 1e3) / 1e9, 1),
+           "expanded_us": round(exp_ms * 1e3, 2),   # kv_verify_attn: one decode row per query
            "clocks": clocks}
     print(json.dumps(res))
 

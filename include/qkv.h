@@ -226,6 +226,33 @@ QKV_API int kv_verify_attn(const qkv_cache_desc* cache, const void* q, int batch
                            void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * kv_verify_attn_fixed -- the verify window in one pass, for windows of the same
+ * length W = window in every sequence (the MTP draft length of a step)
+ * [S8 "What it does": verify windows; K4 "Tests": batched forms with per-query
+ * step arrays]. q: bf16 [batch * window][num_q_heads][head_dim]; row
+ * b * window + w is query w of sequence b, at position seq_lens[b] - window + w,
+ * and attends positions [0, seq_lens[b] - window + w + 1), all from the pool.
+ * out: [batch * window][num_q_heads][head_dim], bf16 or fp32;
+ * batch * window <= 1024. For the int8 format the window's queries share each
+ * K/V tile read: the window x (num_q_heads / num_kv_heads) queries of a KV head
+ * attend as up to 16 columns of the same tile pass (with the V scales folded into
+ * the fp16 V tile, one rounding), so a window of W costs about
+ * ceil(W x (num_q_heads / num_kv_heads) / 16) decode passes rather than W. The
+ * other formats expand the window into one decode row per query, as
+ * kv_verify_attn does. workspace: at least kv_verify_fixed_workspace_size()
+ * bytes, 256-byte aligned, no initialization needed. A sequence shorter than the
+ * window sets the position bit of the device error word; its queries that would
+ * sit before position 0 give zero rows. Errors as kv_decode_attn.
+ */
+QKV_API size_t kv_verify_fixed_workspace_size(const qkv_cache_desc* cache, int batch, int window, int num_q_heads,
+                                              int max_pages_per_seq);
+
+QKV_API int kv_verify_attn_fixed(const qkv_cache_desc* cache, const void* q, int batch, int window, int num_q_heads,
+                                 const int32_t* seq_lens, const int32_t* page_table, int max_pages_per_seq,
+                                 int max_seq_len, float scale, void* out, int out_dtype, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
+/*
  * kv_gather_dequant -- the dequantized K and V of one sequence as dense fp32
  * rows [S8 "What it does": the prompt-chunk path turns the int8 cache back into
  * a dense buffer before a library GEMM; FT "What": the extend fast path unpacks

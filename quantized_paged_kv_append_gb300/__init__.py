@@ -207,3 +207,40 @@ def verify(cache: PagedKVCache, q, cu_seqlens, seq_lens, page_table, max_seq_len
     _lib.check(rc, "kv_verify_attn")
     return out
 
+
+def verify_fixed_workspace(cache: PagedKVCache, batch: int, window: int, num_q_heads: int, max_pages_per_seq: int,
+                           device="cuda"):
+    """Scratch for the fixed-window verify (partial results of the split tiles; for the
+    formats other than int8 also the expanded page-table rows)."""
+    torch = _torch()
+    n = _lib.lib().kv_verify_fixed_workspace_size(C.byref(cache.desc), int(batch), int(window), int(num_q_heads),
+                                                  int(max_pages_per_seq))
+    if n == 0:
+        raise QkvError(-1, "kv_verify_fixed_workspace_size")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def verify_fixed(cache: PagedKVCache, q, seq_lens, page_table, max_seq_len: int, window: int, scale=None, out=None,
+                 out_dtype=None, workspace=None, stream=None):
+    """Verify window of the same length in every sequence, in one pass: q bf16
+    [batch * window, Hq, D]; row b * window + w sits at position seq_lens[b] - window + w
+    and attends [0, seq_lens[b] - window + w + 1). Returns out [batch * window, Hq, D]."""
+    torch = _torch()
+    total, Hq, D = q.shape
+    B, maxp = int(seq_lens.numel()), int(page_table.shape[1])
+    if total != B * int(window):
+        raise QkvError(-1, "verify_fixed: q rows must be batch * window")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((total, Hq, D), dtype=out_dtype or torch.bfloat16, device=q.device)
+    odt = _lib.QKV_OUT_F32 if out.dtype == torch.float32 else _lib.QKV_OUT_BF16
+    if workspace is None and B > 0:
+        workspace = verify_fixed_workspace(cache, B, int(window), Hq, maxp, device=q.device)
+    ws_ptr, ws_bytes = (_ptr(workspace), workspace.numel() * workspace.element_size()) if workspace is not None else (None, 0)
+    rc = _lib.lib().kv_verify_attn_fixed(C.byref(cache.desc), _ptr(q), B, int(window), Hq, _ptr(seq_lens),
+                                         _ptr(page_table), maxp, int(max_seq_len), float(scale), _ptr(out), odt,
+                                         ws_ptr, ws_bytes, _stream(stream))
+    _lib.check(rc, "kv_verify_attn_fixed")
+    return out
+

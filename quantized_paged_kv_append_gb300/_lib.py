@@ -24,7 +24,7 @@ ERRORS = {0: "QKV_OK", -1: "QKV_ERR_ARG", -2: "QKV_ERR_HEAD_DIM", -3: "QKV_ERR_G
 # every symbol include/qkv.h declares
 EXPORTS = ["qkv_row_bytes", "qkv_iso_levels", "iso_kv_append", "kv_decode_workspace_size", "kv_decode_attn",
            "kv_extend_workspace_size", "kv_extend_attn", "kv_gather_dequant", "kv_verify_workspace_size", "kv_verify_attn",
-           "kv_decode_attn_noalloc", "qkv_strerror",
+           "kv_verify_fixed_workspace_size", "kv_verify_attn_fixed", "kv_decode_attn_noalloc", "qkv_strerror",
            "qkv_last_cuda_error", "qkv_device_error"]
 
 
@@ -78,6 +78,10 @@ def lib():
         L.kv_verify_workspace_size.restype = SZ
         L.kv_verify_attn.argtypes = [C.POINTER(CacheDesc), P, I, I, P, P, I, P, I, I, C.c_float, P, I, P, SZ, P]
         L.kv_verify_attn.restype = I
+        L.kv_verify_fixed_workspace_size.argtypes = [C.POINTER(CacheDesc), I, I, I, I]
+        L.kv_verify_fixed_workspace_size.restype = SZ
+        L.kv_verify_attn_fixed.argtypes = [C.POINTER(CacheDesc), P, I, I, I, P, P, I, I, C.c_float, P, I, P, SZ, P]
+        L.kv_verify_attn_fixed.restype = I
         L.kv_gather_dequant.argtypes = [C.POINTER(CacheDesc), P, I, P, P, P]
         L.kv_gather_dequant.restype = I
         L.kv_decode_attn_noalloc.argtypes = [C.POINTER(CacheDesc), P, P, P, I, I, P, I, P, I, C.c_float, P, I, P]

@@ -215,7 +215,8 @@ int enc_of(int fmt, int store) {
 }
 
 struct DecodeLayout {
-    int G;          // query heads per CTA
+    int G;          // query columns (virtual heads) of a head group
+    int Gv;         // virtual query heads per KV head: window x (num_q_heads / num_kv_heads)
     int NH;         // head groups per sequence
     int S;          // segments
     int Cmax;       // CTA upper bound
@@ -223,15 +224,19 @@ struct DecodeLayout {
     size_t bytes;
 };
 
-int decode_layout(const qkv_cache_desc* d, int batch, int num_q_heads, int sms, DecodeLayout* L) {
+// window: queries per sequence (1 for decode; a verify window attends as window x Gtot
+// virtual heads per KV head, query w's heads after query w - 1's)
+int decode_layout(const qkv_cache_desc* d, int batch, int num_q_heads, int window, int sms, DecodeLayout* L) {
     if (num_q_heads <= 0 || num_q_heads % d->num_kv_heads) return QKV_ERR_GQA;
     const int Gtot = num_q_heads / d->num_kv_heads;
     if (!(Gtot == 1 || Gtot == 2 || Gtot == 4 || Gtot % 8 == 0)) return QKV_ERR_GQA;
-    L->G = decode_heads_per_cta(Gtot);
-    L->NH = d->num_kv_heads * (Gtot / L->G);
+    if (window < 1) return QKV_ERR_ARG;
+    L->Gv = window * Gtot;
+    L->G = decode_heads_per_cta(L->Gv, d->format);
+    L->NH = d->num_kv_heads * (L->Gv / L->G);
     L->S = batch * L->NH;
     L->Cmax = sms;
-    L->slot_floats = 16 + 8 * d->head_dim;
+    L->slot_floats = 2 * (L->G > 8 ? 16 : 8) + L->G * d->head_dim;   // m, l, O of one piece
     // partial slots (m, l, O) of the pieces: piece (CTA c, segment s) uses slot c + s
     const size_t slots = (size_t)L->Cmax + L->S;
     auto al = [](size_t x) { return (x + 255) / 256 * 256; };
@@ -335,14 +340,15 @@ size_t kv_decode_workspace_size(const qkv_cache_desc* cache, int batch, int num_
     int dev;
     if (device_setup(&dev)) return 0;
     DecodeLayout L;
-    if (decode_layout(cache, batch, num_q_heads, g_dev_sms[dev], &L)) return 0;
+    if (decode_layout(cache, batch, num_q_heads, 1, g_dev_sms[dev], &L)) return 0;
     return L.bytes;
 }
 
-int kv_decode_attn(const qkv_cache_desc* cache, const void* q, const void* k_new, const void* v_new, int batch,
-                   int num_q_heads, const int32_t* page_table, int max_pages_per_seq, const int32_t* seq_lens,
-                   int max_seq_len, float scale, void* out, int out_dtype, void* workspace, size_t workspace_bytes,
-                   void* stream) {
+// decode of `window` queries per sequence (1: kv_decode_attn; more: the fixed verify window)
+static int decode_common(const qkv_cache_desc* cache, const void* q, const void* k_new, const void* v_new, int batch,
+                         int window, int num_q_heads, const int32_t* page_table, int max_pages_per_seq,
+                         const int32_t* seq_lens, int max_seq_len, float scale, void* out, int out_dtype,
+                         void* workspace, size_t workspace_bytes, void* stream) {
     int rc = check_desc(cache);
     if (rc) return rc;
     if (batch < 0 || max_seq_len < 0) return QKV_ERR_ARG;
@@ -357,7 +363,7 @@ int kv_decode_attn(const qkv_cache_desc* cache, const void* q, const void* k_new
     int dev;
     if ((rc = device_setup(&dev))) return rc;
     DecodeLayout L;
-    if ((rc = decode_layout(cache, batch, num_q_heads, g_dev_sms[dev], &L))) return rc;
+    if ((rc = decode_layout(cache, batch, num_q_heads, window, g_dev_sms[dev], &L))) return rc;
     if (!workspace || workspace_bytes < L.bytes || !aligned16(workspace)) return QKV_ERR_WORKSPACE;
 
     const int D = cache->head_dim;
@@ -387,6 +393,8 @@ int kv_decode_attn(const qkv_cache_desc* cache, const void* q, const void* k_new
     p.B = batch;
     p.Hq = num_q_heads;
     p.Gtot = num_q_heads / cache->num_kv_heads;
+    p.W = window;
+    p.Gv = L.Gv;
     p.NH = L.NH;
     p.page_table = page_table;
     p.max_pages = max_pages_per_seq;
@@ -403,6 +411,14 @@ int kv_decode_attn(const qkv_cache_desc* cache, const void* q, const void* k_new
     cudaError_t e = decode_tc_launch(D, L.G, grid, cache->format, tk, tv, p, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e);
     return QKV_OK;
+}
+
+int kv_decode_attn(const qkv_cache_desc* cache, const void* q, const void* k_new, const void* v_new, int batch,
+                   int num_q_heads, const int32_t* page_table, int max_pages_per_seq, const int32_t* seq_lens,
+                   int max_seq_len, float scale, void* out, int out_dtype, void* workspace, size_t workspace_bytes,
+                   void* stream) {
+    return decode_common(cache, q, k_new, v_new, batch, 1, num_q_heads, page_table, max_pages_per_seq, seq_lens,
+                         max_seq_len, scale, out, out_dtype, workspace, workspace_bytes, stream);
 }
 
 size_t kv_extend_workspace_size(const qkv_cache_desc* cache, int batch, int max_q_len, int max_pages_per_seq) {
@@ -485,7 +501,7 @@ static int verify_layout(const qkv_cache_desc* cache, int num_q_heads, int total
     int rc = device_setup(&dev);
     if (rc) return rc;
     DecodeLayout L;
-    if ((rc = decode_layout(cache, total_q, num_q_heads, g_dev_sms[dev], &L))) return rc;
+    if ((rc = decode_layout(cache, total_q, num_q_heads, 1, g_dev_sms[dev], &L))) return rc;
     auto al = [](size_t x) { return (x + 255) / 256 * 256; };
     *off_lens = al((size_t)total_q * max_pages_per_seq * sizeof(int32_t));
     *off_dec = *off_lens + al((size_t)total_q * sizeof(int32_t));
@@ -517,6 +533,56 @@ int kv_verify_attn(const qkv_cache_desc* cache, const void* q, int batch, int nu
     uint8_t* ws = (uint8_t*)workspace;
     VerifyParams vp;
     vp.cu = cu_seqlens;
+    vp.W_fixed = 0;
+    vp.seq_lens = seq_lens;
+    vp.page_table = page_table;
+    vp.B = batch;
+    vp.max_pages = max_pages_per_seq;
+    vp.table_rep = (int32_t*)ws;
+    vp.lens_rep = (int32_t*)(ws + off_lens);
+    cudaError_t e = verify_expand_launch(vp, total_q, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return kv_decode_attn(cache, q, nullptr, nullptr, total_q, num_q_heads, vp.table_rep, max_pages_per_seq,
+                          vp.lens_rep, max_seq_len, scale, out, out_dtype, ws + off_dec, workspace_bytes - off_dec,
+                          stream);
+}
+
+// The fixed window in one pass is the int8 decode kernel's verify instantiation; the other
+// formats expand the window into one decode row per query (the kv_verify_attn path).
+size_t kv_verify_fixed_workspace_size(const qkv_cache_desc* cache, int batch, int window, int num_q_heads,
+                                      int max_pages_per_seq) {
+    if (check_desc(cache) || batch < 0 || window < 1 || max_pages_per_seq <= 0) return 0;
+    if ((long long)batch * window > decode_max_batch()) return 0;
+    if (cache->format != QKV_INT8) return kv_verify_workspace_size(cache, num_q_heads, batch * window, max_pages_per_seq);
+    int dev;
+    if (device_setup(&dev)) return 0;
+    DecodeLayout L;
+    if (decode_layout(cache, batch, num_q_heads, window, g_dev_sms[dev], &L)) return 0;
+    return L.bytes;
+}
+
+int kv_verify_attn_fixed(const qkv_cache_desc* cache, const void* q, int batch, int window, int num_q_heads,
+                         const int32_t* seq_lens, const int32_t* page_table, int max_pages_per_seq, int max_seq_len,
+                         float scale, void* out, int out_dtype, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+    int rc = check_desc(cache);
+    if (rc) return rc;
+    if (window < 1 || batch < 0) return QKV_ERR_ARG;
+    if ((long long)batch * window > decode_max_batch()) return QKV_ERR_UNSUPPORTED;
+    if (cache->format == QKV_INT8)
+        return decode_common(cache, q, nullptr, nullptr, batch, window, num_q_heads, page_table, max_pages_per_seq,
+                             seq_lens, max_seq_len, scale, out, out_dtype, workspace, workspace_bytes, stream);
+    if (batch == 0) return QKV_OK;
+    if (!q || !seq_lens || !page_table || !out || max_pages_per_seq <= 0) return QKV_ERR_ARG;
+    if (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads) return QKV_ERR_GQA;
+    const int total_q = batch * window;
+    size_t off_lens, off_dec, need;
+    if ((rc = verify_layout(cache, num_q_heads, total_q, max_pages_per_seq, &off_lens, &off_dec, &need))) return rc;
+    if (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 255u)) return QKV_ERR_WORKSPACE;
+    uint8_t* ws = (uint8_t*)workspace;
+    VerifyParams vp;
+    vp.cu = nullptr;
+    vp.W_fixed = window;
     vp.seq_lens = seq_lens;
     vp.page_table = page_table;
     vp.B = batch;

@@ -114,7 +114,7 @@ struct TG {
     static constexpr int OFF_VSC = OFF_KSC + KSTB * kTP * SC_B;     // [2][8][VSC_B]
     static constexpr int OFF_BIAS = OFF_VSC + 2 * kTP * VSC_B;      // float [NA][8]
     static constexpr int OFF_RED = OFF_BIAS + 256;                  // softmax-warp reductions
-    static constexpr int OFF_ROW = OFF_RED + 512;                   // quantize-on-write rows [2][512]
+    static constexpr int OFF_ROW = OFF_RED + 1024;                  // quantize-on-write rows [2][512]
     static constexpr int OFF_BAR = OFF_ROW + 1024;
     static constexpr int OFF_MISC = OFF_BAR + 32 * 8;
     static constexpr int SMEM = OFF_MISC + 64;
@@ -248,16 +248,32 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
     return false;
 }
 
-template <int D, int G>
-__device__ void write_out(const DecodeParams& p, int b, int hq0, int i, float v) {
-    const size_t o = ((size_t)b * p.Hq + hq0) * D + i;
+// Virtual head gv of KV head kvh (gv = w * Gtot + h): query row b * W + w, query head kvh * Gtot + h.
+// VW: the kernel runs a verify window (W > 1); otherwise W = 1 and gv is the head's index in
+// its KV group.
+template <bool VW>
+__device__ __forceinline__ size_t qrow_index(const DecodeParams& p, int b, int kvh, int gv) {
+    if constexpr (!VW) return (size_t)b * p.Hq + (size_t)kvh * p.Gtot + gv;
+    const int w = gv / p.Gtot, h = gv - w * p.Gtot;
+    return ((size_t)b * p.W + w) * p.Hq + (size_t)kvh * p.Gtot + h;
+}
+// element d of the output row whose first element is at orow (= qrow_index(...) * D)
+__device__ __forceinline__ void write_row(const DecodeParams& p, size_t orow, int d, float v) {
+    const size_t o = orow + d;
+    if (p.out_f32) reinterpret_cast<float*>(p.out)[o] = v;
+    else reinterpret_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(v);
+}
+// element i of the head group's output (i = column * D + dim; column = virtual head gv0 + i / D)
+template <int D, int G, bool VW>
+__device__ void write_out(const DecodeParams& p, int b, int kvh, int gv0, int i, float v) {
+    const size_t o = qrow_index<VW>(p, b, kvh, gv0 + i / D) * D + (i % D);
     if (p.out_f32) reinterpret_cast<float*>(p.out)[o] = v;
     else reinterpret_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(v);
 }
 
 }  // namespace
 
-template <int D, int G, int FMT>
+template <int D, int G, int FMT, bool VW>
 __global__ void __launch_bounds__(kThr, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const DecodeParams p) {
@@ -265,6 +281,12 @@ __global__ void __launch_bounds__(kThr, 1)
     constexpr int NA = X::NA;
     constexpr bool VQ = X::VQ;
     constexpr bool kSplitK = X::KB;   // Q K^T issued in two k-step halves (bf16 K)
+    // 16 query columns (int8): the V scales are folded into V' (fp16(c d), one rounding) so that
+    // P' holds 16 heads hi + lo in each 16-row slot pair; QH = per-head arrays of the softmax
+    constexpr bool VFOLD = G > 8;
+    constexpr int QH = G > 8 ? 16 : 8;
+    static_assert(G <= 8 || (FMT == 0 && G == 16), "16 query columns: the int8 format only");
+    static_assert(!VW || FMT == 0, "the one-pass verify window: the int8 format only");
     extern __shared__ __align__(1024) uint8_t dsm_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -333,7 +355,9 @@ __global__ void __launch_bounds__(kThr, 1)
         long long local = 0;
         for (int b = b_lo; b < b_hi; ++b) {
             const int Lr = len_of(b);
-            if (flag_errors && warp == 0 && (Lr < 0 || Lr > p.max_pages * kPage)) atomicOr(&g_err_dtc, kErrPos);
+            // a verify window longer than its sequence is flagged too (its early queries see nothing)
+            if (flag_errors && warp == 0 && (Lr < 0 || Lr > p.max_pages * kPage || (VW && Lr < p.W)))
+                atomicOr(&g_err_dtc, kErrPos);
             local += (max(0, min(Lr, p.max_pages * kPage)) + kPage - 1) / kPage;
         }
         long long incl = local;
@@ -387,7 +411,7 @@ __global__ void __launch_bounds__(kThr, 1)
                 const int pid = __ldcg(p.page_table + (size_t)spc.b * p.max_pages + spc.p0 + lane);
                 if (pid >= 0 && pid < p.num_pages) {
                     const int rowb = kind ? X::VROW : X::KROW, scrow = kind ? X::VSROW : X::KSROW;
-                    const long long prow = ((long long)pid * p.Hkv + spc.hg / (p.Gtot / G)) * kPage;
+                    const long long prow = ((long long)pid * p.Hkv + spc.hg / (p.Gv / G)) * kPage;
                     bulk_prefetch_l2((kind ? p.vc : p.kc) + prow * rowb, kPage * rowb);
                     if (scrow) bulk_prefetch_l2((kind ? p.vs : p.ks) + prow * scrow, kPage * scrow);
                 }
@@ -403,10 +427,10 @@ __global__ void __launch_bounds__(kThr, 1)
                 spid_cur = lane < npc ? row[lane] : 0;
                 spid_nxt = 32 + lane < npc ? row[32 + lane] : 0;
             } else if (warp < kSoftW) {
-                const int kvh = spc.hg / (p.Gtot / G), hgi = spc.hg % (p.Gtot / G);
-                const int hq0 = kvh * p.Gtot + hgi * G;
-                if (tid < G * D * 2 / 128)
-                    prefetch_l1(reinterpret_cast<const uint8_t*>(p.q + ((size_t)spc.b * p.Hq + hq0) * D) + 128 * tid);
+                const int kvh = spc.hg / (p.Gv / G), hgi = spc.hg % (p.Gv / G);
+                if (tid < G * D * 2 / 128)   // the query rows of the first piece (2 D bytes a head)
+                    prefetch_l1(reinterpret_cast<const uint8_t*>(p.q + qrow_index<VW>(p, spc.b, kvh, hgi * G + tid / (D / 64)) * D) +
+                                128 * (tid % (D / 64)));
             }
         } else {
             spc.b = -1;
@@ -423,9 +447,8 @@ __global__ void __launch_bounds__(kThr, 1)
         const int b = (int)(s / p.NH);
         if (seq_len_clamped(p, b) == 0) {
             const int hg = (int)(s % p.NH);
-            const int kvh = hg / (p.Gtot / G), hgi = hg % (p.Gtot / G);
-            const int hq0 = kvh * p.Gtot + hgi * G;
-            for (int i = tid; i < G * D; i += kThr) write_out<D, G>(p, b, hq0, i, 0.0f);
+            const int kvh = hg / (p.Gv / G), hgi = hg % (p.Gv / G);
+            for (int i = tid; i < G * D; i += kThr) write_out<D, G, VW>(p, b, kvh, hgi * G, i, 0.0f);
         }
     }
     Walker walker{b0, pref0, beg, end};
@@ -460,7 +483,7 @@ __global__ void __launch_bounds__(kThr, 1)
         Piece pc;
         bool first = true;
         while (walker.next(p, pc)) {
-            const int kvh = pc.hg / (p.Gtot / G);
+            const int kvh = pc.hg / (p.Gv / G);
             const int32_t* ptrow = p.page_table + (size_t)pc.b * p.max_pages;
             const int last_page = (pc.L - 1) / kPage;
             const int npc = pc.p1 - pc.p0;
@@ -827,6 +850,10 @@ __global__ void __launch_bounds__(kThr, 1)
                     *reinterpret_cast<uint4*>(atom + sw_off(r, ch + 3)) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
                 }
             } else {
+                // 16 query columns: fp16(c d) with the row's scale of the 64-dim group (rows past the
+                // sequence end, whose staged scale may be anything, get scale 0)
+                const uint16_t* vsr = reinterpret_cast<const uint16_t*>(sm + X::OFF_VSC + (buf * kTP + jpage) * X::VSC_B +
+                                                                        rr * X::VSROW);
 #pragma unroll
                 for (int i = 0; i < NCH; ++i) {
                     const int gc = hf * NCH + i;
@@ -837,6 +864,11 @@ __global__ void __launch_bounds__(kThr, 1)
                     for (int k = 0; k < 4; ++k) {
                         w[2 * k] = hsub2_u32(lop3_and_xor(xs[k], 0x00ff00ffu, 0x64806480u), 0x64806480u);
                         w[2 * k + 1] = hsub2_u32(lop3_and_xor(xs[k] >> 8, 0x00ff00ffu, 0x64806480u), 0x64806480u);
+                    }
+                    if constexpr (VFOLD) {
+                        const uint32_t sb = vrow_ok ? (uint32_t)vsr[gc >> 2] : 0u, s2 = sb | (sb << 16);
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) w[k] = hfma2_u32(w[k], s2, 0u);
                     }
                     uint8_t* atom = vp + (gc >> 2) * 16384;
                     const int ch = 2 * (gc & 3);
@@ -965,14 +997,13 @@ __global__ void __launch_bounds__(kThr, 1)
         float* bias_s = reinterpret_cast<float*>(sm + X::OFF_BIAS);
         int* red_flag = reinterpret_cast<int*>(sm + X::OFF_RED);                 // [2][4]
         int* red_e = red_flag + 8;                                               // [2][4]
-        float* red_m = reinterpret_cast<float*>(sm + X::OFF_RED + 64);           // [2][4][8]
-        float* red_l = red_m + 64;                                               // [4][8]
-        float* sML = red_l + 32;                                                 // M[8], L[8]
+        float* red_m = reinterpret_cast<float*>(sm + X::OFF_RED + 64);           // [2][4][QH]
+        float* red_l = red_m + 8 * QH;                                           // [4][QH]
+        float* sML = red_l + 4 * QH;                                             // M[QH], L[QH]
         uint32_t T = 0, piece = 0;
         Piece pc;
         while (walker.next(p, pc)) {
-            const int kvh = pc.hg / (p.Gtot / G), hgi = pc.hg % (p.Gtot / G);
-            const int hq0 = kvh * p.Gtot + hgi * G;
+            const int kvh = pc.hg / (p.Gv / G), gv0 = (pc.hg % (p.Gv / G)) * G;   // KV head, first virtual head
             // ---- query tile (B operand, K-major, dims in converter order) and the offset sums ----
             {
                 uint8_t* qsm = sm + X::OFF_Q;
@@ -983,7 +1014,7 @@ __global__ void __launch_bounds__(kThr, 1)
                 if constexpr (X::KQ) {
                     const int hh = r >> 4, q16 = r & 15;
                     if (hh < G) {
-                        const uint16_t* qrow = p.q + ((size_t)pc.b * p.Hq + hq0 + hh) * D;
+                        const uint16_t* qrow = p.q + qrow_index<VW>(p, pc.b, kvh, gv0 + hh) * D;
                         float x[16];
 #pragma unroll
                         for (int k = 0; k < 16; ++k) x[k] = bf16_bits_to_f32(qrow[q16 + 16 * k]);
@@ -1024,7 +1055,7 @@ __global__ void __launch_bounds__(kThr, 1)
                     const int n = idx / (NA * 8), rem = idx % (NA * 8), a = rem >> 3, cc = rem & 7;
                     uint32_t w[4] = {0u, 0u, 0u, 0u}, wl[4] = {0u, 0u, 0u, 0u};
                     if (n < G) {
-                        const uint16_t* qrow = p.q + ((size_t)pc.b * p.Hq + hq0 + n) * D + 64 * a + 8 * cc;
+                        const uint16_t* qrow = p.q + qrow_index<VW>(p, pc.b, kvh, gv0 + n) * D + 64 * a + 8 * cc;
                         const uint4 raw = *reinterpret_cast<const uint4*>(qrow);
                         const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
                         float v[8];
@@ -1067,12 +1098,12 @@ __global__ void __launch_bounds__(kThr, 1)
                     if constexpr (X::QHL)
                         *reinterpret_cast<uint4*>(qsm + a * 2048 + sw_off(8 + n, cc)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
                 }
-                // 1152 * (sum of the fp16 query over each 64-dim group): thread -> (head, D / 16 dims)
-                constexpr int DPT = D / 16, TPG = 64 / DPT;
-                const int h = r >> 4, s0 = (r & 15) * DPT;
+                // 1152 * (sum of the fp16 query over each 64-dim group): thread -> (head, D / TPH dims)
+                constexpr int TPH = 128 / QH, DPT = D / TPH, TPG = 64 / DPT;
+                const int h = r / TPH, s0 = (r % TPH) * DPT;
                 float part = 0.0f;
                 if (h < G) {
-                    const uint16_t* qrow = p.q + ((size_t)pc.b * p.Hq + hq0 + h) * D + s0;
+                    const uint16_t* qrow = p.q + qrow_index<VW>(p, pc.b, kvh, gv0 + h) * D + s0;
                     for (int d = 0; d < DPT; ++d)
                         part += __half2float(__float2half_rn(bf16_bits_to_f32(qrow[d])));
                 }
@@ -1080,7 +1111,7 @@ __global__ void __launch_bounds__(kThr, 1)
                 for (int off = 1; off < TPG; off <<= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
                 // only the int8 K' carries the 1152 offset
                 constexpr bool KI8 = !X::ISO && !X::KQ && !X::KB;
-                if (h < G && (r & 15) % TPG == 0) bias_s[(s0 / 64) * 8 + h] = KI8 ? 1152.0f * part : 0.0f;
+                if (h < G && (r % TPH) % TPG == 0) bias_s[(s0 / 64) * QH + h] = KI8 ? 1152.0f * part : 0.0f;
             }
             fence_proxy_async();
             soft_sync();
@@ -1089,7 +1120,7 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll
             for (int g = 0; g < NA; ++g)
 #pragma unroll
-                for (int h = 0; h < G; ++h) bias[g][h] = bias_s[g * 8 + h];
+                for (int h = 0; h < G; ++h) bias[g][h] = bias_s[g * QH + h];
 
             float m[G], l[G];
 #pragma unroll
@@ -1151,12 +1182,22 @@ __global__ void __launch_bounds__(kThr, 1)
                 if (lane == 0) mbar_arrive(&bars[B_SF + T % X::NSB]);
 #pragma unroll
                 for (int h = 0; h < G; ++h) s[h] = valid ? s[h] * p.scale_log2 : -INFINITY;
+                // a verify window: query w sees positions < L - W + w + 1, so the last W - 1 rows
+                // of the sequence are hidden from the columns of the earlier queries
+                if (VW && valid && pos > pc.L - p.W) {
+                    // columns of queries w < pos - (L - W) do not see pos: virtual heads below hmin
+                    const int hmin = (pos - (pc.L - p.W)) * p.Gtot - gv0;
+#pragma unroll
+                    for (int h = 0; h < G; ++h)
+                        if (h < hmin) s[h] = -INFINITY;
+                }
                 // ---- V scales ----
                 float vsf[X::VG];
                 int e_row = 0;
                 if constexpr (!X::VB) wait_or_flag(&bars[B_VF + buf], ph);
-                if constexpr (VQ || X::VB) {
-                    // the q4 block scales are folded into V' by the converters; the bf16 V has none
+                if constexpr (VQ || X::VB || VFOLD) {
+                    // the q4 block scales (and the int8 scales with 16 columns) are folded into V' by
+                    // the converters; the bf16 V has none
 #pragma unroll
                     for (int g = 0; g < X::VG; ++g) vsf[g] = 1.0f;
                     e_row = 15;   // the fp16 exponent field of 1.0
@@ -1184,16 +1225,18 @@ __global__ void __launch_bounds__(kThr, 1)
                 soft_sync();
                 const bool any = (red_flag[buf * 4] | red_flag[buf * 4 + 1] | red_flag[buf * 4 + 2] | red_flag[buf * 4 + 3]) != 0;
                 bool rescale = false;
-                float fac[8];
+                float fac[QH];
 #pragma unroll
-                for (int h = 0; h < 8; ++h) fac[h] = 1.0f;
+                for (int h = 0; h < QH; ++h) fac[h] = 1.0f;
                 if (any) {
-                    {
+#pragma unroll
+                    for (int o8 = 0; o8 < QH / 8; ++o8) {   // head octets
                         float v8[8];
 #pragma unroll
-                        for (int h = 0; h < 8; ++h) v8[h] = h < G ? s[h < G ? h : 0] : -INFINITY;
+                        for (int h = 0; h < 8; ++h) v8[h] = 8 * o8 + h < G ? s[8 * o8 + h < G ? 8 * o8 + h : 0] : -INFINITY;
                         const float wm = warp_reduce8<true>(v8, lane);
-                        if ((lane & 3) == 0 && (lane >> 2) < G) red_m[buf * 32 + warp * 8 + (lane >> 2)] = wm;
+                        if ((lane & 3) == 0 && 8 * o8 + (lane >> 2) < G)
+                            red_m[buf * 4 * QH + warp * QH + 8 * o8 + (lane >> 2)] = wm;
                     }
                     const int ew = __reduce_max_sync(0xffffffffu, (unsigned)e_row);
                     if (lane == 0) red_e[buf * 4 + warp] = ew;
@@ -1203,8 +1246,8 @@ __global__ void __launch_bounds__(kThr, 1)
                     const float ef = (E == 1000) ? 1.0f : exp2i(Enew - E);
 #pragma unroll
                     for (int h = 0; h < G; ++h) {
-                        const float M = fmaxf(fmaxf(red_m[buf * 32 + h], red_m[buf * 32 + 8 + h]),
-                                              fmaxf(red_m[buf * 32 + 16 + h], red_m[buf * 32 + 24 + h]));
+                        const float* rm = red_m + buf * 4 * QH + h;
+                        const float M = fmaxf(fmaxf(rm[0], rm[QH]), fmaxf(rm[2 * QH], rm[3 * QH]));
                         const float mn = (M > m[h] + 8.0f) ? M : m[h];
                         const float alpha = (m[h] == -INFINITY) ? 0.0f : (mn == m[h] ? 1.0f : fast_exp2(m[h] - mn));
                         l[h] *= alpha;
@@ -1218,7 +1261,8 @@ __global__ void __launch_bounds__(kThr, 1)
                 float pr[G];
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
-                    pr[h] = valid ? fast_exp2(s[h] - m[h]) : 0.0f;
+                    // (a verify column can be hidden from every row of a tile before its frame is set)
+                    pr[h] = (VW ? s[h] != -INFINITY : valid) ? fast_exp2(s[h] - m[h]) : 0.0f;
                     l[h] += pr[h];
                 }
                 // ---- P' (and the rare rescale of O) once PV of the previous tile is done ----
@@ -1227,7 +1271,25 @@ __global__ void __launch_bounds__(kThr, 1)
                 // O rows 16 g + j (lane j of warp g: head j % 8, hi / lo) over the dims of group g;
                 // ISO V groups are 128 dims, so warp g < VG owns 128 columns
                 constexpr int OW = X::ISO ? X::VG : NA, OCW = X::ISO ? 128 : 64;
-                if (rescale && warp < OW) {
+                if constexpr (VFOLD) {
+                    // 16 columns: slot w (warp w) holds heads 8 (w & 1) + j; it is read over the dims
+                    // [D / 2 (w >> 1), + D / 2) only, so those are the columns rescaled
+                    if (rescale) {
+                        const int hw = 8 * (warp & 1) + (lane & 7);
+                        float f = fac[0];
+#pragma unroll
+                        for (int h = 1; h < QH; ++h) f = (hw == h) ? fac[h] : f;
+#pragma unroll 1
+                        for (int c4 = 0; c4 < D / 32; ++c4) {
+                            float v[16];
+                            const uint32_t ta = tmem + lb + X::OCOL + (D / 2) * (warp >> 1) + 16 * c4;
+                            tmem_ld16(ta, v);
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) v[j] *= f;
+                            tmem_st16(ta, v);
+                        }
+                    }
+                } else if (rescale && warp < OW) {
                     float f = fac[0];
 #pragma unroll
                     for (int h = 1; h < 8; ++h) f = ((lane & 7) == h) ? fac[h] : f;
@@ -1247,11 +1309,14 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll
                     for (int g = 0; g < X::PG; ++g) {
                         uint32_t hw[4] = {0u, 0u, 0u, 0u}, lw[4] = {0u, 0u, 0u, 0u};
-                        if (g < X::VG && valid) {
+                        // (16 columns: every slot, since each carries all D dims of its octet)
+                        if ((VFOLD || g < X::VG) && valid) {
                             const float sc = vsf[g < X::VG ? g : 0] * e2;
+                            // 16 columns: slot g holds heads 8 (g & 1) + h (slots 2, 3 repeat 0, 1)
+                            const int hb = G > 8 ? 8 * (g & 1) : 0;
                             float P[8];
 #pragma unroll
-                            for (int h = 0; h < 8; ++h) P[h] = h < G ? pr[h < G ? h : 0] * sc : 0.0f;
+                            for (int h = 0; h < 8; ++h) P[h] = hb + h < G ? pr[hb + h < G ? hb + h : 0] * sc : 0.0f;
 #pragma unroll
                             for (int k = 0; k < 4; ++k) {
                                 if constexpr (X::VB) {
@@ -1282,12 +1347,13 @@ __global__ void __launch_bounds__(kThr, 1)
             wait_or_flag(&bars[B_PVD + ((T - 1) & 1)], ((T - 1) >> 1) & 1);
             tc_fence_after();
             // row sums first, then O straight from TMEM to the output (or to the partial slot)
-            {
+#pragma unroll
+            for (int o8 = 0; o8 < QH / 8; ++o8) {   // head octets
                 float v8[8];
 #pragma unroll
-                for (int h = 0; h < 8; ++h) v8[h] = h < G ? l[h < G ? h : 0] : 0.0f;
+                for (int h = 0; h < 8; ++h) v8[h] = 8 * o8 + h < G ? l[8 * o8 + h < G ? 8 * o8 + h : 0] : 0.0f;
                 const float ws = warp_reduce8<false>(v8, lane);
-                if ((lane & 3) == 0 && (lane >> 2) < G) red_l[warp * 8 + (lane >> 2)] = ws;
+                if ((lane & 3) == 0 && 8 * o8 + (lane >> 2) < G) red_l[warp * QH + 8 * o8 + (lane >> 2)] = ws;
             }
             soft_sync();
             if (r < G) {
@@ -1295,7 +1361,7 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll
                 for (int h = 1; h < G; ++h) mr = (r == h) ? m[h] : mr;
                 sML[r] = mr;
-                sML[8 + r] = red_l[r] + red_l[8 + r] + red_l[16 + r] + red_l[24 + r];
+                sML[QH + r] = red_l[r] + red_l[QH + r] + red_l[2 * QH + r] + red_l[3 * QH + r];
             }
             soft_sync();
             const long long clo = cta_of(pc.soff), chi = cta_of(pc.soff + pc.np - 1);
@@ -1312,7 +1378,7 @@ __global__ void __launch_bounds__(kThr, 1)
                 float* ox = reinterpret_cast<float*>(sm + X::OFF_PP);   // [8 heads][D]
                 {
                     const float e_inv = (E == 1000) ? 0.0f : exp2i(-E);
-                    const float Lh = lane < G ? sML[8 + (lane < G ? lane : 0)] : 0.0f;
+                    const float Lh = lane < G ? sML[QH + (lane < G ? lane : 0)] : 0.0f;
                     const float inv = npieces == 1 ? (Lh > 0.0f ? e_inv / Lh : 0.0f) : e_inv;
 #pragma unroll 1
                     for (int c4 = 0; c4 < 4; ++c4) {
@@ -1365,11 +1431,45 @@ __global__ void __launch_bounds__(kThr, 1)
                     for (int i = 0; i < 16; ++i) y[i] *= 0.0625f;
                     if (npieces == 1) {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) write_out<D, G>(p, pc.b, hq0, hh * D + 16 * q + i, y[i]);
+                        {
+                            const size_t orow = qrow_index<VW>(p, pc.b, kvh, gv0 + hh) * D;
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) write_row(p, orow, 16 * q + i, y[i]);
+                        }
                     } else {
-                        float4* dst = reinterpret_cast<float4*>(mine + 16 + hh * D + 16 * q);
+                        float4* dst = reinterpret_cast<float4*>(mine + 2 * QH + hh * D + 16 * q);
 #pragma unroll
                         for (int q4 = 0; q4 < 4; ++q4) dst[q4] = make_float4(y[4 * q4], y[4 * q4 + 1], y[4 * q4 + 2], y[4 * q4 + 3]);
+                    }
+                }
+            } else if constexpr (VFOLD) {
+                // 16 columns: slot w (warp w) holds heads 8 (w & 1) + j, hi in lane j, lo in lane 8 + j,
+                // each over all D dims (V' carries the scales); warp w writes the dims
+                // [D / 2 (w >> 1), + D / 2) of its heads, in converter order inside each aligned 4
+                const int head = 8 * (warp & 1) + (lane & 7);
+                const float e_inv = (E == 1000) ? 0.0f : exp2i(-E);
+                const float Lh = sML[QH + head];
+                const float inv = npieces == 1 ? (Lh > 0.0f ? e_inv / Lh : 0.0f) : e_inv;
+                const size_t orow = qrow_index<VW>(p, pc.b, kvh, gv0 + head) * D;
+#pragma unroll 1
+                for (int c4 = 0; c4 < D / 32; ++c4) {
+                    float v[16];
+                    const int d0 = (D / 2) * (warp >> 1) + 16 * c4;
+                    tmem_ld16(tmem + lb + X::OCOL + d0, v);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v[j] += __shfl_xor_sync(0xffffffffu, v[j], 8);
+                    if (lane < 8 && head < G) {
+                        float o[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) o[perm4(j)] = v[j] * inv;
+                        if (npieces == 1) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) write_row(p, orow, d0 + j, o[j]);
+                        } else {
+                            float4* dst = reinterpret_cast<float4*>(mine + 2 * QH + head * D + d0);
+#pragma unroll
+                            for (int q4 = 0; q4 < 4; ++q4) dst[q4] = make_float4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
+                        }
                     }
                 }
             } else if (warp < (X::ISO ? X::VG : NA)) {
@@ -1378,8 +1478,9 @@ __global__ void __launch_bounds__(kThr, 1)
                 // 4-D group is rotated back: conj(q) (x) o)
                 constexpr int OCW = X::ISO ? 128 : 64;
                 const float e_inv = (E == 1000) ? 0.0f : exp2i(-E);
-                const float Lh = lane < G ? sML[8 + lane] : 0.0f;
+                const float Lh = lane < G ? sML[QH + lane] : 0.0f;
                 const float inv = npieces == 1 ? (Lh > 0.0f ? e_inv / Lh : 0.0f) : e_inv;
+                const size_t orow = qrow_index<VW>(p, pc.b, kvh, gv0 + (lane < G ? lane : 0)) * D;
 #pragma unroll 1
                 for (int c4 = 0; c4 < OCW / 16; ++c4) {
                     float v[16];
@@ -1409,9 +1510,9 @@ __global__ void __launch_bounds__(kThr, 1)
                         }
                         if (npieces == 1) {
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) write_out<D, G>(p, pc.b, hq0, lane * D + d0 + j, o[j]);
+                            for (int j = 0; j < 16; ++j) write_row(p, orow, d0 + j, o[j]);
                         } else {
-                            float4* dst = reinterpret_cast<float4*>(mine + 16 + lane * D + d0);
+                            float4* dst = reinterpret_cast<float4*>(mine + 2 * QH + lane * D + d0);
 #pragma unroll
                             for (int q4 = 0; q4 < 4; ++q4) dst[q4] = make_float4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
                         }
@@ -1422,7 +1523,7 @@ __global__ void __launch_bounds__(kThr, 1)
             if (npieces > 1 && r < G) {
                 // the partial slot's frame and row sum; the combine kernel merges the segment's slots
                 mine[r] = sML[r];
-                mine[8 + r] = sML[8 + r];
+                mine[QH + r] = sML[QH + r];
             }
             soft_sync();
             ++piece;
@@ -1450,14 +1551,14 @@ constexpr int kCombThr = 128;
 constexpr int kMaxGrid = 256;   // decode CTAs (pieces of one segment) the combine step can merge
 constexpr int kMaxBatchDec = 1024;
 
-template <int D, int G>
+template <int D, int G, bool VW>
 __global__ void __launch_bounds__(kCombThr) decode_tc_combine(const DecodeParams p) {
     __shared__ float s_w[kMaxGrid], s_l[kMaxGrid];
     __shared__ float4 s_acc[8][16];
     __shared__ float s_red[8];
     __shared__ long long s_pref[kMaxBatchDec + 1];   // pages of the sequences before b
     __shared__ long long s_wsum[kCombThr / 32];
-    __shared__ int s_info[5];
+    __shared__ int s_info[6];
     const int t = threadIdx.x;
     // The next kernel in the stream may be scheduled now: it does its own set-up while this
     // grid waits, and waits for this grid to complete before it reads anything.
@@ -1524,35 +1625,37 @@ __global__ void __launch_bounds__(kCombThr) decode_tc_combine(const DecodeParams
                     }
                 }
             }
-            const int kvh = hg / (p.Gtot / G), hgi = hg % (p.Gtot / G);
+            const int kvh = hg / (p.Gv / G), hgi = hg % (p.Gv / G);
             s_info[0] = n;
             s_info[1] = clo;
             s_info[2] = seg;
             s_info[3] = b;
-            s_info[4] = kvh * p.Gtot + hgi * G;
+            s_info[4] = hgi * G;
+            s_info[5] = kvh;
         }
         __syncthreads();
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");   // the decode grid has completed
     const int n = s_info[0];
     if (n < 2) return;
-    const int clo = s_info[1], seg = s_info[2], b = s_info[3], hq0 = s_info[4];
+    const int clo = s_info[1], seg = s_info[2], b = s_info[3], gv0 = s_info[4], kvh = s_info[5];
     const int s = blockIdx.x;
     const int f0 = 64 * s, h = f0 / D;
     auto slot = [&](int j) { return p.part1 + (size_t)(clo + j + seg) * p.slot_floats; };
+    constexpr int ML = G > 8 ? 16 : 8;   // m[ML], l[ML], then O
     // O loads first (independent of the weights): thread -> float4 e, slots j = sg, sg + 8, ...
     const int e = t & 15, sg = t >> 4;
     float4 v[20];
 #pragma unroll
     for (int k = 0; k < 20; ++k) {
         const int j = sg + 8 * k;
-        v[k] = j < n ? *reinterpret_cast<const float4*>(slot(j) + 16 + f0 + 4 * e) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[k] = j < n ? *reinterpret_cast<const float4*>(slot(j) + 2 * ML + f0 + 4 * e) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     float mloc = -INFINITY;
     for (int j = t; j < n; j += kCombThr) {
         const float mj = slot(j)[h];
         s_w[j] = mj;
-        s_l[j] = slot(j)[8 + h];
+        s_l[j] = slot(j)[ML + h];
         mloc = fmaxf(mloc, mj);
     }
 #pragma unroll
@@ -1586,7 +1689,7 @@ __global__ void __launch_bounds__(kCombThr) decode_tc_combine(const DecodeParams
     }
     for (int j = sg + 160; j < n; j += 8) {   // segments split over more than 160 CTAs
         const float w = s_w[j];
-        const float4 x = *reinterpret_cast<const float4*>(slot(j) + 16 + f0 + 4 * e);
+        const float4 x = *reinterpret_cast<const float4*>(slot(j) + 2 * ML + f0 + 4 * e);
         acc.x += w * x.x;
         acc.y += w * x.y;
         acc.z += w * x.z;
@@ -1602,7 +1705,7 @@ __global__ void __launch_bounds__(kCombThr) decode_tc_combine(const DecodeParams
             const float4 x = s_acc[g2][q];
             a += c4 == 0 ? x.x : c4 == 1 ? x.y : c4 == 2 ? x.z : x.w;
         }
-        write_out<D, G>(p, b, hq0, f0 + 4 * q + c4, L > 0.0f ? a / L : 0.0f);
+        write_out<D, G, VW>(p, b, kvh, gv0, f0 + 4 * q + c4, L > 0.0f ? a / L : 0.0f);
     }
 }
 
@@ -1620,7 +1723,14 @@ cudaError_t decode_tc_upload_levels(const float* lv3, const float* lv4) {
     return cudaMemcpyToSymbol(c_tc_mids, mid, sizeof(mid));
 }
 
-int decode_heads_per_cta(int Gtot) { return Gtot >= 8 ? 8 : Gtot; }
+// query columns of a head group: up to 8 (16 for int8: the Q K^T tile has N = 16 columns, and
+// with the V scales folded into V' the PV tile holds 16 heads hi + lo)
+int decode_heads_per_cta(int Gv, int fmt) {
+    if (fmt == 0 && Gv % 16 == 0) return 16;
+    for (int G = 8; G > 1; G >>= 1)
+        if (Gv % G == 0) return G;
+    return 1;
+}
 int decode_max_batch() { return kMaxBatchDec; }
 
 cudaError_t decode_tc_read_error(unsigned* out, bool clear) {
@@ -1633,14 +1743,14 @@ cudaError_t decode_tc_read_error(unsigned* out, bool clear) {
 // Both kernels are launched with programmatic stream serialization: each may
 // start while its predecessor in the stream drains, and waits for it
 // (griddepcontrol.wait) before touching memory.
-template <int D, int G, int FMT>
+template <int D, int G, int FMT, bool VW>
 static cudaError_t launch_tc(int grid, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p_in,
                              cudaStream_t st) {
     DecodeParams p = p_in;
     p.rec_by_seg = (long long)p.B * p.NH <= grid;
     p.ctas = grid;
     using X = TG<D, FMT>;
-    auto fn = decode_tc_kernel<D, G, FMT>;
+    auto fn = decode_tc_kernel<D, G, FMT, VW>;
     static bool configured[kMaxDevices];   // this instantiation's attribute, per device
     {
         cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(fn), X::SMEM + 1024, configured);
@@ -1661,17 +1771,22 @@ static cudaError_t launch_tc(int grid, const CUtensorMap& tk, const CUtensorMap&
     cfg.gridDim = dim3(G * D / 64, p.rec_by_seg ? p.B * p.NH : grid);
     cfg.blockDim = dim3(kCombThr);
     cfg.dynamicSmemBytes = 0;
-    return cudaLaunchKernelEx(&cfg, decode_tc_combine<D, G>, p);
+    return cudaLaunchKernelEx(&cfg, decode_tc_combine<D, G, VW>, p);
 }
 
-template <int D, int FMT>
+template <int D, int FMT, bool VW = false>
 static cudaError_t launch_tc_g(int G, int grid, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                                cudaStream_t st) {
+    if constexpr (FMT == 0 && !VW)   // a verify window (int8): its own instantiations
+        if (p.W > 1) return launch_tc_g<D, FMT, true>(G, grid, tk, tv, p, st);
     switch (G) {
-        case 1: return launch_tc<D, 1, FMT>(grid, tk, tv, p, st);
-        case 2: return launch_tc<D, 2, FMT>(grid, tk, tv, p, st);
-        case 4: return launch_tc<D, 4, FMT>(grid, tk, tv, p, st);
-        case 8: return launch_tc<D, 8, FMT>(grid, tk, tv, p, st);
+        case 1: return launch_tc<D, 1, FMT, VW>(grid, tk, tv, p, st);
+        case 2: return launch_tc<D, 2, FMT, VW>(grid, tk, tv, p, st);
+        case 4: return launch_tc<D, 4, FMT, VW>(grid, tk, tv, p, st);
+        case 8: return launch_tc<D, 8, FMT, VW>(grid, tk, tv, p, st);
+        case 16:
+            if constexpr (FMT == 0) return launch_tc<D, 16, FMT, VW>(grid, tk, tv, p, st);
+            break;
     }
     return cudaErrorInvalidValue;
 }

@@ -25,9 +25,12 @@ struct DecodeParams {
     const uint8_t* vc;
     const uint8_t* vs;
     int num_pages, Hkv;
-    const uint16_t* q;   // bf16 [B][Hq][D]
+    const uint16_t* q;   // bf16 [B * W][Hq][D]
     int B, Hq, Gtot;     // Gtot = Hq / Hkv
-    int NH;              // head groups per sequence = Hkv * Gtot / G
+    int W;               // queries per sequence: 1 (decode) or a verify window; query w of sequence b
+                         // is row b * W + w, at position seq_lens[b] - W + w
+    int Gv;              // virtual query heads per KV head = W * Gtot (virtual head w * Gtot + h)
+    int NH;              // head groups per sequence = Hkv * Gv / G
     const int32_t* page_table;
     int max_pages;
     const int32_t* seq_lens;
@@ -35,8 +38,8 @@ struct DecodeParams {
     void* out;
     int out_f32;
     float quat[4];
-    float* part1;        // (C + S) partial slots: m[8], l[8], O[8][D] per piece
-    int slot_floats;     // 16 + 8 * D
+    float* part1;        // (C + S) partial slots: m[ML], l[ML], O[G][D] per piece (ML = 8, or 16 when G = 16)
+    int slot_floats;     // 2 ML + G D
     int rec_by_seg;      // merge blocks indexed by segment (when segments <= CTAs), else by the closing CTA
     int ctas;            // CTAs of the decode grid (the split of the units follows from it and seq_lens)
     const uint16_t* k_new;   // optional bf16 [B][Hkv][D]: quantize-on-write of position seq_lens[b] - 1
@@ -84,7 +87,8 @@ struct GatherParams {
 };
 
 struct VerifyParams {
-    const int32_t* cu;          // [B + 1] query rows of each sequence's window
+    const int32_t* cu;          // [B + 1] query rows of each sequence's window, or null: W_fixed rows each
+    int W_fixed;
     const int32_t* seq_lens;    // [B]
     const int32_t* page_table;  // [B][max_pages]
     int B, max_pages;
@@ -106,7 +110,7 @@ cudaError_t append_read_error(unsigned* out, bool clear);
 cudaError_t append_launch(int fmt, int D, const AppendParams& p, cudaStream_t st);
 
 // query heads per CTA of the decode kernel, and the largest batch of one decode call
-int decode_heads_per_cta(int Gtot);
+int decode_heads_per_cta(int Gv, int fmt);   // Gv = virtual query heads per KV head
 int decode_max_batch();
 // decode on tcgen05 tensor cores (decode_tc.cu): every format, D 128 or 256, G in {1, 2, 4, 8}
 cudaError_t decode_tc_launch(int D, int G, int grid, int fmt, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -24,16 +24,20 @@ __global__ void __launch_bounds__(128) verify_expand_kernel(const VerifyParams p
     const int r = blockIdx.x;
     if (threadIdx.x == 0) {
         int lo = 0, hi = p.B - 1;   // the last b with cu[b] <= r
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (p.cu[mid] <= r) lo = mid;
-            else hi = mid - 1;
+        if (p.cu) {
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (p.cu[mid] <= r) lo = mid;
+                else hi = mid - 1;
+            }
+        } else {
+            lo = r / p.W_fixed;     // windows of the same length: rows b W .. b W + W - 1
         }
         s_b = lo;
     }
     __syncthreads();
     const int b = s_b;
-    const int c0 = p.cu[b], W = p.cu[b + 1] - c0, j = r - c0;
+    const int c0 = p.cu ? p.cu[b] : b * p.W_fixed, W = p.cu ? p.cu[b + 1] - c0 : p.W_fixed, j = r - c0;
     int L = p.seq_lens[b];
     const int Lmax = p.max_pages * kPage;
     if (threadIdx.x == 0) {

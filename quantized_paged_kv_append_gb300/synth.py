@@ -19,7 +19,7 @@ _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 
 _STREAMS = {"q": 1, "k": 2, "v": 3, "outlier": 4, "perm": 5, "quat": 6, "lens": 7,
-            "k_new": 8, "v_new": 9, "misc": 10, "q_ext": 11, "k_ext": 12, "v_ext": 13, "q_verify": 14}
+            "k_new": 8, "v_new": 9, "misc": 10, "q_ext": 11, "k_ext": 12, "v_ext": 13, "q_verify": 14, "q_verify_fixed": 15}
 
 
 def _mix(z: np.ndarray) -> np.ndarray:

@@ -41,7 +41,7 @@ def _run(torch, qkv, w, pool, out_dtype=None, table=None, lens=None, workspace=N
 SMALL = [
     # fmt, D, Hkv, Hq
     ("int8", 256, 2, 16), ("int8", 128, 2, 8), ("int8", 256, 4, 4), ("int8", 256, 1, 2),
-    ("int8", 256, 2, 32), ("k8v4", 256, 2, 16), ("k8v4", 256, 1, 4),
+    ("int8", 256, 2, 32), ("int8", 128, 1, 16), ("k8v4", 256, 2, 16), ("k8v4", 256, 1, 4),
     ("iso3", 128, 4, 16), ("iso4", 128, 4, 16), ("iso3", 256, 2, 16), ("iso4", 256, 2, 4),
     ("iso4", 128, 2, 2),
     ("q4", 256, 2, 16), ("q4", 256, 1, 4), ("k8vbf16", 256, 2, 16), ("k8vbf16", 128, 4, 16),
