@@ -441,6 +441,8 @@ DECODE_CONFIGS = {
     "q4_128k": dict(fmt="q4", HQ=16, HKV=2, D=256, L=131072),
     "k8vbf16_128k": dict(fmt="k8vbf16", HQ=16, HKV=2, D=256, L=131072),
     "kbf16v8_128k": dict(fmt="kbf16v8", HQ=16, HKV=2, D=256, L=131072),
+    # 16 query heads per KV head: one 16-column pass over the int8 cache
+    "int8_128k_hq32": dict(fmt="int8", HQ=32, HKV=2, D=256, L=131072),
 }
 
 

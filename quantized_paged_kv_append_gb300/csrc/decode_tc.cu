@@ -1116,11 +1116,13 @@ __global__ void __launch_bounds__(kThr, 1)
             fence_proxy_async();
             soft_sync();
             if (r == 0) mbar_arrive(&bars[B_QRD]);
-            float bias[NA][G];
+            // the offset sums in registers (16 columns: read from shared memory each tile, for room)
+            constexpr int GB = G > 8 ? 1 : G;
+            float bias[NA][GB];
 #pragma unroll
             for (int g = 0; g < NA; ++g)
 #pragma unroll
-                for (int h = 0; h < G; ++h) bias[g][h] = bias_s[g * QH + h];
+                for (int h = 0; h < GB; ++h) bias[g][h] = bias_s[g * QH + h];
 
             float m[G], l[G];
 #pragma unroll
@@ -1174,7 +1176,7 @@ __global__ void __launch_bounds__(kThr, 1)
                         for (int h = 0; h < G; ++h) s[h] += ks[g] * ((v[h] + v[8 + h]) + (v2[h] + v2[8 + h]));
                     } else {
 #pragma unroll
-                        for (int h = 0; h < G; ++h) s[h] += ks[g] * (v[h] - bias[g][h]);
+                        for (int h = 0; h < G; ++h) s[h] += ks[g] * (v[h] - (G > 8 ? bias_s[g * QH + h] : bias[g][h < GB ? h : 0]));
                     }
                 }
                 tc_fence_before();

@@ -69,6 +69,7 @@ def test_decode_small_ragged(env, orc, fmt, d, hkv, hq):
     ("q4", 256, 2, 16, 131072),
     ("k8vbf16", 256, 2, 16, 65536),
     ("kbf16v8", 256, 2, 16, 65536),
+    ("int8", 256, 2, 32, 65536),     # 16 query heads per KV head: one 16-column pass (V scales folded)
 ])
 def test_decode_full_size(env, orc, fmt, d, hkv, hq, L):
     torch, qkv = env
