@@ -34,11 +34,11 @@ B, HQ, HKV, D, L = 1, 16, 2, 256, 131072
 LAYERS = 8   # default; --layers overrides
 LAUNCHES_PER_STEP = 2   # int8 decode: the tensor-core kernel and the split-merge (combine) kernel
 KV_BYTES_PER_TOKEN = 2 * HKV * (D + 2 * D // 64)        # int8 codes + fp16 scales, K and V: 1056
-# dram__bytes_read.sum + dram__bytes_write.sum of one decode_tc_kernel<256,8,0> launch at this workload,
-# from an ncu capture of the current kernel build (138.58 MB read + 3.19 MB written)
-NCU_TRAFFIC_BYTES = 141_770_752
+# dram__bytes_read.sum + dram__bytes_write.sum of one decode_tc_kernel<256,8,0,false> launch at this
+# workload, from an ncu capture of the current kernel build (138.58 MB read + 3.35 MB written)
+NCU_TRAFFIC_BYTES = 141_926_144
 # the same counters for the other decode workloads where a capture of the current kernel exists
-WORKLOAD_NCU_TRAFFIC = {"iso4_82k": 44_712_192}
+WORKLOAD_NCU_TRAFFIC = {}
 DECODE_BYTES = L * KV_BYTES_PER_TOKEN                     # 138,412,032 packed bytes read per step
 WORKLOAD = ("int8 KV decode at 128K context: batch 1, 16 q heads / 2 KV heads, head_dim 256, "
             "131072 cached tokens, page 16, shuffled page table; step = quantize-on-write of 1 token + decode")
