@@ -391,16 +391,33 @@ __global__ void __launch_bounds__(kThr, 1)
     // kernel is still what the copies after the wait read) and, after the wait, load the page
     // ids of the first piece at once; those are kept only if the piece that the share read
     // after the wait gives is the same. Every value the kernel uses is loaded after the wait.
+    // The share itself is kept too: with at most 128 sequences every lane holds its (up to 4)
+    // seq_lens values as read here, and after the wait the warp compares them with a fresh read;
+    // if none changed (and the first piece's own length read agrees), the share and the first
+    // piece stand and the post-wait prefix scan and divisions are skipped.
     Piece spc;
     spc.b = -1;
     int spid_cur = 0, spid_nxt = 0;
+    const int per_lane = (p.B + 31) / 32;
+    const bool sfast = per_lane <= 4;
+    int slen[4] = {0, 0, 0, 0};
+    int b0s = 0;
+    long long pref0s = 0, Tus = 0, begs = 0, ends = 0;
+    bool shas = false;
     {
-        int b0s;
-        long long pref0s, Tus;
-        compute_share([&](int b) { return __ldcg(p.seq_lens + b); }, false, b0s, pref0s, Tus);
-        bool shas = false;
+        const int b_lo = min(p.B, lane * per_lane);
+        if (sfast) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (i < per_lane && b_lo + i < p.B) slen[i] = __ldcg(p.seq_lens + b_lo + i);
+        }
+        auto pick = [&](int i) { return i == 0 ? slen[0] : i == 1 ? slen[1] : i == 2 ? slen[2] : slen[3]; };
+        if (sfast) compute_share([&](int b) { return pick(b - b_lo); }, false, b0s, pref0s, Tus);
+        else compute_share([&](int b) { return __ldcg(p.seq_lens + b); }, false, b0s, pref0s, Tus);
+        begs = Tus * c / C;
+        ends = Tus * (c + 1) / C;
         if (warp == kWProd || warp == kWProdV || warp < kSoftW) {
-            Walker ws{b0s, pref0s, Tus * c / C, Tus * (c + 1) / C};
+            Walker ws{b0s, pref0s, begs, ends};
             shas = ws.template next<true>(p, spc);
         }
         if (shas && (warp == kWProd || warp == kWProdV)) {
@@ -436,10 +453,30 @@ __global__ void __launch_bounds__(kThr, 1)
             spc.b = -1;
         }
     }
+    // validate the share read before the wait (see above); warp 0 also flags bad lengths here
+    bool fast = false;
+    if (sfast && shas && spc.b == b0s) {
+        const int b_lo = min(p.B, lane * per_lane);
+        bool same = true;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (i < per_lane && b_lo + i < p.B) {
+                const int Lr = p.seq_lens[b_lo + i];
+                same &= Lr == slen[i];
+                if (warp == 0 && (Lr < 0 || Lr > p.max_pages * kPage || (VW && Lr < p.W))) atomicOr(&g_err_dtc, kErrPos);
+            }
+        fast = __all_sync(0xffffffffu, same) && spc.L == seq_len_clamped(p, spc.b);
+    }
     int b0;
     long long pref0, Tunits;
-    compute_share([&](int b) { return p.seq_lens[b]; }, true, b0, pref0, Tunits);
-    const long long beg = Tunits * c / C, end = Tunits * (c + 1) / C;
+    if (fast) {
+        b0 = b0s;
+        pref0 = pref0s;
+        Tunits = Tus;
+    } else {
+        compute_share([&](int b) { return p.seq_lens[b]; }, true, b0, pref0, Tunits);
+    }
+    const long long beg = fast ? begs : Tunits * c / C, end = fast ? ends : Tunits * (c + 1) / C;
     auto cta_of = [&](long long x) -> long long { return ((x + 1) * C + Tunits - 1) / Tunits - 1; };
 
     // empty sequences: zero rows, written by CTA (s mod C)
@@ -451,7 +488,16 @@ __global__ void __launch_bounds__(kThr, 1)
             for (int i = tid; i < G * D; i += kThr) write_out<D, G, VW>(p, b, kvh, hgi * G, i, 0.0f);
         }
     }
+    // the piece iterator; with a validated share its first piece is spc, already worked out
     Walker walker{b0, pref0, beg, end};
+    if (fast) walker = Walker{spc.b, pref0s, spc.soff + spc.p1, end};
+    auto first_piece = [&](Piece& pc) -> bool {
+        if (fast) {
+            pc = spc;
+            return true;
+        }
+        return walker.next(p, pc);
+    };
 
     if (warp == kWProd || warp == kWProdV) {
         // ============================ producers (K, V) ============================
@@ -482,7 +528,7 @@ __global__ void __launch_bounds__(kThr, 1)
         uint32_t T = 0, pat_phase = 0;
         Piece pc;
         bool first = true;
-        while (walker.next(p, pc)) {
+        for (bool have = first_piece(pc); have; have = walker.next(p, pc)) {
             const int kvh = pc.hg / (p.Gv / G);
             const int32_t* ptrow = p.page_table + (size_t)pc.b * p.max_pages;
             const int last_page = (pc.L - 1) / kPage;
@@ -885,7 +931,7 @@ __global__ void __launch_bounds__(kThr, 1)
         };
         uint32_t T = 0;
         Piece pc;
-        while (walker.next(p, pc)) {
+        for (bool have = first_piece(pc); have; have = walker.next(p, pc)) {
             for (int pg0 = pc.p0; pg0 < pc.p1; pg0 += kTP, ++T) {
                 const int buf = X::KSTB == 2 ? (int)(T & 1) : 0;
                 // ---- K of tile T: exact fp16 1152 + c (int8), q - 8 (q4) or the bf16 values, one
@@ -1002,7 +1048,7 @@ __global__ void __launch_bounds__(kThr, 1)
         float* sML = red_l + 4 * QH;                                             // M[QH], L[QH]
         uint32_t T = 0, piece = 0;
         Piece pc;
-        while (walker.next(p, pc)) {
+        for (bool have = first_piece(pc); have; have = walker.next(p, pc)) {
             const int kvh = pc.hg / (p.Gv / G), gv0 = (pc.hg % (p.Gv / G)) * G;   // KV head, first virtual head
             // ---- query tile (B operand, K-major, dims in converter order) and the offset sums ----
             {
