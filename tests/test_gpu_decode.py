@@ -211,3 +211,35 @@ def test_decode_fused_quantize_on_write(env, orc, fmt, d, hkv, hq, lens):
         assert np.array_equal(got, want), nm
     r = compare_attention(out.cpu().numpy(), ref)
     assert r["ok"], r
+
+
+def test_decode_seq_lens_changed_in_stream(env, orc):
+    """The kernel works out its share of the units from seq_lens before its dependency wait
+    and keeps it only if a read after the wait finds seq_lens unchanged. Here a kernel
+    earlier in the same stream rewrites seq_lens before every decode call (and one call
+    follows another decode directly): each call must attend exactly its own lengths."""
+    torch, qkv = env
+    full = [900, 37, 2100, 16]
+    w = Workload("int8", full, 2, 16, 256, seed=23)
+    pool = w.oracle_pool(orc)
+    cache = gpu_cache(qkv, w, torch, planes=pool.planes())
+    t = to_dev(w.table, torch)
+    q = bf16_dev(w.q, torch)
+    steps = [np.array(full, np.int32) - d for d in (0, 5, 15, 9)]
+    sl = to_dev(steps[0], torch)
+    outs = []
+    for i, lens in enumerate(steps):
+        if i % 2 == 1:
+            # a device-side rewrite of seq_lens in the same stream just before the call
+            sl.copy_(torch.from_numpy(lens).cuda(non_blocking=False))
+        else:
+            sl.sub_(torch.from_numpy(steps[i - 1] - lens if i else np.zeros_like(lens)).cuda())
+        outs.append(qkv.decode(cache, q, t, sl, max(full), scale=w.scale, out_dtype=torch.float32))
+        outs.append(qkv.decode(cache, q, t, sl, max(full), scale=w.scale, out_dtype=torch.float32))
+    torch.cuda.synchronize()
+    assert qkv.device_error() == 0
+    for i, lens in enumerate(steps):
+        ref = pool.decode(w.q, w.table, lens, w.scale)
+        for o in outs[2 * i:2 * i + 2]:
+            r = compare_attention(o.cpu().numpy(), ref)
+            assert r["ok"], (i, r)
