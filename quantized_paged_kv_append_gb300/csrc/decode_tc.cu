@@ -455,7 +455,8 @@ __global__ void __launch_bounds__(kThr, 1)
     }
     // validate the share read before the wait (see above); warp 0 also flags bad lengths here
     bool fast = false;
-    if (sfast && shas && spc.b == b0s) {
+    // (the verify-window instantiations skip it: their 16-column softmax has no registers to spare)
+    if (!VW && sfast && shas && spc.b == b0s) {
         const int b_lo = min(p.B, lane * per_lane);
         bool same = true;
 #pragma unroll
