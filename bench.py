@@ -35,8 +35,8 @@ LAYERS = 8   # default; --layers overrides
 LAUNCHES_PER_STEP = 2   # int8 decode: the tensor-core kernel and the split-merge (combine) kernel
 KV_BYTES_PER_TOKEN = 2 * HKV * (D + 2 * D // 64)        # int8 codes + fp16 scales, K and V: 1056
 # dram__bytes_read.sum + dram__bytes_write.sum of one decode_tc_kernel<256,8,0,false> launch at this
-# workload, from an ncu capture of the current kernel build (138.58 MB read + 3.35 MB written)
-NCU_TRAFFIC_BYTES = 141_926_144
+# workload, from an ncu capture of the current kernel build (138.59 MB read + 2.97 MB written)
+NCU_TRAFFIC_BYTES = 141_555_456
 # the same counters for the other decode workloads where a capture of the current kernel exists
 WORKLOAD_NCU_TRAFFIC = {}
 DECODE_BYTES = L * KV_BYTES_PER_TOKEN                     # 138,412,032 packed bytes read per step
