@@ -122,6 +122,23 @@ def test_verify_validation_rejects_before_launch(qlib):
     assert v(C.byref(_desc(qlib)), cu=None) == -1
 
 
+def test_verify_fixed_validation_rejects_before_launch(qlib):
+    L = qlib.lib()
+    P = C.c_void_p
+    good = P(1 << 20)
+    v = lambda desc, B=1, W=2, q=good: L.kv_verify_attn_fixed(desc, q, B, W, 16, good, good, 4, 64, 0.0625, good, 0,
+                                                              good, 1 << 30, None)
+    assert v(None) == -1
+    assert v(C.byref(_desc(qlib, fmt=7))) == -5
+    assert v(C.byref(_desc(qlib)), W=0) == -1          # a window of at least one query
+    assert v(C.byref(_desc(qlib)), B=-1) == -1
+    assert v(C.byref(_desc(qlib)), B=0) == 0           # no-op
+    assert v(C.byref(_desc(qlib, fmt=1)), B=0) == 0    # no-op (the expanded path)
+    assert v(C.byref(_desc(qlib)), B=600, W=2) == -8   # more query rows than one decode call takes
+    assert L.kv_verify_fixed_workspace_size(C.byref(_desc(qlib)), 1, 0, 16, 4) == 0
+    assert L.kv_verify_fixed_workspace_size(C.byref(_desc(qlib)), 1, 2, 16, 0) == 0
+
+
 def test_strerror_covers_codes(qlib):
     L = qlib.lib()
     for code in range(-8, 1):
