@@ -1,6 +1,7 @@
 // decode_tc.cu -- paged decode attention over a quantized KV cache (int8, k8v4,
-// ISO3, ISO4) on tcgen05 tensor cores (TMEM accumulators), with the newest
-// token's quantize-on-write fused in.
+// ISO3, ISO4, q4_0 for both stores, one-store int8 with the other store bf16) on
+// tcgen05 tensor cores (TMEM accumulators), with the newest token's
+// quantize-on-write fused in, and the verify window of speculative decoding.
 //
 // Method (page title, section): "qwen35/q36: --kv - int8 K/V caches", "What it
 // does" (int8 K/V planes, one fp16 absmax/127 scale per 64 values, dequantized on
@@ -27,9 +28,9 @@
 //   * warp 13 (one thread) issues tcgen05.mma: S_g = K'_g Q_g^T per 64-dim
 //     scale group g (M = 128 tokens, N = 16 query columns; 16 MMAs per tile at
 //     D = 256) and O += P'^T V' (M = 64 P' columns: 16 per scale group = 8
-//     heads hi + lo, N = D, K = 16 tokens; 8 MMAs per tile). Small MMAs cost
-//     about the same issue time whatever their N, so the tile is laid out to
-//     need as few instructions as possible;
+//     heads hi + lo, N = D, K = 16 tokens; 8 MMAs per tile). An MMA costs at
+//     least ~52 cycles of tensor pipe whatever its N (N <= 64) or M, so the
+//     tile is laid out to need as few instructions as possible;
 //   * warps 0-3 (softmax) own one token each: they combine the group scores in
 //     fp32 with the exact K scales (removing the 1152 offset through the query
 //     sums), run a lazy online softmax (the frame max moves only when a score
@@ -39,7 +40,12 @@
 //     fp16((q - 8) * d) (the block scale folded into V', so P' carries none)
 //     and rotates each piece's O back by the FWHT-256; ISO turns code pairs into
 //     fp16 level pairs through a per-lane table, takes the query rotated by the
-//     pool quaternion as fp16 hi + lo tiles, and rotates O back per 4-D group;
+//     pool quaternion as fp16 hi + lo columns, and rotates O back per 4-D group;
+//   * int8 with 16 query columns (16 heads per KV head, or a verify window's
+//     queries as "virtual heads"): all N = 16 columns of the query tile are
+//     heads, the V scales are folded into V' as for k8v4, and P' holds 16 heads
+//     hi + lo; the verify window (VW) is a template flag with its own
+//     instantiations (per-column causal lengths, query rows b W + w);
 //   * pieces that do not cover a whole sequence write a partial slot (m, l, O) to
 //     the caller's workspace; a second kernel (decode_tc_combine), launched with
 //     programmatic stream serialization, merges them.
