@@ -859,7 +859,7 @@ def main():
     if args.impl == "reference":
         if args.steps > 10:
             args.steps = 10   # each oracle step is seconds of CPU work
-        args.warmup = min(args.warmup, 1)
+        args.warmup = min(args.warmup, 3)
         run_reference(args)
     else:
         run_gpu(args)
